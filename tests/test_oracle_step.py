@@ -1,0 +1,107 @@
+"""Pins for oracle.step: dense equivalence (torch SDPA), append, prefetch and lookahead properties."""
+import numpy as np
+import torch
+
+import workload as W
+from oracle import OracleDecoder, bf16_to_f32, index_keys
+
+
+def _sdpa(q_rows, k_tok, v_tok, scale):
+    g = q_rows.shape[0]
+    tq = torch.from_numpy(bf16_to_f32(q_rows).astype(np.float64))[None, :, None, :]
+    tk = torch.from_numpy(bf16_to_f32(k_tok).astype(np.float64))[None, None].expand(1, g, -1, -1)
+    tv = torch.from_numpy(bf16_to_f32(v_tok).astype(np.float64))[None, None].expand(1, g, -1, -1)
+    return torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=scale)[0, :, 0].numpy()
+
+
+SMALL = W.TINY.with_(name="small", ctx0=1000, steps=4, budget_blocks=8, cap_blocks=12, n_heavy=8)
+
+
+def test_budget_covering_context_is_dense_attention():
+    w = SMALL.with_(budget_blocks=64, cap_blocks=64)      # 1000 tokens = 63 blocks <= 64
+    k, v = W.kv_numpy(w)
+    dec = OracleDecoder(w, k, v, [w.ctx0])
+    qs = W.QueryStream(w)
+    for t in range(3):
+        q = qs.queries(t)
+        out, recs = dec.step(q)
+        for h in range(w.n_kv_head):
+            heads = slice(h * w.group, (h + 1) * w.group)
+            ref = _sdpa(q[0, 0, heads], k[0, 0, h, : w.ctx0], v[0, 0, h, : w.ctx0], w.softmax_scale)
+            np.testing.assert_allclose(out[0, 0, heads], ref, atol=1e-6, rtol=0)
+            assert recs[(0, 0, h)].sel.tolist() == list(range(63))
+
+
+def test_ragged_tail_and_capacity_do_not_change_outputs():
+    w = SMALL.with_(ctx0=1000)
+    k, v = W.kv_numpy(w)
+    qs1, qs2 = W.QueryStream(w), W.QueryStream(w)
+    d1 = OracleDecoder(w, k, v, [997])                               # ragged: 997 = 62*16 + 5
+    d2 = OracleDecoder(w.with_(cap_blocks=40), k, v, [997])
+    for t in range(4):
+        o1, r1 = d1.step(qs1.queries(t))
+        o2, r2 = d2.step(qs2.queries(t))
+        np.testing.assert_array_equal(o1, o2)
+        for u in r1:
+            assert r1[u].sel.tolist() == r2[u].sel.tolist()
+            assert max(r1[u].sel) <= 62
+
+
+def test_append_updates_last_block_key_and_length():
+    w = SMALL.with_(append=True, ctx0=1000, steps=20)
+    k, v = W.kv_numpy(w)
+    dec = OracleDecoder(w, k, v, [w.ctx0])
+    qs = W.QueryStream(w)
+    full_k = k.copy()
+    for t in range(20):
+        nk, nv = W.token(w, w.ctx0 + t)
+        full_k[:, :, :, w.ctx0 + t] = nk
+        dec.step(qs.queries(t), new_k=nk, new_v=nv)
+        L = w.ctx0 + t + 1
+        assert dec.L[0] == L
+        for h in range(w.n_kv_head):
+            nb = (L + 15) // 16
+            np.testing.assert_array_equal(dec.ik[(0, 0, h)][:nb], index_keys(full_k[0, 0, h], L, 16))
+            # the recent blocks (which hold the new token) are always selected
+            assert nb - 1 in dec.records[(0, 0, h)].sel
+
+
+def test_prefetch_never_changes_outputs():
+    w = SMALL.with_(n_layer=3, layer_prefetch=True, rho_layer=0.8, cap_blocks=14)
+    k, v = W.kv_numpy(w)
+    a = OracleDecoder(w, k, v, [w.ctx0])
+    b = OracleDecoder(w.with_(layer_prefetch=False), k, v, [w.ctx0])
+    qa, qb = W.QueryStream(w), W.QueryStream(w)
+    total_pf = 0
+    for t in range(4):
+        oa, ra = a.step(qa.queries(t))
+        ob, rb = b.step(qb.queries(t))
+        np.testing.assert_array_equal(oa, ob)
+        for u, rec in ra.items():
+            assert rec.sel.tolist() == rb[u].sel.tolist()
+            if u[0] > 0:
+                assert len(rec.prefetch.blocks) <= a.max_prefetch
+                total_pf += len(rec.prefetch.blocks)
+        st = a.stats()
+        for l in st:
+            assert st[l]["hits"] + st[l]["misses"] == sum(len(ra[u].sel) for u in ra if u[0] == l)
+    assert total_pf > 0
+
+
+def test_lookahead_pins_attention_set():
+    w = SMALL.with_(lookahead=True, n_draft=4)
+    k, v = W.kv_numpy(w)
+    dec = OracleDecoder(w, k, v, [w.ctx0])
+    qs = W.QueryStream(w)
+    prev = None
+    for t in range(5):
+        out, recs = dec.step(qs.queries(t), qs.drafts(t))
+        for u, rec in recs.items():
+            if t == 0:
+                assert rec.boot is not None
+            else:
+                assert rec.boot is None and rec.attn_sel.tolist() == prev[u].tolist()
+            if not rec.update.pin_fallback:
+                assert set(rec.attn_sel.tolist()) <= dec.cache[u].resident()
+            assert set(rec.sel.tolist()) <= dec.cache[u].resident()
+        prev = {u: rec.sel for u, rec in recs.items()}

@@ -1,0 +1,314 @@
+"""Seeded synthetic workloads for the sparse KV-cache decode step.
+
+This package draws the inputs (host K/V history, queries, draft queries, appended
+tokens) that both the CPU oracle and the CUDA path consume.  It contains no part of
+the decode method's arithmetic.  The random numbers come from ``kvs_gen.c``
+(counter-based SplitMix64 + Box-Muller, bf16 round-to-nearest-even).
+
+Workload shapes follow the pages' workloads (sources: the tuntang.top survey of
+speculative KV sparsity, section 1 "Llama3.1-8B, 32K" and section 2.2 "2048-token
+budget"; the HiSparse promo page, "fixed GPU cache + host KV"; the jiusizaji KV-cache
+overview, section 2.3 "MLA d_c = 512").  No dataset is used.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+from dataclasses import dataclass, field, replace
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvs_gen.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libkvs_gen.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the generator shared library in-tree (gcc, no FMA contraction)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-shared", "-fPIC", "-pthread",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _KVParams(ctypes.Structure):
+    _fields_ = [("seed", ctypes.c_uint64),
+                ("n_req", ctypes.c_int32), ("n_layer", ctypes.c_int32), ("n_kv_head", ctypes.c_int32),
+                ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
+                ("ctx0", ctypes.c_int32), ("n_heavy", ctypes.c_int32),
+                ("max_ctx", ctypes.c_int64),
+                ("heavy_scale", ctypes.c_float),
+                ("heavy_shared_layers", ctypes.c_int32),
+                ("rho_layer", ctypes.c_double),
+                ("n_threads", ctypes.c_int32)]
+
+
+class _QParams(ctypes.Structure):
+    _fields_ = [("seed", ctypes.c_uint64),
+                ("n_req", ctypes.c_int32), ("n_layer", ctypes.c_int32), ("n_q_head", ctypes.c_int32),
+                ("d", ctypes.c_int32),
+                ("rho", ctypes.c_double), ("rho_layer", ctypes.c_double)]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = ctypes.CDLL(build())
+            P = ctypes.POINTER
+            _lib.kvs_gen_fill_kv.argtypes = [P(_KVParams), ctypes.c_void_p, ctypes.c_void_p]
+            _lib.kvs_gen_token.argtypes = [P(_KVParams), ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+            _lib.kvs_gen_heavy_positions.argtypes = [P(_KVParams), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_void_p]
+            _lib.kvs_gen_q_advance.argtypes = [P(_QParams), ctypes.c_void_p, ctypes.c_int64]
+            _lib.kvs_gen_q_values.argtypes = [P(_QParams), ctypes.c_void_p, ctypes.c_void_p]
+            _lib.kvs_gen_q_values.restype = None
+            _lib.kvs_gen_to_bf16.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+            _lib.kvs_gen_to_bf16.restype = None
+            _lib.kvs_gen_draft.argtypes = [P(_QParams), ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                           ctypes.c_double, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_int64]
+            _lib.kvs_gen_uniform_f32.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                                 ctypes.c_float, ctypes.c_void_p]
+            _lib.kvs_gen_uniform_f32.restype = None
+            _lib.kvs_gen_randint.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_void_p]
+            _lib.kvs_gen_randint.restype = None
+        return _lib
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One synthetic decode workload.
+
+    Layouts (all row-major):
+      host K   [n_layer][n_req][n_kv_head][max_ctx][d_k]  bf16
+      host V   [n_layer][n_req][n_kv_head][max_ctx][d_v]  bf16 (absent when v_shares_k)
+      queries  [n_layer][n_req][n_q_head][d_k]            bf16, one array per step
+      drafts   [n_layer][n_req][n_draft][n_q_head][d_k]   bf16, one array per step
+    """
+    name: str
+    n_req: int
+    n_layer: int
+    n_q_head: int
+    n_kv_head: int
+    d_k: int
+    d_v: int
+    block_size: int
+    ctx0: int
+    steps: int
+    budget_blocks: int
+    n_sink: int
+    n_recent: int
+    cap_blocks: int
+    v_shares_k: bool = False
+    lookahead: bool = False
+    n_draft: int = 0
+    draft_sigma: float = 0.3
+    append: bool = False
+    layer_prefetch: bool = False
+    rho: float = 0.9
+    rho_layer: float = 0.0
+    n_heavy: int = 0
+    heavy_scale: float = 1.0
+    heavy_shared_layers: bool = False
+    seed: int = 0
+    notes: str = ""
+
+    @property
+    def group(self) -> int:
+        return self.n_q_head // self.n_kv_head
+
+    @property
+    def max_ctx(self) -> int:
+        return self.ctx0 + (self.steps if self.append else 0)
+
+    @property
+    def n_score_q(self) -> int:
+        return self.n_draft if self.lookahead else 1
+
+    @property
+    def max_blocks(self) -> int:
+        return (self.max_ctx + self.block_size - 1) // self.block_size
+
+    @property
+    def softmax_scale(self) -> float:
+        # fp32 value of 1/sqrt(d_k): the scale both sides receive as an input.
+        return float(np.float32(1.0 / math.sqrt(self.d_k)))
+
+    @property
+    def host_kv_bytes(self) -> int:
+        per_tok = self.d_k + (0 if self.v_shares_k else self.d_v)
+        return self.n_layer * self.n_req * self.n_kv_head * self.max_ctx * per_tok * 2
+
+    def kv_params(self, n_threads: int = 0) -> _KVParams:
+        return _KVParams(self.seed, self.n_req, self.n_layer, self.n_kv_head, self.d_k,
+                         0 if self.v_shares_k else self.d_v, self.ctx0, self.n_heavy, self.max_ctx,
+                         self.heavy_scale, 1 if self.heavy_shared_layers else 0, self.rho_layer, n_threads)
+
+    def q_params(self) -> _QParams:
+        return _QParams(self.seed, self.n_req, self.n_layer, self.n_q_head, self.d_k, self.rho, self.rho_layer)
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+def _heavy(frac: float, ctx: int) -> int:
+    return int(round(frac * ctx))
+
+
+# The five workloads.  Readings where the description leaves a value open are listed in
+# the design notes (sink/recent counts, cache capacity of the MLA case, rho of the 8B case).
+TINY = Workload(name="tiny", n_req=1, n_layer=1, n_q_head=8, n_kv_head=2, d_k=128, d_v=128, block_size=16,
+                ctx0=4096, steps=32, budget_blocks=16, n_sink=1, n_recent=2, cap_blocks=32, rho=0.9,
+                n_heavy=32, heavy_scale=4.0)
+
+LLAMA8B_32K = Workload(name="llama8b_32k_lookahead", n_req=8, n_layer=32, n_q_head=32, n_kv_head=8, d_k=128,
+                       d_v=128, block_size=16, ctx0=32768, steps=64, budget_blocks=128, n_sink=1, n_recent=2,
+                       cap_blocks=192, lookahead=True, n_draft=4, draft_sigma=0.3, rho=0.9,
+                       n_heavy=_heavy(0.01, 32768), heavy_scale=3.0)
+
+LONG_128K = Workload(name="llama8b_128k_append", n_req=4, n_layer=32, n_q_head=32, n_kv_head=8, d_k=128,
+                     d_v=128, block_size=16, ctx0=131072, steps=128, budget_blocks=128, n_sink=1, n_recent=2,
+                     cap_blocks=256, append=True, rho=0.95, n_heavy=_heavy(0.01, 131072), heavy_scale=3.0)
+
+MLA_128K = Workload(name="mla_128k_token_topk", n_req=16, n_layer=16, n_q_head=128, n_kv_head=1, d_k=576,
+                    d_v=512, v_shares_k=True, block_size=1, ctx0=131072, steps=32, budget_blocks=2048,
+                    n_sink=0, n_recent=0, cap_blocks=3072, layer_prefetch=True, rho=0.9, rho_layer=0.6,
+                    n_heavy=_heavy(0.01, 131072), heavy_scale=3.0, heavy_shared_layers=True)
+
+
+def sweep_workload(block_size: int, budget_tokens: int, rho: float, n_layer: int = 8) -> Workload:
+    """Budget/eviction sweep case: 8B shape, batch 32, context 65536, cache 1.25x budget.
+
+    32 layers would need 256 GiB of pinned host memory; the GPU host has 199 GB, so the
+    sweep runs with n_layer = 8 (64 GiB) by default."""
+    kb = budget_tokens // block_size
+    return Workload(name=f"sweep_bs{block_size}_b{budget_tokens}_rho{rho:g}", n_req=32, n_layer=n_layer,
+                    n_q_head=32, n_kv_head=8, d_k=128, d_v=128, block_size=block_size, ctx0=65536, steps=64,
+                    budget_blocks=kb, n_sink=1, n_recent=2, cap_blocks=(kb * 5) // 4, rho=rho,
+                    n_heavy=_heavy(0.01, 65536), heavy_scale=3.0)
+
+
+WORKLOADS = {w.name: w for w in (TINY, LLAMA8B_32K, LONG_128K, MLA_128K)}
+
+
+# --------------------------------------------------------------------------- fills
+
+def _ptr(a) -> int:
+    if isinstance(a, np.ndarray):
+        assert a.flags["C_CONTIGUOUS"]
+        return a.ctypes.data
+    return int(a.data_ptr())  # torch tensor (pinned host or otherwise)
+
+
+def fill_kv(w: Workload, k, v=None, n_threads: int = 0) -> None:
+    """Fill host K (and V) arrays of the documented layout; positions >= ctx0 are zero."""
+    p = w.kv_params(n_threads)
+    rc = lib().kvs_gen_fill_kv(ctypes.byref(p), _ptr(k), _ptr(v) if v is not None else None)
+    if rc != 0:
+        raise ValueError(f"kvs_gen_fill_kv failed ({rc}) for {w.name}")
+
+
+def kv_numpy(w: Workload, n_threads: int = 0):
+    """Host K, V as numpy uint16 (bf16 bit patterns); V is None when it shares the K row."""
+    k = np.empty((w.n_layer, w.n_req, w.n_kv_head, w.max_ctx, w.d_k), np.uint16)
+    v = None if w.v_shares_k else np.empty((w.n_layer, w.n_req, w.n_kv_head, w.max_ctx, w.d_v), np.uint16)
+    fill_kv(w, k, v, n_threads)
+    return k, v
+
+
+def token(w: Workload, pos: int):
+    """The token appended at position pos: K [n_layer][n_req][n_kv_head][d_k], V likewise (or None)."""
+    k = np.empty((w.n_layer, w.n_req, w.n_kv_head, w.d_k), np.uint16)
+    v = None if w.v_shares_k else np.empty((w.n_layer, w.n_req, w.n_kv_head, w.d_v), np.uint16)
+    p = w.kv_params()
+    rc = lib().kvs_gen_token(ctypes.byref(p), pos, k.ctypes.data, v.ctypes.data if v is not None else None)
+    if rc != 0:
+        raise ValueError("kvs_gen_token failed")
+    return k, v
+
+
+def heavy_positions(w: Workload, req: int, layer: int, head: int) -> np.ndarray:
+    out = np.empty(max(w.ctx0, 1), np.int32)
+    p = w.kv_params()
+    n = lib().kvs_gen_heavy_positions(ctypes.byref(p), req, layer, head, out.ctypes.data)
+    return out[:n]
+
+
+def uniform_f32(seed: int, stream: int, n: int, lo: float, hi: float) -> np.ndarray:
+    out = np.empty(n, np.float32)
+    lib().kvs_gen_uniform_f32(seed, stream, n, lo, hi, out.ctypes.data)
+    return out
+
+
+def randint(seed: int, stream: int, n: int, high: int) -> np.ndarray:
+    out = np.empty(n, np.int64)
+    lib().kvs_gen_randint(seed, stream, n, high, out.ctypes.data)
+    return out
+
+
+class QueryStream:
+    """Per-step queries and draft queries of a workload.
+
+    q_t follows an AR(1) over steps per (layer, req, head): q_0 = e_0,
+    q_t = rho q_{t-1} + sqrt(1 - rho^2) e_t (fp64, stored bf16).  Draft j of step t is
+    q_{t+j} + N(0, sigma^2), j = 1..n_draft (lookahead drafts predict the next positions)."""
+
+    def __init__(self, w: Workload):
+        self.w = w
+        self.p = w.q_params()
+        self.n = w.n_layer * w.n_req * w.n_q_head * w.d_k
+        self._base = {}   # t -> fp64 base state
+        self._last_t = -1
+        self._state = np.zeros(self.n, np.float64)
+
+    def _base_at(self, t: int) -> np.ndarray:
+        if t in self._base:
+            return self._base[t]
+        if t < self._last_t:
+            raise ValueError("QueryStream only moves forward")
+        while self._last_t < t:
+            self._last_t += 1
+            rc = lib().kvs_gen_q_advance(ctypes.byref(self.p), self._state.ctypes.data, self._last_t)
+            if rc != 0:
+                raise ValueError("kvs_gen_q_advance failed")
+            self._base[self._last_t] = self._state.copy()
+        keep = self.w.n_draft + 2
+        for old in [k for k in self._base if k < self._last_t - keep]:
+            del self._base[old]
+        return self._base[t]
+
+    def _values(self, t: int) -> np.ndarray:
+        q = np.empty(self.n, np.float64)
+        lib().kvs_gen_q_values(ctypes.byref(self.p), self._base_at(t).ctypes.data, q.ctypes.data)
+        return q
+
+    def queries(self, t: int) -> np.ndarray:
+        w = self.w
+        q = self._values(t)
+        out = np.empty((w.n_layer, w.n_req, w.n_q_head, w.d_k), np.uint16)
+        lib().kvs_gen_to_bf16(q.ctypes.data, q.size, out.ctypes.data)
+        return out
+
+    def drafts(self, t: int) -> np.ndarray:
+        w = self.w
+        nd = w.n_draft
+        out = np.empty((w.n_layer, w.n_req, nd, w.n_q_head, w.d_k), np.uint16)
+        for j in range(1, nd + 1):
+            qf = self._values(t + j)
+            sub = out[:, :, j - 1]
+            rc = lib().kvs_gen_draft(ctypes.byref(self.p), qf.ctypes.data, t, j, w.draft_sigma,
+                                     sub.ctypes.data, out.strides[0] // 2, out.strides[1] // 2,
+                                     out.strides[3] // 2)
+            if rc != 0:
+                raise ValueError("kvs_gen_draft failed")
+        return out
