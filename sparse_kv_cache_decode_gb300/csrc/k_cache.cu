@@ -1,0 +1,395 @@
+// GPU working-set cache of each (request, layer, kv-head) unit: hit detection, the delta of
+// missing blocks, least-recently-used victims under the capacity cap, slot assignment and
+// stamps (one CTA per unit, so the state of a unit has a single writer), the cross-layer
+// prefetch, and the zero-copy host -> slot fetch of the blocks each of them maps.
+//
+// Stamps are assigned, never incremented: every block of a selection gets 2*clock, a prefetched
+// block 2*clock + 1, so the (stamp, slot) order is deterministic.
+#include "kvs_block.cuh"
+#include "kvs_common.cuh"
+#include "kvs_ptx.cuh"
+
+#include <algorithm>
+
+namespace kvs {
+
+namespace {
+
+constexpr int kCacheThreads = 512;
+
+struct CacheSmem {
+  uint8_t* flags;     // [C]  bit 0: holds a selected (or hint) block, bit 1: pinned
+  uint32_t* lt_key;   // [MV] victims strictly below the threshold key (slot order)
+  int* lt_slot;       // [MV]
+  int* vict;          // [MV] victim slots in LRU order
+  int* list_blk;      // [Kb] misses (update) or non-resident hint blocks (prefetch), ascending
+  int* list_pos;      // [Kb] position of each miss in the selection
+  int* sos;           // [Kb] slot of each selected block
+};
+
+__host__ __device__ inline int max_victims(const Dims& d) { return d.Kb > d.max_prefetch ? d.Kb : d.max_prefetch; }
+
+__host__ __device__ inline size_t cache_smem_bytes(const Dims& d) {
+  size_t mv = (size_t)max_victims(d);
+  return ((size_t)d.C + 15) / 16 * 16 + mv * 12 + (size_t)d.Kb * 12;
+}
+
+__device__ CacheSmem carve(unsigned char* base, const Dims& d) {
+  CacheSmem s;
+  size_t mv = (size_t)max_victims(d);
+  s.flags = base;
+  base += ((size_t)d.C + 15) / 16 * 16;
+  s.lt_key = reinterpret_cast<uint32_t*>(base); base += mv * 4;
+  s.lt_slot = reinterpret_cast<int*>(base); base += mv * 4;
+  s.vict = reinterpret_cast<int*>(base); base += mv * 4;
+  s.list_blk = reinterpret_cast<int*>(base); base += (size_t)d.Kb * 4;
+  s.list_pos = reinterpret_cast<int*>(base); base += (size_t)d.Kb * 4;
+  s.sos = reinterpret_cast<int*>(base);
+  return s;
+}
+
+// The m eligible slots with the smallest (key, slot), in that order, into vict[0 .. m).
+// Requires m <= number of eligible slots.
+template <class Elig, class Key>
+__device__ void select_victims(int C, int m, Elig elig, Key key, int* hist, int* ws, int* pick, CacheSmem& sm) {
+  const int tid = threadIdx.x, NT = blockDim.x;
+  if (m <= 0) return;
+  uint32_t prefix = 0, mask = 0;
+  int remaining = m;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 256; i += NT) hist[i] = 0;
+    __syncthreads();
+    for (int s = tid; s < C; s += NT) {
+      if (!elig(s)) continue;
+      uint32_t k = key(s);
+      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (tid < 32) radix_pick_digit(hist, remaining, false, pick);
+    __syncthreads();
+    prefix |= (uint32_t)pick[0] << shift;
+    mask |= 255u << shift;
+    remaining -= pick[1];
+    __syncthreads();
+  }
+  const uint32_t T = prefix;
+  const int need_eq = remaining, n_lt = m - remaining;
+  const int per = (C + NT - 1) / NT;
+  const int s0 = min(C, tid * per), s1 = min(C, s0 + per);
+  int my_lt = 0, my_eq = 0;
+  for (int s = s0; s < s1; ++s) {
+    if (!elig(s)) continue;
+    uint32_t k = key(s);
+    my_lt += k < T;
+    my_eq += k == T;
+  }
+  int tot;
+  int lt_pos = block_excl_sum(my_lt, ws, &tot);
+  int eq_pos = block_excl_sum(my_eq, ws, &tot);
+  for (int s = s0; s < s1; ++s) {
+    if (!elig(s)) continue;
+    uint32_t k = key(s);
+    if (k < T) { sm.lt_key[lt_pos] = k; sm.lt_slot[lt_pos] = s; ++lt_pos; }
+    else if (k == T) { if (eq_pos < need_eq) sm.vict[n_lt + eq_pos] = s; ++eq_pos; }
+  }
+  __syncthreads();
+  // entries below T are in slot order: rank = #smaller keys + #equal keys earlier in slot order
+  for (int i = tid; i < n_lt; i += NT) {
+    uint32_t k = sm.lt_key[i];
+    int rank = 0;
+    for (int j = 0; j < n_lt; ++j) {
+      uint32_t kj = sm.lt_key[j];
+      rank += (kj < k) || (kj == k && j < i);
+    }
+    sm.vict[rank] = sm.lt_slot[i];
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ unsigned long long fetch_rows(const Dims& d, int len, int b) {
+  return (unsigned long long)min(d.bs, len - b * d.bs);
+}
+
+__global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Layer L, const int* __restrict__ sel,
+                                                                     const int* __restrict__ nsel,
+                                                                     const int* __restrict__ ctx_len,
+                                                                     int* __restrict__ slot_of_sel, kvs_stats* stats) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  __shared__ int hist[256];
+  __shared__ int ws[33];
+  __shared__ int pick[2];
+  __shared__ unsigned s_now;
+  __shared__ int s_bad;
+  __shared__ unsigned long long s_cnt[4];  // hits, prefetch hits, evictions, bytes
+  CacheSmem sm = carve(smraw, d);
+  const int u = blockIdx.x, r = u / d.Hkv;
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int len = ctx_len[r];
+  const int n = nsel[u];
+  const int nb = n_blocks_of(len, d.bs);
+  if (len < 0 || len > d.max_ctx || n < 0 || n > d.Kb) {
+    if (tid == 0) set_error(L.err, KVS_ERR_BAD_INDEX);
+    return;
+  }
+  const int* su = sel + (size_t)u * d.Kb;
+  int* b2s = L.block2slot + (size_t)u * d.nb_max;
+  int* s2b = L.slot2block + (size_t)u * d.C;
+  unsigned* st = L.stamp + (size_t)u * d.C;
+  if (tid == 0) {
+    unsigned clk = L.clock[u] + 1u;
+    L.clock[u] = clk;
+    s_now = 2u * clk;
+    s_bad = 0;
+  }
+  if (tid < 4) s_cnt[tid] = 0;
+  for (int s = tid; s < d.C; s += NT) sm.flags[s] = 0;
+  __syncthreads();
+  const unsigned now = s_now;
+
+  // hits and misses, misses compacted in selection (ascending block) order
+  const int per = (n + NT - 1) / NT;
+  const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+  int my_miss = 0;
+  unsigned long long my_pfh = 0;
+  for (int i = i0; i < i1; ++i) {
+    int b = su[i];
+    if (b < 0 || b >= nb) { s_bad = 1; continue; }
+    int s = b2s[b];
+    if (s >= d.C) { s_bad = 1; continue; }
+    if (s >= 0) {
+      sm.flags[s] = 1;
+      sm.sos[i] = s;
+      my_pfh += st[s] == now - 1u;
+    } else {
+      ++my_miss;
+    }
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) set_error(L.err, KVS_ERR_BAD_INDEX);
+    return;
+  }
+  int m;
+  int mpos = block_excl_sum(my_miss, ws, &m);
+  for (int i = i0; i < i1; ++i) {
+    int b = su[i];
+    if (b2s[b] < 0) { sm.list_blk[mpos] = b; sm.list_pos[mpos] = i; ++mpos; }
+  }
+  const bool pinned = d.lookahead && L.pend_n[u] >= 0;
+  if (pinned) {
+    const int np = L.pend_n[u];
+    for (int i = tid; i < np && i < d.Kb; i += NT) {
+      int s = L.pend_slot[(size_t)u * d.Kb + i];
+      if (s >= 0 && s < d.C) sm.flags[s] |= 2;
+    }
+  }
+  if (my_pfh) atomicAdd(&s_cnt[1], my_pfh);
+  __syncthreads();
+
+  int my_el = 0, my_el_nopin = 0;
+  for (int s = tid; s < d.C; s += NT) {
+    my_el += sm.flags[s] == 0;
+    my_el_nopin += (sm.flags[s] & 1) == 0;
+  }
+  int n_el, n_el_nopin;
+  block_excl_sum(my_el, ws, &n_el);
+  block_excl_sum(my_el_nopin, ws, &n_el_nopin);
+  bool fallback = false;
+  if (n_el < m && pinned) { fallback = true; n_el = n_el_nopin; }
+  if (n_el < m) {
+    if (tid == 0) set_error(L.err, KVS_ERR_CAPACITY);
+    return;
+  }
+  const uint8_t emask = fallback ? 1 : 3;
+  select_victims(
+      d.C, m, [&](int s) { return (sm.flags[s] & emask) == 0; },
+      [&](int s) { return s2b[s] < 0 ? 0u : st[s]; }, hist, ws, pick, sm);
+
+  unsigned long long my_ev = 0, my_bytes = 0;
+  for (int j = tid; j < m; j += NT) {
+    int b = sm.list_blk[j], s = sm.vict[j];
+    int old = s2b[s];
+    if (old >= 0 && old < d.nb_max) { b2s[old] = -1; ++my_ev; }
+    s2b[s] = b;
+    b2s[b] = s;
+    sm.sos[sm.list_pos[j]] = s;
+    L.fetch_blk[(size_t)u * d.C + j] = b;
+    L.fetch_slot[(size_t)u * d.C + j] = s;
+    my_bytes += fetch_rows(d, len, b) * (unsigned long long)d.row_bytes;
+  }
+  if (my_ev) atomicAdd(&s_cnt[2], my_ev);
+  if (my_bytes) atomicAdd(&s_cnt[3], my_bytes);
+  __syncthreads();
+  for (int i = tid; i < n; i += NT) {
+    int s = sm.sos[i];
+    st[s] = now;
+    slot_of_sel[(size_t)u * d.Kb + i] = s;
+    if (d.lookahead) {
+      L.pend_sel[(size_t)u * d.Kb + i] = su[i];
+      L.pend_slot[(size_t)u * d.Kb + i] = s;
+    }
+  }
+  if (tid == 0) {
+    L.n_fetch[u] = m;
+    if (d.lookahead) L.pend_n[u] = n;
+    if (stats) {
+      kvs_stats* sl = stats + L.layer;
+      atomicAdd(&sl->hits, (unsigned long long)(n - m));
+      atomicAdd(&sl->misses, (unsigned long long)m);
+      atomicAdd(&sl->prefetch_hits, s_cnt[1]);
+      atomicAdd(&sl->evictions, s_cnt[2]);
+      atomicAdd(&sl->bytes_fetched, s_cnt[3]);
+      if (fallback) atomicAdd(&sl->pin_fallbacks, 1ull);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kCacheThreads) prefetch_kernel(Dims d, Layer L, const int* __restrict__ hint,
+                                                                 const int* __restrict__ hint_n,
+                                                                 const int* __restrict__ ctx_len, kvs_stats* stats) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  __shared__ int hist[256];
+  __shared__ int ws[33];
+  __shared__ int pick[2];
+  __shared__ int s_bad;
+  __shared__ unsigned long long s_cnt[2];  // evictions, bytes
+  CacheSmem sm = carve(smraw, d);
+  const int u = blockIdx.x, r = u / d.Hkv;
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int len = ctx_len[r];
+  const int nh = hint_n[u];
+  const int nb = n_blocks_of(len, d.bs);
+  if (len < 0 || len > d.max_ctx || nh < 0 || nh > d.Kb) {
+    if (tid == 0) set_error(L.err, KVS_ERR_BAD_INDEX);
+    return;
+  }
+  const int* hu = hint + (size_t)u * d.Kb;
+  int* b2s = L.block2slot + (size_t)u * d.nb_max;
+  int* s2b = L.slot2block + (size_t)u * d.C;
+  unsigned* st = L.stamp + (size_t)u * d.C;
+  const unsigned clk = L.clock[u];
+  const unsigned tag = 2u * clk + 1u, last_use = 2u * clk;
+  if (tid == 0) s_bad = 0;
+  if (tid < 2) s_cnt[tid] = 0;
+  for (int s = tid; s < d.C; s += NT) sm.flags[s] = 0;
+  __syncthreads();
+  const int per = (nh + NT - 1) / NT;
+  const int i0 = min(nh, tid * per), i1 = min(nh, i0 + per);
+  int my_nr = 0;
+  for (int i = i0; i < i1; ++i) {
+    int b = hu[i];
+    if (b < 0 || b >= nb) { s_bad = 1; continue; }
+    int s = b2s[b];
+    if (s >= d.C) { s_bad = 1; continue; }
+    if (s >= 0) sm.flags[s] = 1; else ++my_nr;
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) set_error(L.err, KVS_ERR_BAD_INDEX);
+    return;
+  }
+  int n_nr;
+  int pos = block_excl_sum(my_nr, ws, &n_nr);
+  for (int i = i0; i < i1; ++i) {
+    int b = hu[i];
+    if (b2s[b] < 0) sm.list_blk[pos++] = b;
+  }
+  auto elig = [&](int s) { return s2b[s] < 0 || (st[s] < last_use && sm.flags[s] == 0); };
+  int my_el = 0;
+  for (int s = tid; s < d.C; s += NT) my_el += elig(s);
+  int n_el;
+  block_excl_sum(my_el, ws, &n_el);
+  const int k = min(min(n_nr, d.max_prefetch), n_el);
+  select_victims(d.C, k, elig, [&](int s) { return s2b[s] < 0 ? 0u : st[s]; }, hist, ws, pick, sm);
+  unsigned long long my_ev = 0, my_bytes = 0;
+  for (int j = tid; j < k; j += NT) {
+    int b = sm.list_blk[j], s = sm.vict[j];
+    int old = s2b[s];
+    if (old >= 0 && old < d.nb_max) { b2s[old] = -1; ++my_ev; }
+    s2b[s] = b;
+    b2s[b] = s;
+    st[s] = tag;
+    L.fetch_blk[(size_t)u * d.C + j] = b;
+    L.fetch_slot[(size_t)u * d.C + j] = s;
+    my_bytes += fetch_rows(d, len, b) * (unsigned long long)d.row_bytes;
+  }
+  if (my_ev) atomicAdd(&s_cnt[0], my_ev);
+  if (my_bytes) atomicAdd(&s_cnt[1], my_bytes);
+  __syncthreads();
+  if (tid == 0) {
+    L.n_fetch[u] = k;
+    if (stats) {
+      kvs_stats* sl = stats + L.layer;
+      atomicAdd(&sl->prefetched, (unsigned long long)k);
+      atomicAdd(&sl->evictions, s_cnt[0]);
+      atomicAdd(&sl->bytes_fetched, s_cnt[1]);
+    }
+  }
+}
+
+// Zero-copy fetch: warps walk the (unit, item) list; each item copies the present rows of one
+// block from the mapped host history into its slot with 16-byte loads, 4 in flight per lane.
+__device__ __forceinline__ void copy_rows(const uint4* __restrict__ src, uint4* __restrict__ dst, int nvec, int lane) {
+  int v = lane;
+  for (; v + 96 < nvec; v += 128) {
+    uint4 a = src[v], b = src[v + 32], c = src[v + 64], e = src[v + 96];
+    dst[v] = a; dst[v + 32] = b; dst[v + 64] = c; dst[v + 96] = e;
+  }
+  for (; v < nvec; v += 32) dst[v] = src[v];
+}
+
+__global__ void __launch_bounds__(256) fetch_kernel(Dims d, Layer L, const int* __restrict__ ctx_len, int max_items) {
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long total = (long long)d.U * max_items;
+  for (long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += nwarps) {
+    const int u = (int)(w / max_items), j = (int)(w % max_items);
+    if (j >= L.n_fetch[u]) continue;
+    const int b = L.fetch_blk[(size_t)u * d.C + j], s = L.fetch_slot[(size_t)u * d.C + j];
+    const int len = ctx_len[u / d.Hkv];
+    const int rows = min(d.bs, len - b * d.bs);
+    if (rows <= 0) continue;
+    const size_t t0 = (size_t)u * d.max_ctx + (size_t)b * d.bs;
+    const size_t slot_row = ((size_t)u * d.C + s) * d.bs;
+    copy_rows(reinterpret_cast<const uint4*>(L.host_k + t0 * d.dk), reinterpret_cast<uint4*>(L.kpool + slot_row * d.dk),
+              rows * d.dk / 8, lane);
+    if (!d.v_shares_k)
+      copy_rows(reinterpret_cast<const uint4*>(L.host_v + t0 * d.dv),
+                reinterpret_cast<uint4*>(L.vpool + slot_row * d.dv), rows * d.dv / 8, lane);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_cache_update(const Dims& d, const Layer& L, const int* sel, const int* nsel, const int* ctx_len,
+                                int* slot_of_sel, kvs_stats* stats, cudaStream_t s) {
+  size_t smem = cache_smem_bytes(d);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(cache_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cache_update_kernel<<<d.U, kCacheThreads, smem, s>>>(d, L, sel, nsel, ctx_len, slot_of_sel, stats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefetch(const Dims& d, const Layer& L, const int* hint, const int* hint_n, const int* ctx_len,
+                            kvs_stats* stats, cudaStream_t s) {
+  size_t smem = cache_smem_bytes(d);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(prefetch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  prefetch_kernel<<<d.U, kCacheThreads, smem, s>>>(d, L, hint, hint_n, ctx_len, stats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fetch(const Dims& d, const Layer& L, const int* ctx_len, cudaStream_t s) {
+  int max_items = max_victims(d);
+  long long warps = (long long)d.U * max_items;
+  int blocks = (int)std::min<long long>((warps + 7) / 8, 8 * 152);
+  fetch_kernel<<<blocks, 256, 0, s>>>(d, L, ctx_len, max_items);
+  return cudaGetLastError();
+}
+
+}  // namespace kvs

@@ -1,0 +1,129 @@
+// Index keys (block means of the keys) and the per-step append of one token.
+#include "kvs_common.cuh"
+#include "kvs_ptx.cuh"
+
+namespace kvs {
+
+// One warp per block: lanes own 4 consecutive dims at a time; tokens are summed in fp32 one at
+// a time in ascending position, divided by the present-token count (IEEE) and rounded to bf16
+// (round-to-nearest-even).
+template <int CHUNKS>  // 4-dim chunks per lane = ceil(dk / 128)
+__global__ void __launch_bounds__(256) index_build_kernel(Dims d, Layer L, __nv_bfloat16* __restrict__ index,
+                                                          const int* __restrict__ ctx_len) {
+  const int u = blockIdx.y;
+  const int r = u / d.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x * 8 + warp;
+  const int len = ctx_len[r];
+  if (len < 0 || len > d.max_ctx) {
+    if (threadIdx.x == 0) set_error(L.err, KVS_ERR_BAD_INDEX);
+    return;
+  }
+  const int nb = n_blocks_of(len, d.bs);
+  if (b >= nb) return;
+  const int t0 = b * d.bs, t1 = min(t0 + d.bs, len);
+  const int nchunk = d.dk / 4;
+  const __nv_bfloat16* rows = L.host_k + (size_t)u * d.max_ctx * d.dk;
+  float acc[CHUNKS][4];
+#pragma unroll
+  for (int c = 0; c < CHUNKS; ++c)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[c][e] = 0.f;
+  for (int t = t0; t < t1; ++t) {
+    const uint2* row = reinterpret_cast<const uint2*>(rows + (size_t)t * d.dk);
+#pragma unroll
+    for (int c = 0; c < CHUNKS; ++c) {
+      int ch = lane + 32 * c;
+      if (ch < nchunk) {
+        uint2 v = row[ch];
+        acc[c][0] = __fadd_rn(acc[c][0], bf16_lo(v.x));
+        acc[c][1] = __fadd_rn(acc[c][1], bf16_hi(v.x));
+        acc[c][2] = __fadd_rn(acc[c][2], bf16_lo(v.y));
+        acc[c][3] = __fadd_rn(acc[c][3], bf16_hi(v.y));
+      }
+    }
+  }
+  const float n = (float)(t1 - t0);
+  uint2* out = reinterpret_cast<uint2*>(index + ((size_t)u * d.nb_max + b) * d.dk);
+#pragma unroll
+  for (int c = 0; c < CHUNKS; ++c) {
+    int ch = lane + 32 * c;
+    if (ch < nchunk) {
+      uint2 o;
+      o.x = pack_bf16x2(__fdiv_rn(acc[c][0], n), __fdiv_rn(acc[c][1], n));
+      o.y = pack_bf16x2(__fdiv_rn(acc[c][2], n), __fdiv_rn(acc[c][3], n));
+      out[ch] = o;
+    }
+  }
+}
+
+cudaError_t launch_index_build(const Dims& d, const Layer& L, __nv_bfloat16* index, const int* ctx_len,
+                               cudaStream_t s) {
+  dim3 grid((d.nb_max + 7) / 8, d.U);
+  int chunks = (d.dk / 4 + 31) / 32;
+  if (chunks <= 1) index_build_kernel<1><<<grid, 256, 0, s>>>(d, L, index, ctx_len);
+  else if (chunks <= 2) index_build_kernel<2><<<grid, 256, 0, s>>>(d, L, index, ctx_len);
+  else if (chunks <= 5) index_build_kernel<5><<<grid, 256, 0, s>>>(d, L, index, ctx_len);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+// One CTA per unit.  Writes the token at position len-1 to the host history and, when its block
+// is resident, to the block's slot; then recomputes the block's index key from its present
+// tokens, taking the new token's values from k_new (not read back from host memory).
+__global__ void __launch_bounds__(128) append_kernel(Dims d, Layer L, const __nv_bfloat16* __restrict__ k_new,
+                                                     const __nv_bfloat16* __restrict__ v_new,
+                                                     __nv_bfloat16* __restrict__ index,
+                                                     const int* __restrict__ ctx_len) {
+  const int u = blockIdx.x;
+  const int r = u / d.Hkv;
+  const int len = ctx_len[r];
+  if (len < 1 || len > d.max_ctx) {
+    if (threadIdx.x == 0) set_error(L.err, KVS_ERR_BAD_INDEX);
+    return;
+  }
+  const int p = len - 1;
+  const int b = p / d.bs, row_in_blk = p - b * d.bs;
+  const int slot = L.block2slot[(size_t)u * d.nb_max + b];
+  __nv_bfloat16* hk = const_cast<__nv_bfloat16*>(L.host_k) + ((size_t)u * d.max_ctx + p) * d.dk;
+  const __nv_bfloat16* kn = k_new + (size_t)u * d.dk;
+  for (int i = threadIdx.x; i < d.dk; i += blockDim.x) {
+    hk[i] = kn[i];
+    if (slot >= 0) L.kpool[(((size_t)u * d.C + slot) * d.bs + row_in_blk) * d.dk + i] = kn[i];
+  }
+  if (!d.v_shares_k) {
+    __nv_bfloat16* hv = const_cast<__nv_bfloat16*>(L.host_v) + ((size_t)u * d.max_ctx + p) * d.dv;
+    const __nv_bfloat16* vn = v_new + (size_t)u * d.dv;
+    for (int i = threadIdx.x; i < d.dv; i += blockDim.x) {
+      hv[i] = vn[i];
+      if (slot >= 0) L.vpool[(((size_t)u * d.C + slot) * d.bs + row_in_blk) * d.dv + i] = vn[i];
+    }
+  }
+  // index key of block b over tokens [b*bs, len)
+  const __nv_bfloat16* rows = L.host_k + (size_t)u * d.max_ctx * d.dk;
+  const float n = (float)(len - b * d.bs);
+  for (int i = threadIdx.x; i < d.dk; i += blockDim.x) {
+    float acc = 0.f;
+    for (int t = b * d.bs; t < p; ++t) acc = __fadd_rn(acc, __bfloat162float(rows[(size_t)t * d.dk + i]));
+    acc = __fadd_rn(acc, __bfloat162float(kn[i]));
+    index[((size_t)u * d.nb_max + b) * d.dk + i] = __float2bfloat16_rn(__fdiv_rn(acc, n));
+  }
+}
+
+cudaError_t launch_append(const Dims& d, const Layer& L, const __nv_bfloat16* k_new, const __nv_bfloat16* v_new,
+                          __nv_bfloat16* index, const int* ctx_len, cudaStream_t s) {
+  append_kernel<<<d.U, 128, 0, s>>>(d, L, k_new, v_new, index, ctx_len);
+  return cudaGetLastError();
+}
+
+__global__ void advance_kernel(int B, int* ctx_len) {
+  int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r < B) ctx_len[r] += 1;
+}
+
+cudaError_t launch_advance(int B, int* ctx_len, cudaStream_t s) {
+  advance_kernel<<<(B + 127) / 128, 128, 0, s>>>(B, ctx_len);
+  return cudaGetLastError();
+}
+
+}  // namespace kvs

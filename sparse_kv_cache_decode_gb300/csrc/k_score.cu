@@ -1,0 +1,199 @@
+// Block scoring: s[b] = scale * max over the unit's scoring rows r of (q_r . ik[b]).
+//
+// Tensor-core tile (m16n8k16, bf16 in, fp32 accumulate): A = 16 index keys (blocks) x 16 dims,
+// B = 16 dims x 8 scoring rows.  The scoring rows of unit (request, kv-head h) are the q heads
+// of group h for every scoring query j (row = j * G + g).  Rows are kept in shared memory for the
+// whole CTA; index tiles stream through per-warp double buffers with cp.async.  The max over
+// rows is taken in registers and across the 4 lanes of a quad.
+#include <float.h>
+
+#include "kvs_common.cuh"
+#include "kvs_ptx.cuh"
+
+namespace kvs {
+
+namespace {
+
+constexpr int kScoreMaxRows = 128;
+
+struct ScoreSmem {
+  int rows_pad;     // scoring rows rounded up to 16
+  int row_stride;   // bytes per smem row (dk * 2 + 16 pad: conflict-free ldmatrix)
+  int nwarps;
+  size_t bytes() const { return (size_t)rows_pad * row_stride + (size_t)nwarps * 2 * 16 * row_stride; }
+};
+
+template <int DK, int NP>  // NP = number of n8 tiles of scoring rows (rows_pad / 8)
+__global__ void __launch_bounds__(128) score_kernel(Dims d, const __nv_bfloat16* __restrict__ index,
+                                                    const __nv_bfloat16* __restrict__ q, int nq,
+                                                    const int* __restrict__ ctx_len, float* __restrict__ scores,
+                                                    int tiles_per_cta, unsigned* err) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int RS = DK * 2 + 16;  // row stride in bytes
+  constexpr int KSTEPS = DK / 16;
+  constexpr int CH = DK * 2 / 16;  // 16-byte chunks per row
+  const int u = blockIdx.y;
+  const int r = u / d.Hkv, h = u % d.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  const int len = ctx_len[r];
+  if (len < 0 || len > d.max_ctx) {
+    if (threadIdx.x == 0) set_error(err, KVS_ERR_BAD_INDEX);
+    return;
+  }
+  const int nb = n_blocks_of(len, d.bs);
+  const int n_tiles = (nb + 15) / 16;
+  const int tile0 = blockIdx.x * tiles_per_cta;
+  const int tile1 = min(n_tiles, tile0 + tiles_per_cta);
+  if (tile0 >= tile1) return;
+  const int R = nq * d.G;
+
+  // scoring rows -> smem (zero rows beyond R)
+  unsigned char* qs = smem;
+  for (int i = threadIdx.x; i < NP * 8 * CH; i += blockDim.x) {
+    int row = i / CH, ch = i % CH;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (row < R) {
+      int j = row / d.G, g = row % d.G;
+      const uint4* src = reinterpret_cast<const uint4*>(q + (((size_t)r * nq + j) * d.Hq + h * d.G + g) * DK);
+      v = src[ch];
+    }
+    *reinterpret_cast<uint4*>(qs + row * RS + ch * 16) = v;
+  }
+  __syncthreads();
+
+  unsigned char* buf = smem + NP * 8 * RS + (size_t)warp * 2 * 16 * RS;
+  const __nv_bfloat16* ik = index + (size_t)u * d.nb_max * DK;
+
+  auto load_tile = [&](int tile, int stage) {
+    unsigned char* dst = buf + stage * 16 * RS;
+    for (int i = lane; i < 16 * CH; i += 32) {
+      int row = i / CH, ch = i % CH;
+      int b = tile * 16 + row;
+      const __nv_bfloat16* src = ik + (size_t)min(b, nb - 1) * DK + ch * 8;
+      cp_async16(dst + row * RS + ch * 16, src, b < nb ? 16 : 0);
+    }
+    cp_async_commit();
+  };
+
+  int my = tile0 + warp;
+  if (my < tile1) load_tile(my, 0);
+  int stage = 0;
+  for (; my < tile1; my += nwarps, stage ^= 1) {
+    int next = my + nwarps;
+    if (next < tile1) {
+      load_tile(next, stage ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncwarp();
+    const unsigned char* a_tile = buf + stage * 16 * RS;
+    float acc[NP][4];
+#pragma unroll
+    for (int n = 0; n < NP; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      // matrices: (rows 0-7, k 0-7), (rows 8-15, k 0-7), (rows 0-7, k 8-15), (rows 8-15, k 8-15)
+      {
+        int mrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+        int kcol = ks * 16 + (lane >> 4) * 8;
+        ldmatrix_x4(a0, a1, a2, a3, a_tile + mrow * RS + kcol * 2);
+      }
+#pragma unroll
+      for (int n = 0; n < NP; n += 2) {
+        if (n + 1 < NP) {
+          uint32_t b0, b1, b2, b3;
+          // matrices: (rows n0..+7, k 0-7), (rows n0..+7, k 8-15), (rows n0+8.., k 0-7), (rows n0+8.., k 8-15)
+          int qrow = n * 8 + (lane & 7) + (lane >> 4) * 8;
+          int kcol = ks * 16 + ((lane >> 3) & 1) * 8;
+          ldmatrix_x4(b0, b1, b2, b3, qs + qrow * RS + kcol * 2);
+          mma_bf16_16816(acc[n], a0, a1, a2, a3, b0, b1);
+          mma_bf16_16816(acc[n + 1], a0, a1, a2, a3, b2, b3);
+        } else {
+          uint32_t b0, b1;
+          int qrow = n * 8 + (lane & 7);
+          int kcol = ks * 16 + ((lane >> 3) & 1) * 8;
+          ldmatrix_x2(b0, b1, qs + qrow * RS + kcol * 2);
+          mma_bf16_16816(acc[n], a0, a1, a2, a3, b0, b1);
+        }
+      }
+    }
+    __syncwarp();
+    // max over valid scoring rows (columns)
+    float m_lo = -FLT_MAX, m_hi = -FLT_MAX;
+#pragma unroll
+    for (int n = 0; n < NP; ++n) {
+      int c0 = n * 8 + (lane & 3) * 2;
+      if (c0 < R) { m_lo = fmaxf(m_lo, acc[n][0]); m_hi = fmaxf(m_hi, acc[n][2]); }
+      if (c0 + 1 < R) { m_lo = fmaxf(m_lo, acc[n][1]); m_hi = fmaxf(m_hi, acc[n][3]); }
+    }
+    m_lo = fmaxf(m_lo, __shfl_xor_sync(0xffffffffu, m_lo, 1));
+    m_lo = fmaxf(m_lo, __shfl_xor_sync(0xffffffffu, m_lo, 2));
+    m_hi = fmaxf(m_hi, __shfl_xor_sync(0xffffffffu, m_hi, 1));
+    m_hi = fmaxf(m_hi, __shfl_xor_sync(0xffffffffu, m_hi, 2));
+    if ((lane & 3) == 0) {
+      int b_lo = my * 16 + (lane >> 2), b_hi = b_lo + 8;
+      float* out = scores + (size_t)u * d.nb_max;
+      if (b_lo < nb) out[b_lo] = __fmul_rn(d.scale, m_lo);
+      if (b_hi < nb) out[b_hi] = __fmul_rn(d.scale, m_hi);
+    }
+  }
+}
+
+template <int DK, int NP>
+cudaError_t launch_score_t(const Dims& d, const __nv_bfloat16* index, const __nv_bfloat16* q, int nq,
+                           const int* ctx_len, float* scores, unsigned* err, cudaStream_t s) {
+  int nwarps = (DK * 2 + 16) * (NP * 8 + 4 * 32) <= 200 * 1024 ? 4 : 2;
+  ScoreSmem sm{NP * 8, DK * 2 + 16, nwarps};
+  size_t bytes = sm.bytes();
+  auto kern = score_kernel<DK, NP>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int max_tiles = (d.nb_max + 15) / 16;
+  // about 2 waves of CTAs over 152 SMs, at least 4 tiles per warp
+  int ctas_per_unit = max(1, min((max_tiles + 4 * nwarps - 1) / (4 * nwarps), (2 * 152 + d.U - 1) / d.U));
+  int tiles_per_cta = (max_tiles + ctas_per_unit - 1) / ctas_per_unit;
+  dim3 grid(ctas_per_unit, d.U);
+  kern<<<grid, 32 * nwarps, bytes, s>>>(d, index, q, nq, ctx_len, scores, tiles_per_cta, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int score_supported(const Dims& d) {
+  return (d.dk == 128 || d.dk == 576) && d.max_nq * d.G <= kScoreMaxRows;
+}
+
+cudaError_t launch_score(const Dims& d, const __nv_bfloat16* index, const __nv_bfloat16* q, int nq,
+                             const int* ctx_len, float* scores, unsigned* err, cudaStream_t s) {
+  int R = nq * d.G;
+  int np = (R + 7) / 8;
+  if (np > 16 || nq < 1) return cudaErrorInvalidValue;
+  np = np <= 2 ? 2 : np <= 4 ? 4 : np <= 8 ? 8 : 16;  // padded rows are zero and masked out
+  if (d.dk == 128) {
+    switch (np) {
+      case 2: return launch_score_t<128, 2>(d, index, q, nq, ctx_len, scores, err, s);
+      case 4: return launch_score_t<128, 4>(d, index, q, nq, ctx_len, scores, err, s);
+      case 8: return launch_score_t<128, 8>(d, index, q, nq, ctx_len, scores, err, s);
+      case 16: return launch_score_t<128, 16>(d, index, q, nq, ctx_len, scores, err, s);
+      default: break;
+    }
+  } else if (d.dk == 576) {
+    switch (np) {
+      case 2: return launch_score_t<576, 2>(d, index, q, nq, ctx_len, scores, err, s);
+      case 4: return launch_score_t<576, 4>(d, index, q, nq, ctx_len, scores, err, s);
+      case 8: return launch_score_t<576, 8>(d, index, q, nq, ctx_len, scores, err, s);
+      case 16: return launch_score_t<576, 16>(d, index, q, nq, ctx_len, scores, err, s);
+      default: break;
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvs

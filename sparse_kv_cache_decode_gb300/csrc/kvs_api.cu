@@ -1,0 +1,504 @@
+// libkvs host side: configuration checks, workspace carving and the C-ABI entry points.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "kvs_common.cuh"
+
+using namespace kvs;
+
+struct kvs_ctx {
+  kvs_config cfg;
+  Dims d;
+  unsigned char* ws;
+  size_t ws_bytes;
+  std::vector<Layer> layers;
+  unsigned* err;
+  const __nv_bfloat16* host_k_dev;  // whole host history, device-mapped
+  const __nv_bfloat16* host_v_dev;
+  std::vector<int> booted;          // lookahead: layer has a pending selection
+  std::vector<cudaEvent_t> fetch_done;
+  std::vector<int> fetch_pending;
+  cudaEvent_t fork;
+  // diagnostics
+  unsigned long long launches = 0;
+  int timer_kernel = 0, timer_count = 0;
+  std::vector<cudaEvent_t> timer_start, timer_stop;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool fill_dims(const kvs_config* c, Dims* d) {
+  if (!c) return false;
+  if (c->n_req < 1 || c->n_layer < 1 || c->n_q_head < 1 || c->n_kv_head < 1) return false;
+  if (c->n_q_head % c->n_kv_head) return false;
+  if (c->n_req > 4096 || c->n_layer > 1024 || c->n_kv_head > 1024) return false;
+  if (c->d_k < 8 || c->d_k % 8 || c->d_v < 8 || c->d_v % 8) return false;
+  if (c->v_shares_k != 0 && c->v_shares_k != 1) return false;
+  if (c->v_shares_k && c->d_v > c->d_k) return false;
+  if (c->block_size < 1 || c->max_ctx < 1) return false;
+  if (c->budget_blocks < 1 || c->n_sink < 0 || c->n_recent < 0) return false;
+  if (c->n_sink + c->n_recent > c->budget_blocks) return false;
+  if (c->budget_blocks > 4096) return false;
+  if (c->cap_blocks < c->budget_blocks || c->cap_blocks > 8192) return false;
+  if (c->max_score_q < 1 || c->max_score_q > 64) return false;
+  if (c->lookahead != 0 && c->lookahead != 1) return false;
+  if (c->max_prefetch < 0 || c->max_prefetch > c->cap_blocks - c->budget_blocks) return false;
+  if (!(c->softmax_scale >= 0.f) || isinf(c->softmax_scale)) return false;
+  d->B = c->n_req;
+  d->NL = c->n_layer;
+  d->Hq = c->n_q_head;
+  d->Hkv = c->n_kv_head;
+  d->G = c->n_q_head / c->n_kv_head;
+  d->dk = c->d_k;
+  d->dv = c->d_v;
+  d->v_shares_k = c->v_shares_k;
+  d->bs = c->block_size;
+  d->max_ctx = c->max_ctx;
+  d->nb_max = (c->max_ctx + c->block_size - 1) / c->block_size;
+  d->Kb = c->budget_blocks;
+  d->n_sink = c->n_sink;
+  d->n_recent = c->n_recent;
+  d->C = c->cap_blocks;
+  d->max_nq = c->max_score_q;
+  d->lookahead = c->lookahead;
+  d->max_prefetch = c->max_prefetch ? c->max_prefetch : c->cap_blocks - c->budget_blocks;
+  d->U = c->n_req * c->n_kv_head;
+  d->scale = c->softmax_scale > 0.f ? c->softmax_scale : (float)(1.0 / sqrt((double)c->d_k));
+  d->timeout_us = c->wait_timeout_us ? c->wait_timeout_us : 20000u;
+  d->row_bytes = 2 * (c->d_k + (c->v_shares_k ? 0 : c->d_v));
+  return true;
+}
+
+// Byte sizes of the per-layer and shared workspace regions.
+struct Plan {
+  size_t kpool, vpool, b2s, s2b, stamp, clock, pend_sel, pend_slot, pend_n, sel, nsel, sos, fblk, fslot, nfetch;
+  size_t per_layer;
+  size_t err, scores, part, ml;
+  size_t total;
+};
+
+Plan plan_of(const Dims& d) {
+  Plan p;
+  size_t U = d.U;
+  p.kpool = align_up(U * d.C * d.bs * (size_t)d.dk * 2);
+  p.vpool = d.v_shares_k ? 0 : align_up(U * d.C * d.bs * (size_t)d.dv * 2);
+  p.b2s = align_up(U * d.nb_max * 4);
+  p.s2b = align_up(U * d.C * 4);
+  p.stamp = align_up(U * d.C * 4);
+  p.clock = align_up(U * 4);
+  p.pend_sel = align_up(U * d.Kb * 4);
+  p.pend_slot = align_up(U * d.Kb * 4);
+  p.pend_n = align_up(U * 4);
+  p.sel = align_up(U * d.Kb * 4);
+  p.nsel = align_up(U * 4);
+  p.sos = align_up(U * d.Kb * 4);
+  p.fblk = align_up(U * d.C * 4);
+  p.fslot = align_up(U * d.C * 4);
+  p.nfetch = align_up(U * 4);
+  p.per_layer = p.kpool + p.vpool + p.b2s + p.s2b + p.stamp + p.clock + p.pend_sel + p.pend_slot + p.pend_n + p.sel +
+                p.nsel + p.sos + p.fblk + p.fslot + p.nfetch;
+  p.err = align_up(16);
+  p.scores = align_up(U * d.nb_max * 4);
+  p.part = align_up(U * (size_t)kAttnSplitMax * d.G * d.dv * 4);
+  p.ml = align_up(U * (size_t)kAttnSplitMax * d.G * 2 * 4);
+  p.total = p.per_layer * d.NL + p.err + p.scores + p.part + p.ml;
+  return p;
+}
+
+inline kvs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVS_OK : KVS_ERR_CUDA; }
+
+inline bool layer_ok(const kvs_ctx* c, int layer) { return c && layer >= 0 && layer < c->d.NL; }
+
+// Brackets one launcher call with the armed timer's events and counts its kernels.
+template <class F>
+cudaError_t timed(kvs_ctx* c, int kernel, cudaStream_t s, int n_kernels, F&& launch) {
+  bool on = c->timer_kernel == kernel && c->timer_count < (int)c->timer_start.size();
+  cudaError_t e = cudaSuccess;
+  if (on) e = cudaEventRecord(c->timer_start[c->timer_count], s);
+  if (e == cudaSuccess) e = launch();
+  if (e == cudaSuccess && on) {
+    e = cudaEventRecord(c->timer_stop[c->timer_count], s);
+    ++c->timer_count;
+  }
+  if (e == cudaSuccess) c->launches += n_kernels;
+  return e;
+}
+
+int attn_kernels(const Dims& d) {
+  // attention kernel, plus the split combine when the selection is split across CTAs
+  int n_split = 1, bps = 0;
+  if (!attention_split(d, &n_split, &bps)) return 1;
+  return n_split > 1 ? 2 : 1;
+}
+
+inline cudaStream_t S(kvs_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char* kvs_version(void) { return "kvs 0.1 (sm_103a)"; }
+
+size_t kvs_workspace_bytes(const kvs_config* cfg) {
+  Dims d;
+  if (!fill_dims(cfg, &d)) return 0;
+  return plan_of(d).total;
+}
+
+kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace_bytes, kvs_ctx** out) {
+  if (!out) return KVS_ERR_INVALID_ARG;
+  *out = nullptr;
+  Dims d;
+  if (!fill_dims(cfg, &d)) return KVS_ERR_INVALID_ARG;
+  Plan p = plan_of(d);
+  if (!d_workspace || workspace_bytes < p.total || (reinterpret_cast<uintptr_t>(d_workspace) % kAlign))
+    return KVS_ERR_INVALID_ARG;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, d_workspace) != cudaSuccess || attr.type != cudaMemoryTypeDevice) {
+    cudaGetLastError();
+    return KVS_ERR_INVALID_ARG;
+  }
+  kvs_ctx* c = new (std::nothrow) kvs_ctx();
+  if (!c) return KVS_ERR_INVALID_ARG;
+  c->cfg = *cfg;
+  c->d = d;
+  c->ws = static_cast<unsigned char*>(d_workspace);
+  c->ws_bytes = workspace_bytes;
+  c->host_k_dev = c->host_v_dev = nullptr;
+  unsigned char* base = c->ws;
+  c->layers.resize(d.NL);
+  unsigned char* shared = base + p.per_layer * d.NL;
+  c->err = reinterpret_cast<unsigned*>(shared);
+  float* scores = reinterpret_cast<float*>(shared + p.err);
+  float* part = reinterpret_cast<float*>(shared + p.err + p.scores);
+  float* ml = reinterpret_cast<float*>(shared + p.err + p.scores + p.part);
+  for (int l = 0; l < d.NL; ++l) {
+    unsigned char* b = base + p.per_layer * l;
+    Layer& L = c->layers[l];
+    L.layer = l;
+    L.kpool = reinterpret_cast<__nv_bfloat16*>(b); b += p.kpool;
+    L.vpool = d.v_shares_k ? nullptr : reinterpret_cast<__nv_bfloat16*>(b); b += p.vpool;
+    L.block2slot = reinterpret_cast<int*>(b); b += p.b2s;
+    L.slot2block = reinterpret_cast<int*>(b); b += p.s2b;
+    L.stamp = reinterpret_cast<unsigned*>(b); b += p.stamp;
+    L.clock = reinterpret_cast<unsigned*>(b); b += p.clock;
+    L.pend_sel = reinterpret_cast<int*>(b); b += p.pend_sel;
+    L.pend_slot = reinterpret_cast<int*>(b); b += p.pend_slot;
+    L.pend_n = reinterpret_cast<int*>(b); b += p.pend_n;
+    L.sel = reinterpret_cast<int*>(b); b += p.sel;
+    L.nsel = reinterpret_cast<int*>(b); b += p.nsel;
+    L.slot_of_sel = reinterpret_cast<int*>(b); b += p.sos;
+    L.fetch_blk = reinterpret_cast<int*>(b); b += p.fblk;
+    L.fetch_slot = reinterpret_cast<int*>(b); b += p.fslot;
+    L.n_fetch = reinterpret_cast<int*>(b); b += p.nfetch;
+    L.scores = scores;
+    L.attn_part = part;
+    L.attn_ml = ml;
+    L.host_k = L.host_v = nullptr;
+    L.err = c->err;
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = cudaMemset(L.block2slot, 0xff, p.b2s);
+    if (e == cudaSuccess) e = cudaMemset(L.slot2block, 0xff, p.s2b);
+    if (e == cudaSuccess) e = cudaMemset(L.stamp, 0, p.stamp);
+    if (e == cudaSuccess) e = cudaMemset(L.clock, 0, p.clock);
+    if (e == cudaSuccess) e = cudaMemset(L.pend_n, 0xff, p.pend_n);
+    if (e == cudaSuccess) e = cudaMemset(L.n_fetch, 0, p.nfetch);
+    if (e != cudaSuccess) {
+      delete c;
+      return KVS_ERR_CUDA;
+    }
+  }
+  if (cudaMemset(c->err, 0, p.err) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    delete c;
+    return KVS_ERR_CUDA;
+  }
+  c->booted.assign(d.NL, 0);
+  c->fetch_done.assign(d.NL, nullptr);
+  c->fetch_pending.assign(d.NL, 0);
+  for (int l = 0; l < d.NL; ++l)
+    if (cudaEventCreateWithFlags(&c->fetch_done[l], cudaEventDisableTiming) != cudaSuccess) {
+      delete c;
+      return KVS_ERR_CUDA;
+    }
+  if (cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming) != cudaSuccess) {
+    delete c;
+    return KVS_ERR_CUDA;
+  }
+  *out = c;
+  return KVS_OK;
+}
+
+kvs_status kvs_kernel_timer_arm(kvs_ctx* c, int kernel, int capacity) {
+  if (!c || capacity < 0 || kernel < 0 || kernel > KVS_K_INDEX) return KVS_ERR_INVALID_ARG;
+  while ((int)c->timer_start.size() < capacity) {
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess) return KVS_ERR_CUDA;
+    if (cudaEventCreate(&b) != cudaSuccess) { cudaEventDestroy(a); return KVS_ERR_CUDA; }
+    c->timer_start.push_back(a);
+    c->timer_stop.push_back(b);
+  }
+  while ((int)c->timer_start.size() > capacity) {
+    cudaEventDestroy(c->timer_start.back()); c->timer_start.pop_back();
+    cudaEventDestroy(c->timer_stop.back()); c->timer_stop.pop_back();
+  }
+  c->timer_kernel = capacity ? kernel : 0;
+  c->timer_count = 0;
+  return KVS_OK;
+}
+
+kvs_status kvs_kernel_timer_read(kvs_ctx* c, double* total_ms, int* n_timed) {
+  if (!c || !total_ms || !n_timed) return KVS_ERR_INVALID_ARG;
+  double tot = 0.0;
+  for (int i = 0; i < c->timer_count; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(c->timer_stop[i]) != cudaSuccess) return KVS_ERR_CUDA;
+    if (cudaEventElapsedTime(&ms, c->timer_start[i], c->timer_stop[i]) != cudaSuccess) return KVS_ERR_CUDA;
+    tot += ms;
+  }
+  *total_ms = tot;
+  *n_timed = c->timer_count;
+  return KVS_OK;
+}
+
+unsigned long long kvs_launch_count(kvs_ctx* c) { return c ? c->launches : 0ull; }
+
+kvs_status kvs_destroy(kvs_ctx* c) {
+  if (!c) return KVS_ERR_INVALID_ARG;
+  for (cudaEvent_t e : c->timer_start) cudaEventDestroy(e);
+  for (cudaEvent_t e : c->timer_stop) cudaEventDestroy(e);
+  for (cudaEvent_t e : c->fetch_done)
+    if (e) cudaEventDestroy(e);
+  if (c->fork) cudaEventDestroy(c->fork);
+  delete c;
+  return KVS_OK;
+}
+
+kvs_status kvs_bind_host_kv(kvs_ctx* c, void* h_k, void* h_v) {
+  if (!c || !h_k) return KVS_ERR_INVALID_ARG;
+  if (c->d.v_shares_k ? h_v != nullptr : h_v == nullptr) return KVS_ERR_INVALID_ARG;
+  void* dk = nullptr;
+  void* dv = nullptr;
+  if (cudaHostGetDevicePointer(&dk, h_k, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return KVS_ERR_HOST_MEM;
+  }
+  if (h_v && cudaHostGetDevicePointer(&dv, h_v, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return KVS_ERR_HOST_MEM;
+  }
+  c->host_k_dev = static_cast<const __nv_bfloat16*>(dk);
+  c->host_v_dev = static_cast<const __nv_bfloat16*>(dv);
+  const Dims& d = c->d;
+  for (int l = 0; l < d.NL; ++l) {
+    size_t unit_rows = (size_t)d.U * d.max_ctx;
+    c->layers[l].host_k = c->host_k_dev + (size_t)l * unit_rows * d.dk;
+    c->layers[l].host_v = dv ? c->host_v_dev + (size_t)l * unit_rows * d.dv : nullptr;
+  }
+  return KVS_OK;
+}
+
+kvs_status kvs_index_build(kvs_ctx* c, int layer, void* d_index, const int* d_ctx_len, kvs_stream_t stream) {
+  if (!layer_ok(c, layer) || !d_index || !d_ctx_len) return KVS_ERR_INVALID_ARG;
+  if (!c->host_k_dev) return KVS_ERR_HOST_MEM;
+  const Dims& d = c->d;
+  __nv_bfloat16* idx = static_cast<__nv_bfloat16*>(d_index) + (size_t)layer * d.U * d.nb_max * d.dk;
+  return cuda_status(timed(c, KVS_K_INDEX, S(stream), 1, [&] { return launch_index_build(d, c->layers[layer], idx, d_ctx_len, S(stream)); }));
+}
+
+kvs_status kvs_score_blocks(kvs_ctx* c, int layer, const void* d_score_q, int nq, const void* d_index,
+                            const int* d_ctx_len, float* d_scores, kvs_stream_t stream) {
+  if (!layer_ok(c, layer) || !d_score_q || !d_index || !d_ctx_len || !d_scores) return KVS_ERR_INVALID_ARG;
+  const Dims& d = c->d;
+  if (nq < 1 || nq > d.max_nq) return KVS_ERR_INVALID_ARG;
+  if (!score_supported(d)) return KVS_ERR_NOT_SUPPORTED;
+  const __nv_bfloat16* idx = static_cast<const __nv_bfloat16*>(d_index) + (size_t)layer * d.U * d.nb_max * d.dk;
+  return cuda_status(timed(c, KVS_K_SCORE, S(stream), 1, [&] {
+    return launch_score(d, idx, static_cast<const __nv_bfloat16*>(d_score_q), nq, d_ctx_len, d_scores, c->err, S(stream));
+  }));
+}
+
+kvs_status kvs_topk_select(kvs_ctx* c, const float* d_scores, const int* d_ctx_len, int* d_sel, int* d_nsel,
+                           kvs_stream_t stream) {
+  if (!c || !d_scores || !d_ctx_len || !d_sel || !d_nsel) return KVS_ERR_INVALID_ARG;
+  return cuda_status(timed(c, KVS_K_TOPK, S(stream), 1, [&] { return launch_topk(c->d, d_scores, d_ctx_len, d_sel, d_nsel, c->err, S(stream)); }));
+}
+
+kvs_status kvs_cache_update(kvs_ctx* c, int layer, const int* d_sel, const int* d_nsel, const int* d_ctx_len,
+                            int* d_slot_of_sel, kvs_stats* d_stats, kvs_stream_t stream) {
+  if (!layer_ok(c, layer) || !d_sel || !d_nsel || !d_ctx_len || !d_slot_of_sel) return KVS_ERR_INVALID_ARG;
+  if (!c->host_k_dev) return KVS_ERR_HOST_MEM;
+  const Layer& L = c->layers[layer];
+  cudaError_t e = timed(c, KVS_K_UPDATE, S(stream), 1, [&] {
+    return launch_cache_update(c->d, L, d_sel, d_nsel, d_ctx_len, d_slot_of_sel, d_stats, S(stream));
+  });
+  if (e == cudaSuccess) e = timed(c, KVS_K_FETCH, S(stream), 1, [&] { return launch_fetch(c->d, L, d_ctx_len, S(stream)); });
+  return cuda_status(e);
+}
+
+kvs_status kvs_sparse_decode_attn(kvs_ctx* c, int layer, const void* d_q, const int* d_sel, const int* d_slot_of_sel,
+                                  const int* d_nsel, const int* d_ctx_len, float* d_out, kvs_stream_t stream) {
+  if (!layer_ok(c, layer) || !d_q || !d_sel || !d_slot_of_sel || !d_nsel || !d_ctx_len || !d_out)
+    return KVS_ERR_INVALID_ARG;
+  if (!attention_supported(c->d)) return KVS_ERR_NOT_SUPPORTED;
+  return cuda_status(timed(c, KVS_K_ATTN, S(stream), attn_kernels(c->d), [&] {
+    return launch_attention(c->d, c->layers[layer], static_cast<const __nv_bfloat16*>(d_q), d_sel, d_slot_of_sel, d_nsel,
+                            d_ctx_len, d_out, S(stream));
+  }));
+}
+
+kvs_status kvs_layer_prefetch(kvs_ctx* c, int dst_layer, const int* d_hint_sel, const int* d_hint_nsel,
+                              const int* d_ctx_len, kvs_stats* d_stats, kvs_stream_t stream) {
+  if (!layer_ok(c, dst_layer) || dst_layer < 1 || !d_hint_sel || !d_hint_nsel || !d_ctx_len)
+    return KVS_ERR_INVALID_ARG;
+  if (!c->host_k_dev) return KVS_ERR_HOST_MEM;
+  const Layer& L = c->layers[dst_layer];
+  cudaError_t e = timed(c, KVS_K_PREFETCH, S(stream), 1, [&] {
+    return launch_prefetch(c->d, L, d_hint_sel, d_hint_nsel, d_ctx_len, d_stats, S(stream));
+  });
+  if (e == cudaSuccess) e = timed(c, KVS_K_FETCH, S(stream), 1, [&] { return launch_fetch(c->d, L, d_ctx_len, S(stream)); });
+  return cuda_status(e);
+}
+
+kvs_status kvs_advance_ctx(kvs_ctx* c, int* d_ctx_len, kvs_stream_t stream) {
+  if (!c || !d_ctx_len) return KVS_ERR_INVALID_ARG;
+  return cuda_status(timed(c, 0, S(stream), 1, [&] { return launch_advance(c->d.B, d_ctx_len, S(stream)); }));
+}
+
+kvs_status kvs_append(kvs_ctx* c, int layer, const void* d_k_new, const void* d_v_new, void* d_index,
+                      const int* d_ctx_len, kvs_stream_t stream) {
+  if (!layer_ok(c, layer) || !d_k_new || !d_index || !d_ctx_len) return KVS_ERR_INVALID_ARG;
+  if (!c->d.v_shares_k && !d_v_new) return KVS_ERR_INVALID_ARG;
+  if (!c->host_k_dev) return KVS_ERR_HOST_MEM;
+  const Dims& d = c->d;
+  __nv_bfloat16* idx = static_cast<__nv_bfloat16*>(d_index) + (size_t)layer * d.U * d.nb_max * d.dk;
+  return cuda_status(timed(c, KVS_K_APPEND, S(stream), 1, [&] {
+    return launch_append(d, c->layers[layer], static_cast<const __nv_bfloat16*>(d_k_new),
+                         static_cast<const __nv_bfloat16*>(d_v_new), idx, d_ctx_len, S(stream));
+  }));
+}
+
+kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d_score_q, int nq,
+                           const void* d_k_new, const void* d_v_new, void* d_index, const int* d_ctx_len,
+                           float* d_out, kvs_stats* d_stats, int* d_sel_out, int* d_nsel_out, kvs_stream_t stream,
+                           kvs_stream_t copy_stream) {
+  if (!layer_ok(c, layer) || !d_q || !d_index || !d_ctx_len || !d_out) return KVS_ERR_INVALID_ARG;
+  if (!c->host_k_dev) return KVS_ERR_HOST_MEM;
+  const Dims& d = c->d;
+  if (!score_supported(d) || !attention_supported(d)) return KVS_ERR_NOT_SUPPORTED;
+  if (d_score_q == nullptr) nq = 1;
+  if (nq < 1 || nq > d.max_nq) return KVS_ERR_INVALID_ARG;
+  if (d_k_new && !d.v_shares_k && !d_v_new) return KVS_ERR_INVALID_ARG;
+  cudaStream_t s = S(stream);
+  cudaStream_t cs = copy_stream ? S(copy_stream) : s;
+  Layer& L = c->layers[layer];
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(d_q);
+  const __nv_bfloat16* sq = d_score_q ? static_cast<const __nv_bfloat16*>(d_score_q) : q;
+  __nv_bfloat16* idx = static_cast<__nv_bfloat16*>(d_index) + (size_t)layer * d.U * d.nb_max * d.dk;
+  int* sel = d_sel_out ? d_sel_out : L.sel;
+  int* nsel = d_nsel_out ? d_nsel_out : L.nsel;
+  cudaError_t e = cudaSuccess;
+  const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(d_k_new);
+  const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(d_v_new);
+  auto score = [&](const __nv_bfloat16* rows, int n) {
+    return timed(c, KVS_K_SCORE, s, 1, [&] { return launch_score(d, idx, rows, n, d_ctx_len, L.scores, c->err, s); });
+  };
+  auto topk = [&](int* so, int* no) {
+    return timed(c, KVS_K_TOPK, s, 1, [&] { return launch_topk(d, L.scores, d_ctx_len, so, no, c->err, s); });
+  };
+  auto update = [&](const int* so, const int* no) {
+    return timed(c, KVS_K_UPDATE, s, 1,
+                 [&] { return launch_cache_update(d, L, so, no, d_ctx_len, L.slot_of_sel, d_stats, s); });
+  };
+  auto fetch = [&](cudaStream_t fs) {
+    return timed(c, KVS_K_FETCH, fs, 1, [&] { return launch_fetch(d, L, d_ctx_len, fs); });
+  };
+  auto attn = [&](const int* so, const int* slots, const int* no) {
+    return timed(c, KVS_K_ATTN, s, attn_kernels(d),
+                 [&] { return launch_attention(d, L, q, so, slots, no, d_ctx_len, d_out, s); });
+  };
+  if (kn) e = timed(c, KVS_K_APPEND, s, 1, [&] { return launch_append(d, L, kn, vn, idx, d_ctx_len, s); });
+  if (!d.lookahead) {
+    if (e == cudaSuccess) e = score(sq, nq);
+    if (e == cudaSuccess) e = topk(sel, nsel);
+    if (e == cudaSuccess) e = update(sel, nsel);
+    if (e == cudaSuccess) e = fetch(s);
+    if (e == cudaSuccess) e = attn(sel, L.slot_of_sel, nsel);
+    return cuda_status(e);
+  }
+  if (!c->booted[layer]) {
+    // no selection yet: pick S_t from the current query and make it resident (sync part)
+    if (e == cudaSuccess) e = score(q, 1);
+    if (e == cudaSuccess) e = topk(L.sel, L.nsel);
+    if (e == cudaSuccess) e = update(L.sel, L.nsel);
+    if (e == cudaSuccess) e = fetch(s);
+    if (e == cudaSuccess) c->booted[layer] = 1;
+  }
+  if (e == cudaSuccess) e = attn(L.pend_sel, L.pend_slot, L.pend_n);
+  if (e == cudaSuccess) e = score(sq, nq);
+  if (e == cudaSuccess) e = topk(sel, nsel);
+  if (e == cudaSuccess) e = update(sel, nsel);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (cs != s) {
+    e = cudaEventRecord(c->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, c->fork, 0);
+    if (e == cudaSuccess) e = fetch(cs);
+    if (e == cudaSuccess) e = cudaEventRecord(c->fetch_done[layer], cs);
+    if (e == cudaSuccess) c->fetch_pending[layer] = 1;
+  } else {
+    e = fetch(s);
+  }
+  return cuda_status(e);
+}
+
+kvs_status kvs_join(kvs_ctx* c, kvs_stream_t stream) {
+  if (!c) return KVS_ERR_INVALID_ARG;
+  for (int l = 0; l < c->d.NL; ++l) {
+    if (!c->fetch_pending[l]) continue;
+    if (cudaStreamWaitEvent(S(stream), c->fetch_done[l], 0) != cudaSuccess) return KVS_ERR_CUDA;
+    c->fetch_pending[l] = 0;
+  }
+  return KVS_OK;
+}
+
+kvs_status kvs_cache_export(kvs_ctx* c, int layer, int* h_block2slot, int* h_slot2block, unsigned* h_stamp,
+                            unsigned* h_clock) {
+  if (!layer_ok(c, layer)) return KVS_ERR_INVALID_ARG;
+  const Dims& d = c->d;
+  const Layer& L = c->layers[layer];
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess && h_block2slot)
+    e = cudaMemcpy(h_block2slot, L.block2slot, (size_t)d.U * d.nb_max * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && h_slot2block)
+    e = cudaMemcpy(h_slot2block, L.slot2block, (size_t)d.U * d.C * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && h_stamp) e = cudaMemcpy(h_stamp, L.stamp, (size_t)d.U * d.C * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && h_clock) e = cudaMemcpy(h_clock, L.clock, (size_t)d.U * 4, cudaMemcpyDeviceToHost);
+  return cuda_status(e);
+}
+
+kvs_status kvs_slot_pools(kvs_ctx* c, int layer, void** d_k_pool, void** d_v_pool) {
+  if (!layer_ok(c, layer) || !d_k_pool || !d_v_pool) return KVS_ERR_INVALID_ARG;
+  *d_k_pool = c->layers[layer].kpool;
+  *d_v_pool = c->layers[layer].vpool;
+  return KVS_OK;
+}
+
+kvs_status kvs_poll_error(kvs_ctx* c, kvs_status* device_status) {
+  if (!c || !device_status) return KVS_ERR_INVALID_ARG;
+  unsigned v = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&v, c->err, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(c->err, 0, sizeof(v));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  *device_status = static_cast<kvs_status>(v);
+  return cuda_status(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// Internal declarations shared by the libkvs translation units (not part of the C ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvs.h"
+
+namespace kvs {
+
+// Shape and policy of one context, as the kernels see it (passed by value).
+struct Dims {
+  int B, NL, Hq, Hkv, G;
+  int dk, dv, v_shares_k;
+  int bs, max_ctx, nb_max;
+  int Kb, n_sink, n_recent, C, max_nq, lookahead, max_prefetch;
+  int U;                 // units per layer = B * Hkv
+  float scale;
+  unsigned timeout_us;
+  int row_bytes;         // host bytes moved per token: 2 * (dk + (v_shares_k ? 0 : dv))
+};
+
+// Device pointers of one layer.
+struct Layer {
+  int layer;
+  __nv_bfloat16* kpool;  // [U][C][bs][dk]
+  __nv_bfloat16* vpool;  // [U][C][bs][dv] (nullptr when v_shares_k)
+  int* block2slot;       // [U][nb_max]
+  int* slot2block;       // [U][C]
+  unsigned* stamp;       // [U][C]
+  unsigned* clock;       // [U]
+  int* pend_sel;         // [U][Kb]  selection the next lookahead attention reads
+  int* pend_slot;        // [U][Kb]
+  int* pend_n;           // [U]      -1: none yet
+  float* scores;         // [U][nb_max]   scratch
+  int* sel;              // [U][Kb]       scratch (fused step)
+  int* nsel;             // [U]
+  int* slot_of_sel;      // [U][Kb]
+  int* fetch_blk;        // [U][C]  blocks to copy host -> slot (misses or prefetches)
+  int* fetch_slot;       // [U][C]
+  int* n_fetch;          // [U]
+  float* attn_part;      // [U][n_split_max][Hq/Hkv][dv] partial outputs
+  float* attn_ml;        // [U][n_split_max][Hq/Hkv][2] partial (max, sum)
+  const __nv_bfloat16* host_k;  // device-mapped host history of this layer [B][Hkv][max_ctx][dk]
+  const __nv_bfloat16* host_v;  // [B][Hkv][max_ctx][dv] or nullptr
+  unsigned* err;         // sticky status word (shared by all layers)
+};
+
+constexpr int kAttnSplitMax = 32;
+
+__device__ __forceinline__ void set_error(unsigned* err, unsigned code) {
+  atomicCAS(err, 0u, code);
+}
+
+__device__ __forceinline__ int n_blocks_of(int L, int bs) { return (L + bs - 1) / bs; }
+
+// Orderable key of an fp32 score: larger score -> larger key; -0.0 and +0.0 share a key;
+// every NaN maps to 0, below -inf (whose key is 0x007FFFFF).
+__device__ __forceinline__ uint32_t score_key(float s) {
+  uint32_t u = __float_as_uint(s);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0u;      // NaN
+  if (u == 0x80000000u) u = 0u;                         // -0.0 -> +0.0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// -------------------------------------------------------------- launchers (one per kernel TU)
+cudaError_t launch_index_build(const Dims& d, const Layer& L, __nv_bfloat16* index, const int* ctx_len,
+                               cudaStream_t s);
+cudaError_t launch_append(const Dims& d, const Layer& L, const __nv_bfloat16* k_new,
+                          const __nv_bfloat16* v_new, __nv_bfloat16* index, const int* ctx_len, cudaStream_t s);
+cudaError_t launch_advance(int B, int* ctx_len, cudaStream_t s);
+cudaError_t launch_score(const Dims& d, const __nv_bfloat16* index, const __nv_bfloat16* q, int nq,
+                         const int* ctx_len, float* scores, unsigned* err, cudaStream_t s);
+cudaError_t launch_topk(const Dims& d, const float* scores, const int* ctx_len, int* sel, int* nsel,
+                        unsigned* err, cudaStream_t s);
+cudaError_t launch_cache_update(const Dims& d, const Layer& L, const int* sel, const int* nsel, const int* ctx_len,
+                                int* slot_of_sel, kvs_stats* stats, cudaStream_t s);
+cudaError_t launch_prefetch(const Dims& d, const Layer& L, const int* hint, const int* hint_n, const int* ctx_len,
+                            kvs_stats* stats, cudaStream_t s);
+cudaError_t launch_fetch(const Dims& d, const Layer& L, const int* ctx_len, cudaStream_t s);
+cudaError_t launch_attention(const Dims& d, const Layer& L, const __nv_bfloat16* q, const int* sel,
+                             const int* slot_of_sel, const int* nsel, const int* ctx_len, float* out,
+                             cudaStream_t s);
+int attention_supported(const Dims& d);
+int attention_split(const Dims& d, int* n_split, int* blocks_per_split);
+int score_supported(const Dims& d);
+
+}  // namespace kvs

@@ -1,0 +1,113 @@
+"""Shared set-up for the GPU parity tests: one workload bound to a libkvs context, and the
+oracle on the same seeded inputs.  Inputs only ever flow oracle/generator -> GPU; the oracle
+never reads anything the CUDA path wrote."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import workload as W
+from oracle import OracleDecoder, bf16_to_f32
+
+
+def torch_mod():
+    import torch
+    return torch
+
+
+class GpuCase:
+    """Host history (pinned), device index, contexts and per-step buffers for one workload."""
+
+    def __init__(self, w: W.Workload, ctx_lens=None, copy_stream=False, n_threads=0):
+        torch = torch_mod()
+        import sparse_kv_cache_decode_gb300 as K
+        self.w = w
+        self.K = K
+        B, NL, Hkv = w.n_req, w.n_layer, w.n_kv_head
+        self.k_host = torch.empty((NL, B, Hkv, w.max_ctx, w.d_k), dtype=torch.int16, pin_memory=True)
+        self.v_host = None if w.v_shares_k else torch.empty((NL, B, Hkv, w.max_ctx, w.d_v), dtype=torch.int16,
+                                                            pin_memory=True)
+        W.fill_kv(w, self.k_host, self.v_host, n_threads)
+        self.k_np = self.k_host.numpy().view(np.uint16)
+        self.v_np = None if self.v_host is None else self.v_host.numpy().view(np.uint16)
+        self.ctx_lens = list(ctx_lens) if ctx_lens is not None else [w.ctx0] * B
+        self.ctx_len = torch.tensor(self.ctx_lens, dtype=torch.int32, device="cuda")
+        self.cfg = K.make_config(w)
+        self.ctx = K.Context(self.cfg)
+        self.ctx.bind_host_kv(self.k_host, self.v_host)
+        self.nb_max = w.max_blocks
+        self.index = torch.zeros((NL, B, Hkv, self.nb_max, w.d_k), dtype=torch.int16, device="cuda")
+        for l in range(NL):
+            self.ctx.index_build(l, self.index, self.ctx_len)
+        self.stats = torch.zeros((NL, 7), dtype=torch.int64, device="cuda")
+        self.sel = torch.zeros((NL, B, Hkv, w.budget_blocks), dtype=torch.int32, device="cuda")
+        self.nsel = torch.zeros((NL, B, Hkv), dtype=torch.int32, device="cuda")
+        self.out = torch.zeros((NL, B, w.n_q_head, w.d_v), dtype=torch.float32, device="cuda")
+        self.copy_stream = torch.cuda.Stream() if copy_stream else None
+        self.qs = W.QueryStream(w)
+        self.t = 0
+        torch.cuda.synchronize()
+
+    def oracle(self, reqs=None) -> OracleDecoder:
+        """Oracle on the same inputs (copies the host rows now, before any GPU append)."""
+        return OracleDecoder(self.w, self.k_np, self.v_np, self.ctx_lens, reqs)
+
+    def step_inputs(self, t: int):
+        w = self.w
+        q = self.qs.queries(t)
+        d = self.qs.drafts(t) if w.lookahead else None
+        nk = nv = None
+        if w.append:
+            nk, nv = W.token(w, w.ctx0 + t)
+        return q, d, nk, nv
+
+    def gpu_step(self, q, d, nk, nv):
+        """One decode step over all layers through kvs_decode_step (+ prefetch, append)."""
+        torch = torch_mod()
+        w = self.w
+        qd = torch.from_numpy(q.view(np.int16)).cuda()
+        dd = None if d is None else torch.from_numpy(d.view(np.int16)).cuda()
+        nkd = None if nk is None else torch.from_numpy(nk.view(np.int16)).cuda()
+        nvd = None if nv is None else torch.from_numpy(nv.view(np.int16)).cuda()
+        if w.append:
+            self.ctx.advance_ctx(self.ctx_len)
+        for l in range(w.n_layer):
+            if w.layer_prefetch and l > 0:
+                self.ctx.layer_prefetch(l, self.sel[l - 1], self.nsel[l - 1], self.ctx_len, self.stats)
+            self.ctx.decode_step(l, qd[l], None if dd is None else dd[l], w.n_score_q if dd is not None else 1,
+                                 self.index, self.ctx_len, self.out[l], self.stats,
+                                 None if nkd is None else nkd[l], None if nvd is None else nvd[l],
+                                 self.sel[l], self.nsel[l], copy_stream=self.copy_stream)
+        if self.copy_stream is not None:
+            self.ctx.join()
+        torch.cuda.synchronize()
+        self.t += 1
+
+
+def score_tolerance(s_ref: np.ndarray, a_ref: np.ndarray) -> np.ndarray:
+    """|s_gpu - s| <= 1e-4 (|s| + A): the relative 1e-4 score bound, measured against the
+    conditioning A = scale * max sum |q.ik| so that near-cancelling dot products are fair."""
+    return 1e-4 * (np.abs(s_ref) + a_ref)
+
+
+def selection_is_valid(sel, s_ref, a_ref, nb, budget, n_sink, n_recent) -> bool:
+    """A GPU selection that differs from the oracle's is still correct when some perturbation
+    of the reference scores within the tolerance makes it the top-K (several results are
+    correct at near-ties): every chosen free block must not lose to an unchosen one by more
+    than the two tolerances."""
+    from oracle import forced_blocks
+    sel = np.asarray(sel)
+    if nb <= budget:
+        return sel.tolist() == list(range(nb))
+    forced = set(forced_blocks(nb, budget, n_sink, n_recent).tolist())
+    if not forced <= set(sel.tolist()) or len(sel) != budget or np.any(np.diff(sel) <= 0):
+        return False
+    tol = score_tolerance(s_ref, a_ref)
+    chosen = [b for b in sel if b not in forced]
+    rest = np.array([b for b in range(nb) if b not in forced and b not in set(chosen)], np.int64)
+    if len(rest) == 0:
+        return True
+    worst_chosen = min(s_ref[b] + tol[b] for b in chosen)
+    best_rest = np.max(s_ref[rest] - tol[rest])
+    return worst_chosen >= best_rest

@@ -1,0 +1,280 @@
+"""GPU parity of each libkvs entry point against the CPU oracle (run on a GB300).
+
+Each stage is fed inputs that come from the seeded generator or from the oracle, never from
+another GPU stage, and compared with the oracle stage: bit-exact for index keys, selections
+and cache state; within 1e-4 (|s| + A) for scores; within 2e-3 absolute for attention."""
+import math
+
+import numpy as np
+import pytest
+
+import workload as W
+from kvs_harness import GpuCase, score_tolerance
+from oracle import (UnitCache, attend, bf16_to_f32, block_scores, cache_update, index_keys, layer_prefetch,
+                    select_blocks)
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+MLA_G128 = W.MLA_128K.with_(name="mla_g128_small", n_req=2, n_layer=1, ctx0=2048, steps=4, budget_blocks=256,
+                            cap_blocks=384, n_heavy=20)
+TINY3 = W.TINY.with_(name="tiny3", n_req=3)
+TINY_G8 = W.TINY.with_(name="tiny_g8", n_req=2, n_q_head=16, n_kv_head=2)
+TINY_BS64 = W.TINY.with_(name="tiny_bs64", n_req=2, block_size=64, ctx0=3000, budget_blocks=8, cap_blocks=12)
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def _nb(L, bs):
+    return (L + bs - 1) // bs
+
+
+@pytest.mark.parametrize("w,lens", [(TINY3, [4096, 1000, 17]), (W.TINY_MLA, [4096]),
+                                    (TINY_BS64, [3000, 2999]), (MLA_G128, [2048, 333])])
+def test_index_build_bit_exact(w, lens):
+    g = GpuCase(w, lens)
+    idx = g.index.cpu().numpy().view(np.uint16)
+    for l in range(w.n_layer):
+        for r, L in enumerate(lens):
+            for h in range(w.n_kv_head):
+                nb = _nb(L, w.block_size)
+                ref = index_keys(g.k_np[l, r, h], L, w.block_size)
+                np.testing.assert_array_equal(idx[l, r, h, :nb], ref, err_msg=f"unit {(l, r, h)}")
+
+
+def _score_rows(w, q, d, l, r, h):
+    heads = slice(h * w.group, (h + 1) * w.group)
+    if d is None:
+        return q[l, r, heads]
+    return d[l, r, :, heads].reshape(-1, w.d_k)
+
+
+@pytest.mark.parametrize("w,lens", [(TINY3, [4096, 1000, 17]), (W.TINY_LOOKAHEAD.with_(n_req=2), [4096, 2222]),
+                                    (TINY_G8, [4096, 4000]), (W.TINY_MLA, [4096]), (MLA_G128, [2048, 1500]),
+                                    (TINY3.with_(int_scale=2.0), [4096, 1000, 17])])
+def test_score_blocks(w, lens):
+    g = GpuCase(w, lens)
+    scores = torch.full((w.n_req, w.n_kv_head, g.nb_max), float("nan"), dtype=torch.float32, device="cuda")
+    for t in range(2):
+        q, d, _, _ = g.step_inputs(t)
+        src = d if d is not None else q
+        nq = w.n_score_q
+        for l in range(w.n_layer):
+            g.ctx.score_blocks(l, _dev(src[l]), nq, g.index, g.ctx_len, scores)
+            got = scores.cpu().numpy()
+            for r, L in enumerate(lens):
+                for h in range(w.n_kv_head):
+                    nb = _nb(L, w.block_size)
+                    ik = index_keys(g.k_np[l, r, h], L, w.block_size)
+                    s, a = block_scores(_score_rows(w, q, d, l, r, h), ik, w.softmax_scale)
+                    gs = got[r, h, :nb].astype(np.float64)
+                    if w.int_scale > 0:     # exact integer-valued dot products: bit-exact fp32
+                        np.testing.assert_array_equal(got[r, h, :nb], s.astype(np.float32))
+                    else:
+                        err = np.abs(gs - s)
+                        tol = score_tolerance(s, a)
+                        assert np.all(err <= tol), f"unit {(l, r, h)} max err/tol {np.max(err / tol)}"
+
+
+def _special_scores(seed, n):
+    u = W.uniform_f32(seed, 7, n, -4.0, 4.0)
+    s = np.round(u * 4.0).astype(np.float32) / 4.0          # coarse values: many ties
+    pos = W.randint(seed, 8, 12, n)
+    specials = np.array([np.nan, np.inf, -np.inf, -0.0, 0.0, np.nan], np.float32)
+    for i, p in enumerate(pos):
+        s[p] = specials[i % len(specials)]
+    return s
+
+
+@pytest.mark.parametrize("lens,budget,sink,recent", [
+    ([4096, 1000, 17], 16, 1, 2),        # ragged, one context below the budget
+    ([4096, 4096], 2, 1, 1),              # budget == forced set
+    ([300000, 123457], 128, 1, 2),        # > 16384 blocks: scores read from global memory
+    ([65536, 65536], 256, 0, 0),          # pure top-k
+])
+def test_topk_select_bit_exact(lens, budget, sink, recent):
+    w = W.TINY.with_(name="topk", n_req=len(lens), ctx0=max(lens), budget_blocks=budget, n_sink=sink,
+                     n_recent=recent, cap_blocks=budget, n_heavy=0, n_layer=1)
+    g = GpuCase(w, lens)
+    nbm = g.nb_max
+    host = np.stack([np.stack([_special_scores(17 + r * 7 + h, nbm) for h in range(w.n_kv_head)])
+                     for r in range(w.n_req)])
+    scores = torch.from_numpy(host).cuda()
+    sel = torch.full((w.n_req, w.n_kv_head, budget), -7, dtype=torch.int32, device="cuda")
+    nsel = torch.zeros((w.n_req, w.n_kv_head), dtype=torch.int32, device="cuda")
+    g.ctx.topk_select(scores, g.ctx_len, sel, nsel)
+    gs, gn = sel.cpu().numpy(), nsel.cpu().numpy()
+    for r, L in enumerate(lens):
+        for h in range(w.n_kv_head):
+            nb = _nb(L, w.block_size)
+            ref = select_blocks(host[r, h], nb, budget, sink, recent)
+            assert gn[r, h] == len(ref)
+            np.testing.assert_array_equal(gs[r, h, :len(ref)], ref, err_msg=f"unit {(r, h)}")
+    assert g.ctx.poll_error() == 0
+
+
+def _correlated_selections(seed, nb, budget, steps, keep=0.7):
+    rng = np.random.default_rng(seed)
+    cur = np.sort(rng.choice(nb, min(budget, nb), replace=False))
+    out = []
+    for _ in range(steps):
+        k = cur[rng.random(len(cur)) < keep]
+        n_new = min(budget, nb) - len(k)
+        fresh = rng.choice(np.setdiff1d(np.arange(nb), k), n_new, replace=False)
+        cur = np.sort(np.concatenate([k, fresh]))
+        n = len(cur) if rng.random() > 0.15 else max(1, len(cur) - int(rng.integers(0, 3)))
+        out.append(cur[:n] if n == len(cur) else np.sort(rng.choice(cur, n, replace=False)))
+    return out
+
+
+def _check_state(g, layer, caches, lens):
+    w = g.w
+    b2s, s2b, st, clk = g.ctx.cache_export(layer)
+    for u in range(g.ctx.units):
+        c = caches[u]
+        np.testing.assert_array_equal(s2b[u], c.slot2block, err_msg=f"slot2block unit {u}")
+        np.testing.assert_array_equal(st[u].astype(np.int64), c.stamp, err_msg=f"stamp unit {u}")
+        assert int(clk[u]) == c.clock
+        np.testing.assert_array_equal(b2s[u, : c.n_blocks], c.block2slot[: g.nb_max], err_msg=f"block2slot unit {u}")
+
+
+def _check_slots(g, layer, caches, lens, blocks_by_unit):
+    w = g.w
+    kp, vp = g.ctx.slot_pool_tensors(layer)
+    kp = kp.cpu().numpy().view(np.uint16)
+    vp = None if vp is None else vp.cpu().numpy().view(np.uint16)
+    for u, blocks in blocks_by_unit.items():
+        r, h = divmod(u, w.n_kv_head)
+        L = lens[r]
+        for b in blocks:
+            s = caches[u].block2slot[b]
+            rows = min(w.block_size, L - b * w.block_size)
+            t0 = b * w.block_size
+            np.testing.assert_array_equal(kp[u, s, :rows], g.k_np[layer, r, h, t0:t0 + rows], err_msg=f"K slot {u}/{b}")
+            if vp is not None:
+                np.testing.assert_array_equal(vp[u, s, :rows], g.v_np[layer, r, h, t0:t0 + rows])
+
+
+@pytest.mark.parametrize("lookahead,cap", [(False, 11), (False, 8), (True, 12), (True, 9)])
+def test_cache_update_sequences_bit_exact(lookahead, cap):
+    lens = [1000, 997]
+    w = W.TINY.with_(name="cache", n_req=2, ctx0=1000, budget_blocks=8, cap_blocks=cap, lookahead=lookahead,
+                     n_draft=4 if lookahead else 0)
+    g = GpuCase(w, lens)
+    U = g.ctx.units
+    caches = [UnitCache(cap, g.nb_max) for _ in range(U)]
+    seqs = [_correlated_selections(40 + u, _nb(lens[u // w.n_kv_head], 16), 8, 30) for u in range(U)]
+    prev = [None] * U
+    sel = torch.zeros((w.n_req, w.n_kv_head, 8), dtype=torch.int32, device="cuda")
+    nsel = torch.zeros((w.n_req, w.n_kv_head), dtype=torch.int32, device="cuda")
+    sos = torch.full((w.n_req, w.n_kv_head, 8), -1, dtype=torch.int32, device="cuda")
+    stats = torch.zeros((1, 7), dtype=torch.int64, device="cuda")
+    tot = dict(hits=0, misses=0, evictions=0, pin_fallbacks=0)
+    for step in range(30):
+        hs = np.zeros((U, 8), np.int32)
+        hn = np.zeros(U, np.int32)
+        for u in range(U):
+            s = seqs[u][step]
+            hs[u, :len(s)] = s
+            hn[u] = len(s)
+        sel.copy_(torch.from_numpy(hs.reshape(w.n_req, w.n_kv_head, 8)))
+        nsel.copy_(torch.from_numpy(hn.reshape(w.n_req, w.n_kv_head)))
+        g.ctx.cache_update(0, sel, nsel, g.ctx_len, sos, stats)
+        got_sos = sos.cpu().numpy().reshape(U, 8)
+        for u in range(U):
+            s = seqs[u][step]
+            res = cache_update(caches[u], s, prev[u] if lookahead else None)
+            prev[u] = s
+            np.testing.assert_array_equal(got_sos[u, :len(s)], res.slot_of_sel, err_msg=f"step {step} unit {u}")
+            tot["hits"] += len(res.hits)
+            tot["misses"] += len(res.misses)
+            tot["evictions"] += res.n_evictions
+            tot["pin_fallbacks"] += int(res.pin_fallback)
+        _check_state(g, 0, caches, lens)
+        _check_slots(g, 0, caches, lens, {u: seqs[u][step] for u in range(U)})
+    st = stats.cpu().numpy()[0]
+    assert [st[0], st[1], st[2], st[5]] == [tot["hits"], tot["misses"], tot["evictions"], tot["pin_fallbacks"]]
+    assert g.ctx.poll_error() == 0
+
+
+def test_layer_prefetch_sequences_bit_exact():
+    lens = [1000, 1000]
+    w = W.TINY.with_(name="prefetch", n_req=2, n_layer=2, ctx0=1000, budget_blocks=8, cap_blocks=12,
+                     layer_prefetch=True)
+    g = GpuCase(w, lens)
+    U = g.ctx.units
+    caches = [UnitCache(12, g.nb_max) for _ in range(U)]
+    sels = [_correlated_selections(70 + u, 63, 8, 25) for u in range(U)]
+    hints = [_correlated_selections(90 + u, 63, 8, 25, keep=0.5) for u in range(U)]
+
+    def dev_sel(lists):
+        a = np.zeros((U, 8), np.int32)
+        n = np.zeros(U, np.int32)
+        for u, s in enumerate(lists):
+            a[u, :len(s)] = s
+            n[u] = len(s)
+        return (torch.from_numpy(a.reshape(w.n_req, w.n_kv_head, 8)).cuda(),
+                torch.from_numpy(n.reshape(w.n_req, w.n_kv_head)).cuda())
+
+    sos = torch.zeros((w.n_req, w.n_kv_head, 8), dtype=torch.int32, device="cuda")
+    stats = torch.zeros((2, 7), dtype=torch.int64, device="cuda")
+    n_pf = n_pfh = 0
+    for step in range(25):
+        hs, hn = dev_sel([hints[u][step] for u in range(U)])
+        g.ctx.layer_prefetch(1, hs, hn, g.ctx_len, stats)
+        pfs = [layer_prefetch(caches[u], hints[u][step], 12 - 8) for u in range(U)]
+        n_pf += sum(len(p.blocks) for p in pfs)
+        _check_state(g, 1, caches, lens)
+        _check_slots(g, 1, caches, lens, {u: pfs[u].blocks for u in range(U)})
+        ss, sn = dev_sel([sels[u][step] for u in range(U)])
+        g.ctx.cache_update(1, ss, sn, g.ctx_len, sos, stats)
+        for u in range(U):
+            n_pfh += cache_update(caches[u], sels[u][step]).prefetch_hits
+        _check_state(g, 1, caches, lens)
+    st = stats.cpu().numpy()[1]
+    assert st[3] == n_pf and st[4] == n_pfh and n_pf > 0
+    assert g.ctx.poll_error() == 0
+
+
+@pytest.mark.parametrize("w,lens", [(TINY3, [4096, 1000, 17]), (TINY_G8, [4096, 3001]), (TINY_BS64, [3000, 2999]),
+                                    (W.TINY_MLA, [4096]), (MLA_G128, [2048, 1999]),
+                                    (W.TINY.with_(name="tiny_bigbudget", n_req=2, budget_blocks=300, cap_blocks=300),
+                                     [4096, 4000])])
+def test_sparse_decode_attention(w, lens):
+    g = GpuCase(w, lens)
+    U = g.ctx.units
+    Kb = w.budget_blocks
+    rng = np.random.default_rng(5)
+    sel_h = np.zeros((U, Kb), np.int32)
+    n_h = np.zeros(U, np.int32)
+    sels = []
+    for u in range(U):
+        nb = _nb(lens[u // w.n_kv_head], w.block_size)
+        k = min(Kb, nb)
+        s = np.sort(np.concatenate([[nb - 1], rng.choice(nb - 1, k - 1, replace=False)])) if k > 1 else np.array([nb - 1])
+        sels.append(s)
+        sel_h[u, :k] = s
+        n_h[u] = k
+    sel = torch.from_numpy(sel_h.reshape(w.n_req, w.n_kv_head, Kb)).cuda()
+    nsel = torch.from_numpy(n_h.reshape(w.n_req, w.n_kv_head)).cuda()
+    sos = torch.zeros_like(sel)
+    g.ctx.cache_update(0, sel, nsel, g.ctx_len, sos)
+    q, _, _, _ = g.step_inputs(0)
+    out = torch.zeros((w.n_req, w.n_q_head, w.d_v), dtype=torch.float32, device="cuda")
+    g.ctx.sparse_decode_attn(0, _dev(q[0]), sel, sos, nsel, g.ctx_len, out)
+    got = out.cpu().numpy()
+    worst = 0.0
+    for u in range(U):
+        r, h = divmod(u, w.n_kv_head)
+        L = lens[r]
+        pos = np.concatenate([np.arange(b * w.block_size, min((b + 1) * w.block_size, L)) for b in sels[u]])
+        kt = g.k_np[0, r, h, pos]
+        vt = kt[:, : w.d_v] if w.v_shares_k else g.v_np[0, r, h, pos]
+        heads = slice(h * w.group, (h + 1) * w.group)
+        ref = attend(q[0, r, heads], kt, vt, w.softmax_scale)
+        err = np.abs(got[r, heads] - ref).max()
+        worst = max(worst, err)
+        assert err <= 2e-3, f"unit {u}: max abs err {err}"
+    assert g.ctx.poll_error() == 0

@@ -48,14 +48,16 @@ class _KVParams(ctypes.Structure):
                 ("heavy_scale", ctypes.c_float),
                 ("heavy_shared_layers", ctypes.c_int32),
                 ("rho_layer", ctypes.c_double),
-                ("n_threads", ctypes.c_int32)]
+                ("n_threads", ctypes.c_int32),
+                ("int_scale", ctypes.c_float), ("int_clip", ctypes.c_float)]
 
 
 class _QParams(ctypes.Structure):
     _fields_ = [("seed", ctypes.c_uint64),
                 ("n_req", ctypes.c_int32), ("n_layer", ctypes.c_int32), ("n_q_head", ctypes.c_int32),
                 ("d", ctypes.c_int32),
-                ("rho", ctypes.c_double), ("rho_layer", ctypes.c_double)]
+                ("rho", ctypes.c_double), ("rho_layer", ctypes.c_double),
+                ("int_scale", ctypes.c_float), ("int_clip", ctypes.c_float)]
 
 
 def lib():
@@ -71,7 +73,7 @@ def lib():
             _lib.kvs_gen_q_advance.argtypes = [P(_QParams), ctypes.c_void_p, ctypes.c_int64]
             _lib.kvs_gen_q_values.argtypes = [P(_QParams), ctypes.c_void_p, ctypes.c_void_p]
             _lib.kvs_gen_q_values.restype = None
-            _lib.kvs_gen_to_bf16.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+            _lib.kvs_gen_to_bf16.argtypes = [P(_QParams), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
             _lib.kvs_gen_to_bf16.restype = None
             _lib.kvs_gen_draft.argtypes = [P(_QParams), ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                            ctypes.c_double, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
@@ -121,6 +123,8 @@ class Workload:
     heavy_scale: float = 1.0
     heavy_shared_layers: bool = False
     seed: int = 0
+    int_scale: float = 0.0   # > 0: integer-valued inputs round(x * int_scale), clipped (exact fp32 scores)
+    int_clip: float = 7.0
     notes: str = ""
 
     @property
@@ -152,10 +156,12 @@ class Workload:
     def kv_params(self, n_threads: int = 0) -> _KVParams:
         return _KVParams(self.seed, self.n_req, self.n_layer, self.n_kv_head, self.d_k,
                          0 if self.v_shares_k else self.d_v, self.ctx0, self.n_heavy, self.max_ctx,
-                         self.heavy_scale, 1 if self.heavy_shared_layers else 0, self.rho_layer, n_threads)
+                         self.heavy_scale, 1 if self.heavy_shared_layers else 0, self.rho_layer, n_threads,
+                         self.int_scale, self.int_clip)
 
     def q_params(self) -> _QParams:
-        return _QParams(self.seed, self.n_req, self.n_layer, self.n_q_head, self.d_k, self.rho, self.rho_layer)
+        return _QParams(self.seed, self.n_req, self.n_layer, self.n_q_head, self.d_k, self.rho, self.rho_layer,
+                        self.int_scale, self.int_clip)
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -198,7 +204,16 @@ def sweep_workload(block_size: int, budget_tokens: int, rho: float, n_layer: int
                     n_heavy=_heavy(0.01, 65536), heavy_scale=3.0)
 
 
-WORKLOADS = {w.name: w for w in (TINY, LLAMA8B_32K, LONG_128K, MLA_128K)}
+# Variants of the tiny case that exercise each mode at oracle-friendly sizes.
+TINY_LOOKAHEAD = TINY.with_(name="tiny_lookahead", lookahead=True, n_draft=4)
+TINY_APPEND = TINY.with_(name="tiny_append", append=True, rho=0.95)
+TINY_PREFETCH = TINY.with_(name="tiny_prefetch", n_layer=2, layer_prefetch=True, rho_layer=0.8)
+TINY_MLA = Workload(name="tiny_mla", n_req=1, n_layer=1, n_q_head=16, n_kv_head=1, d_k=576, d_v=512,
+                    v_shares_k=True, block_size=1, ctx0=4096, steps=32, budget_blocks=256, n_sink=0, n_recent=0,
+                    cap_blocks=384, rho=0.9, n_heavy=32, heavy_scale=4.0)
+
+WORKLOADS = {w.name: w for w in (TINY, TINY_LOOKAHEAD, TINY_APPEND, TINY_PREFETCH, TINY_MLA, LLAMA8B_32K, LONG_128K,
+                                 MLA_128K)}
 
 
 # --------------------------------------------------------------------------- fills
@@ -296,7 +311,7 @@ class QueryStream:
         w = self.w
         q = self._values(t)
         out = np.empty((w.n_layer, w.n_req, w.n_q_head, w.d_k), np.uint16)
-        lib().kvs_gen_to_bf16(q.ctypes.data, q.size, out.ctypes.data)
+        lib().kvs_gen_to_bf16(ctypes.byref(self.p), q.ctypes.data, q.size, out.ctypes.data)
         return out
 
     def drafts(self, t: int) -> np.ndarray:

@@ -69,6 +69,18 @@ static inline uint16_t gen_bf16(double v) {
   return (uint16_t)hi;
 }
 
+/* Stored value of a drawn real number: bf16 of v, or, in integer mode (int_scale > 0), bf16 of
+ * round(v * int_scale) clipped to [-int_clip, int_clip] (small integers are exact in bf16). */
+static inline uint16_t gen_store(double v, float int_scale, float int_clip) {
+  if (int_scale > 0.f) {
+    double x = nearbyint(v * (double)int_scale);
+    if (x > int_clip) x = int_clip;
+    if (x < -int_clip) x = -int_clip;
+    return gen_bf16(x);
+  }
+  return gen_bf16(v);
+}
+
 int kvs_gen_counter_limits_ok(int n_req, int n_layer, int n_head, int64_t n_pos, int d) {
   return n_req <= 64 && n_layer <= 64 && n_head <= 256 && n_pos <= (1 << 24) && d <= 2048 && (d % 2) == 0;
 }
@@ -85,6 +97,8 @@ typedef struct {
   int32_t heavy_shared_layers;                 /* 1: one heavy set per (req, head) for all layers */
   double rho_layer;                            /* 0: layers independent; else AR(1) mix across layers */
   int32_t n_threads;
+  float int_scale;                             /* > 0: integer-valued mode (see gen_store) */
+  float int_clip;
 } kvs_gen_kv_params;
 
 /* Heavy positions of one set: the first n_heavy entries of a partial Fisher-Yates
@@ -158,8 +172,12 @@ static void* gen_kv_worker(void* arg) {
             z1 = p->rho_layer * prev_k[2 * pr + 1] + sk * z1;
           }
           prev_k[2 * pr] = z0; prev_k[2 * pr + 1] = z1;
-          krow[2 * pr] = gen_bf16(z0 * hs);
-          krow[2 * pr + 1] = gen_bf16(z1 * hs);
+          krow[2 * pr] = gen_store(z0, p->int_scale, p->int_clip);
+          krow[2 * pr + 1] = gen_store(z1, p->int_scale, p->int_clip);
+          if (hs != 1.0) {
+            krow[2 * pr] = gen_store(z0 * hs, p->int_scale, p->int_clip * (float)hs);
+            krow[2 * pr + 1] = gen_store(z1 * hs, p->int_scale, p->int_clip * (float)hs);
+          }
         }
         for (int pr = 0; vrow && pr < dv / 2; ++pr) {
           double z0, z1;
@@ -169,8 +187,8 @@ static void* gen_kv_worker(void* arg) {
             z1 = p->rho_layer * prev_v[2 * pr + 1] + sk * z1;
           }
           prev_v[2 * pr] = z0; prev_v[2 * pr + 1] = z1;
-          vrow[2 * pr] = gen_bf16(z0);
-          vrow[2 * pr + 1] = gen_bf16(z1);
+          vrow[2 * pr] = gen_store(z0, p->int_scale, p->int_clip);
+          vrow[2 * pr + 1] = gen_store(z1, p->int_scale, p->int_clip);
         }
       }
     }
@@ -244,8 +262,8 @@ int kvs_gen_token(const kvs_gen_kv_params* p, int64_t pos, uint16_t* out_k, uint
               z1 = p->rho_layer * prev[2 * pr + 1] + sk * z1;
             }
             prev[2 * pr] = z0; prev[2 * pr + 1] = z1;
-            o[2 * pr] = gen_bf16(z0);
-            o[2 * pr + 1] = gen_bf16(z1);
+            o[2 * pr] = gen_store(z0, p->int_scale, p->int_clip);
+            o[2 * pr + 1] = gen_store(z1, p->int_scale, p->int_clip);
           }
         }
       }
@@ -260,6 +278,8 @@ typedef struct {
   int32_t n_req, n_layer, n_q_head, d;
   double rho;       /* AR(1) coefficient over decode steps */
   double rho_layer; /* 0: layers independent; else AR(1) mix across layers */
+  float int_scale;  /* > 0: integer-valued mode (see gen_store) */
+  float int_clip;
 } kvs_gen_q_params;
 
 /* Base state e[layer][req][head][d] (fp64) of the per-layer AR(1) over steps:
@@ -292,8 +312,8 @@ void kvs_gen_q_values(const kvs_gen_q_params* p, const double* state, double* q)
     }
 }
 
-void kvs_gen_to_bf16(const double* x, size_t n, uint16_t* out) {
-  for (size_t i = 0; i < n; ++i) out[i] = gen_bf16(x[i]);
+void kvs_gen_to_bf16(const kvs_gen_q_params* p, const double* x, size_t n, uint16_t* out) {
+  for (size_t i = 0; i < n; ++i) out[i] = gen_store(x[i], p->int_scale, p->int_clip);
 }
 
 /* Draft query j of step t: q_future (the fp64 query of step t + j) plus sigma * N(0,1) noise
@@ -310,8 +330,8 @@ int kvs_gen_draft(const kvs_gen_q_params* p, const double* q_future, int64_t t, 
         for (int pr = 0; pr < p->d / 2; ++pr, i += 2) {
           double z0, z1;
           gen_normal_pair(gen_at(p->seed, gen_ctr(4, r, l, h, 8 * t + j, pr)), &z0, &z1);
-          o[2 * pr] = gen_bf16(q_future[i] + sigma * z0);
-          o[2 * pr + 1] = gen_bf16(q_future[i + 1] + sigma * z1);
+          o[2 * pr] = gen_store(q_future[i] + sigma * z0, p->int_scale, p->int_clip);
+          o[2 * pr + 1] = gen_store(q_future[i + 1] + sigma * z1, p->int_scale, p->int_clip);
         }
       }
   return 0;
