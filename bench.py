@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--threads", type=int, default=0, help="generator threads (0: all cores)")
+    ap.add_argument("--serial", action="store_true", help="fetch on the compute stream (kernels run one at a time)")
     return ap.parse_args()
 
 
@@ -144,6 +145,28 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- peaks
+
+def upload_graphs(graphs, stream):
+    """Upload every instantiated graph before timing, so no first launch pays for it."""
+    import ctypes
+    import torch
+    cands = [os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64", n)
+             for n in ("libcudart.so.13", "libcudart.so")]
+    rt = None
+    for c in cands:
+        if os.path.exists(c):
+            rt = ctypes.CDLL(c)
+            break
+    if rt is None or not all(hasattr(g, "raw_cuda_graph_exec") for g in graphs):
+        return False
+    rt.cudaGraphUpload.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    for g in graphs:
+        rc = rt.cudaGraphUpload(ctypes.c_void_p(g.raw_cuda_graph_exec()), ctypes.c_void_p(stream.cuda_stream))
+        if rc != 0:
+            raise RuntimeError(f"cudaGraphUpload failed ({rc})")
+    torch.cuda.synchronize()
+    return True
+
 
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -272,11 +295,34 @@ def run_ours(args, dist):
     B, NL, Hkv = w.n_req, w.n_layer, w.n_kv_head
     T = args.warmup + args.steps
     T_e2e = 0 if args.no_e2e else args.steps
+    if w.append:   # history capacity for every appended token of the run (timed, measured, e2e)
+        w = w.with_(steps=max(w.steps, T + 8 + T_e2e + 1))
     t0 = time.time()
-    k_host = torch.empty((NL, B, Hkv, w.max_ctx, w.d_k), dtype=torch.int16, pin_memory=True)
-    v_host = None if w.v_shares_k else torch.empty((NL, B, Hkv, w.max_ctx, w.d_v), dtype=torch.int16,
-                                                   pin_memory=True)
-    W.fill_kv(w, k_host, v_host, args.threads)
+    # K and V histories; each filled by the generator (which draws both in one pass), so fill into
+    # a staging pair when V exists
+    if w.v_shares_k:
+        k_host, k_keep, host_desc = K.pinned_host_history((NL, B, Hkv, w.max_ctx, w.d_k),
+                                                          lambda t: W.fill_kv(w, t, None, args.threads))
+        v_host, v_keep = None, None
+    else:
+        k_arr = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_k))
+        v_arr = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_v))
+        W.fill_kv(w, k_arr.tensor, v_arr.tensor, args.threads)
+        fk, fv = k_arr.huge_fraction(), v_arr.huge_fraction()
+        if min(fk, fv) >= 0.95:
+            k_arr.register()
+            v_arr.register()
+            k_host, v_host, k_keep, v_keep = k_arr.tensor, v_arr.tensor, k_arr, v_arr
+            host_desc = f"mmap + transparent huge pages ({min(fk, fv):.0%}) + cudaHostRegister"
+        else:
+            k_host = torch.empty(k_arr.tensor.shape, dtype=torch.int16, pin_memory=True)
+            v_host = torch.empty(v_arr.tensor.shape, dtype=torch.int16, pin_memory=True)
+            k_host.copy_(k_arr.tensor)
+            v_host.copy_(v_arr.tensor)
+            del k_arr, v_arr
+            k_keep = v_keep = None
+            host_desc = f"cudaHostAlloc (huge pages covered only {min(fk, fv):.0%})"
+    log(f"host memory: {host_desc}")
     log(f"host KV {w.host_kv_bytes / 2**30:.1f} GiB generated in {time.time() - t0:.1f}s")
 
     ctx = K.Context(K.make_config(w))
@@ -313,7 +359,7 @@ def run_ours(args, dist):
     nsel = torch.zeros((NL, B, Hkv), dtype=torch.int32, device="cuda")
     stats = torch.zeros((NL, 7), dtype=torch.int64, device="cuda")
     s = torch.cuda.Stream()
-    cs = torch.cuda.Stream()
+    cs = torch.cuda.Stream(priority=-1)   # fetch CTAs are scheduled ahead of compute CTAs
 
     def step(qt, dt, tok):
         if w.append:
@@ -324,34 +370,46 @@ def run_ours(args, dist):
             ctx.decode_step(l, qt[l], None if dt is None else dt[l], nq if dt is not None else 1, index, ctx_len,
                             out[l], stats, None if tok is None else tok[0][l],
                             None if tok is None or tok[1] is None else tok[1][l], sel[l], nsel[l], stream=s,
-                            copy_stream=cs)
+                            copy_stream=None if args.serial else cs)
         ctx.join(s)
 
-    # step 0 eagerly (bootstraps lookahead selections), then one graph per remaining step
+    # Step 0 eagerly (bootstraps the lookahead selections).  Then one graph over fixed input
+    # buffers; each step copies its device-resident inputs into them (inside the timed region)
+    # and replays the graph.
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
         step(q_dev[0], None if d_dev is None else d_dev[0], tok_dev[0] if w.append else None)
     s.synchronize()
-    graphs = {}
+    q_fix = torch.empty_like(q_dev[0])
+    d_fix = torch.empty_like(d_dev[0]) if d_dev is not None else None
+    tok_fix = None
+    if w.append:
+        tok_fix = (torch.empty_like(tok_dev[0][0]),
+                   None if tok_dev[0][1] is None else torch.empty_like(tok_dev[0][1]))
 
-    def capture(t, qt, dt, tok):
+    def stage_inputs(t):
+        q_fix.copy_(q_dev[t], non_blocking=True)
+        if d_fix is not None:
+            d_fix.copy_(d_dev[t], non_blocking=True)
+        if tok_fix is not None:
+            tok_fix[0].copy_(tok_dev[t][0], non_blocking=True)
+            if tok_fix[1] is not None:
+                tok_fix[1].copy_(tok_dev[t][1], non_blocking=True)
+
+    def capture(qt, dt, tok):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             step(qt, dt, tok)
         return g
 
-    for t in range(1, args.warmup):
-        graphs[t] = capture(t, q_dev[t], None if d_dev is None else d_dev[t], tok_dev[t] if w.append else None)
-    n_timed_kernel_per_step = {"attn": NL, "score": NL, "fetch": NL + (NL - 1 if w.layer_prefetch else 0),
-                               "update": NL, "topk": NL}[args.timed_kernel]
-    ctx.kernel_timer_arm(args.timed_kernel, args.steps * n_timed_kernel_per_step)
     launches0 = ctx.launch_count()
-    for t in range(args.warmup, T):
-        graphs[t] = capture(t, q_dev[t], None if d_dev is None else d_dev[t], tok_dev[t] if w.append else None)
-    launches = ctx.launch_count() - launches0
+    graph = capture(q_fix, d_fix, tok_fix)
+    launches_per_step = ctx.launch_count() - launches0
+    upload_graphs([graph], s)
     with torch.cuda.stream(s):
         for t in range(1, args.warmup):
-            graphs[t].replay()
+            stage_inputs(t)
+            graph.replay()
     torch.cuda.synchronize()
     stats0 = stats.cpu().numpy().copy()
 
@@ -366,7 +424,8 @@ def run_ours(args, dist):
     with torch.cuda.stream(s):
         ev0.record(s)
         for t in range(args.warmup, T):
-            graphs[t].replay()
+            stage_inputs(t)
+            graph.replay()
         ev1.record(s)
     torch.cuda.synchronize()
     dist.barrier()
@@ -375,10 +434,34 @@ def run_ours(args, dist):
     elapsed = dist.max(elapsed)
     stats1 = stats.cpu().numpy()
     dstat = (stats1 - stats0).sum(axis=0)
-    kernel_ms, kernel_n = ctx.kernel_timer_read()
+    launches = launches_per_step * args.steps
     dev_status = ctx.poll_error()
     if dev_status != 0:
         raise RuntimeError(f"device status {K.STATUS.get(dev_status, dev_status)}")
+
+    # Kernel durations: CUDA events around every launch of each kernel, in graphs of their own
+    # (one per step, events recorded as graph nodes) run right after the timed region.  Event
+    # nodes order each kernel after the work before it, so these are the kernels' durations when
+    # they run without a concurrent fetch.
+    per_step_launches = {"attn": NL, "score": NL, "fetch": NL + (NL - 1 if w.layer_prefetch else 0),
+                         "update": NL, "topk": NL}
+    n_meas = min(args.steps, 8, len(tok_all) - T if w.append else 8)
+    n_meas = max(1, n_meas)
+    for kname, n in per_step_launches.items():
+        ctx.kernel_timer_arm(kname, n_meas * n)
+    meas_graphs = []
+    for i in range(n_meas):
+        meas_graphs.append(capture(q_fix, d_fix, tok_fix))
+    upload_graphs(meas_graphs, s)
+    with torch.cuda.stream(s):
+        for i, g in enumerate(meas_graphs):
+            stage_inputs(args.warmup + i)    # the inputs of timed steps, replayed once more
+            g.replay()
+    torch.cuda.synchronize()
+    kernel_times = {k: ctx.kernel_timer_read(k) for k in per_step_launches}
+    for kname in per_step_launches:
+        ctx.kernel_timer_arm(kname, 0)
+    kernel_ms, kernel_n = kernel_times[args.timed_kernel]
 
     ms_per_step = elapsed / args.steps * 1e3
     value = dist.world * args.steps / elapsed
@@ -389,23 +472,26 @@ def run_ours(args, dist):
     kv_gbs = hbm_step / t_step / 1e9
     misses, hits = float(dstat[1]), float(dstat[0])
 
-    # dominant-kernel roofline: algorithmic bytes per launch / live CUDA-event duration
+    # dominant-kernel roofline: algorithmic bytes per launch / CUDA-event duration per launch
     per_launch_ms = kernel_ms / max(1, kernel_n)
     if args.timed_kernel == "attn":
         alg = per_layer["attn"]
     elif args.timed_kernel == "score":
         alg = per_layer["index"] + w.n_req * nq * w.n_q_head * w.d_k * 2
     elif args.timed_kernel == "fetch":
-        alg = link_per_step / max(1, n_timed_kernel_per_step)
+        alg = link_per_step / max(1, per_step_launches["fetch"])
     else:
         alg = 0
     achieved = alg / (per_launch_ms * 1e-3) / 1e9 if per_launch_ms > 0 else 0.0
     bound_peak = link_peak if args.timed_kernel == "fetch" else hbm_peak
-    roofline = {"bound": "hbm" if args.timed_kernel != "fetch" else "host-link", "kernel": args.timed_kernel,
+    roofline = {"bound": "hbm", "kernel": args.timed_kernel,
                 "achieved": round(achieved, 1), "peak": round(bound_peak, 1), "unit": "GB/s",
                 "frac": round(achieved / bound_peak, 4), "traffic": None,
                 "bytes_per_launch": alg, "avg_launch_ms": round(per_launch_ms, 5), "launches_timed": kernel_n,
-                "peak_source": hbm_src if args.timed_kernel != "fetch" else "measured in this run (H2D copy)"}
+                "peak_source": hbm_src if args.timed_kernel != "fetch" else "measured in this run (H2D copy)",
+                "timing": "CUDA events around each launch, measurement pass after the timed region"}
+    if args.timed_kernel == "fetch":
+        roofline["bound"] = "host-link"
 
     e2e = None
     if not args.no_e2e:
@@ -422,7 +508,11 @@ def run_ours(args, dist):
                               "frac": round(step_roof / t_step, 4),
                               "bound": "host-link" if link_step / link_peak > hbm_step / hbm_peak else "hbm"},
             "miss_fraction": round(misses / max(1.0, misses + hits), 4),
-            "roofline": roofline, "clocks": clk, "gpu_launches": int(launches)}
+            "roofline": roofline, "clocks": clk, "gpu_launches": int(launches),
+            "kernel_ms_per_step": {k: round(ms / max(1, n) * per_step_launches[k], 4)
+                                   for k, (ms, n) in kernel_times.items()},
+            "fetch": "inline" if args.serial else "side stream", "host_memory": host_desc,
+            "launches_per_step": int(launches_per_step)}
     if e2e:
         line["e2e"] = e2e
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -456,6 +546,7 @@ def run_e2e(args, w, ctx, ctx_len, index, out, sel, nsel, stats, s, cs, q_all, d
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         step(q_fix, d_fix, tok_fix)
+    upload_graphs([g], s)
     torch.cuda.synchronize()
     h2d = q_fix.numel() * 2 + (d_fix.numel() * 2 if d_fix is not None else 0)
     if tok_fix is not None:

@@ -99,14 +99,17 @@ typedef struct kvs_ctx kvs_ctx;
 size_t kvs_workspace_bytes(const kvs_config* cfg);
 
 /* Validate cfg and carve d_workspace (>= kvs_workspace_bytes, 256-byte aligned device memory).
- * Clears the cache state (all slots empty, clocks 0) on the current device, synchronously.
+ * Clears the cache state (all slots empty and zero-filled, clocks 0) on the current device,
+ * synchronously.
  * Errors: KVS_ERR_INVALID_ARG (bad cfg, short or misaligned workspace), KVS_ERR_CUDA. */
 kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace_bytes, kvs_ctx** out);
 kvs_status kvs_destroy(kvs_ctx* ctx);
 
 /* Bind the pinned host history [HISP insight 1]: h_k, h_v in the layouts above (h_v NULL when
- * v_shares_k).  The memory must be page-locked and mapped into the device address space.
- * Errors: KVS_ERR_HOST_MEM when the pointers are not device-accessible. */
+ * v_shares_k).  The memory must be page-locked and mapped into the device address space.  The
+ * device reads one word of every 4 KiB page once (synchronously), so the translations of the
+ * whole history exist before the first fetch.  Errors: KVS_ERR_HOST_MEM when the pointers are
+ * not device-accessible. */
 kvs_status kvs_bind_host_kv(kvs_ctx* ctx, void* h_k, void* h_v);
 
 /* Build the block-mean index keys of one layer from the host history (setup after prefill):
@@ -196,17 +199,17 @@ kvs_status kvs_slot_pools(kvs_ctx* ctx, int layer, void** d_k_pool, void** d_v_p
  * device-side error happened since the last poll. */
 kvs_status kvs_poll_error(kvs_ctx* ctx, kvs_status* device_status);
 
-/* Kernel timer (diagnostics).  After kvs_kernel_timer_arm(ctx, kernel, capacity), the next
+/* Kernel timers (diagnostics).  After kvs_kernel_timer_arm(ctx, kernel, capacity), the next
  * `capacity` launches of that kernel (by any call, eager or captured in a CUDA graph) are each
- * bracketed by a pair of CUDA events recorded on the launch stream; kvs_kernel_timer_read
- * (synchronous) returns the summed elapsed milliseconds and the number of timed launches.
- * kernel: one of kvs_kernel_id; capacity 0 disarms. */
+ * bracketed by a pair of CUDA events recorded on the launch stream; several kernels can be armed
+ * at once.  kvs_kernel_timer_read (synchronous) returns that kernel's summed elapsed milliseconds
+ * and number of timed launches.  kernel: one of kvs_kernel_id; capacity 0 disarms it. */
 typedef enum {
   KVS_K_SCORE = 1, KVS_K_TOPK = 2, KVS_K_UPDATE = 3, KVS_K_FETCH = 4, KVS_K_ATTN = 5,
   KVS_K_PREFETCH = 6, KVS_K_APPEND = 7, KVS_K_INDEX = 8
 } kvs_kernel_id;
 kvs_status kvs_kernel_timer_arm(kvs_ctx* ctx, int kernel, int capacity);
-kvs_status kvs_kernel_timer_read(kvs_ctx* ctx, double* total_ms, int* n_timed);
+kvs_status kvs_kernel_timer_read(kvs_ctx* ctx, int kernel, double* total_ms, int* n_timed);
 
 /* Number of kernels this context has launched (or captured into graphs) so far. */
 unsigned long long kvs_launch_count(kvs_ctx* ctx);

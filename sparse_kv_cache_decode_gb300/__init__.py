@@ -66,7 +66,7 @@ _SIGS = {
     "kvs_slot_pools": (_I, [_P, _I, ctypes.POINTER(_P), ctypes.POINTER(_P)]),
     "kvs_poll_error": (_I, [_P, ctypes.POINTER(_I)]),
     "kvs_kernel_timer_arm": (_I, [_P, _I, _I]),
-    "kvs_kernel_timer_read": (_I, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
+    "kvs_kernel_timer_read": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "kvs_launch_count": (ctypes.c_ulonglong, [_P]),
 }
 
@@ -225,9 +225,10 @@ class Context:
     def kernel_timer_arm(self, kernel: str, capacity: int):
         _check(self.L.kvs_kernel_timer_arm(self.h, KERNEL_IDS[kernel], capacity), "kvs_kernel_timer_arm")
 
-    def kernel_timer_read(self):
+    def kernel_timer_read(self, kernel: str):
         ms, n = ctypes.c_double(), _I()
-        _check(self.L.kvs_kernel_timer_read(self.h, ctypes.byref(ms), ctypes.byref(n)), "kvs_kernel_timer_read")
+        _check(self.L.kvs_kernel_timer_read(self.h, KERNEL_IDS[kernel], ctypes.byref(ms), ctypes.byref(n)),
+               "kvs_kernel_timer_read")
         return ms.value, n.value
 
     def launch_count(self) -> int:
@@ -237,6 +238,88 @@ class Context:
         st = _I()
         _check(self.L.kvs_poll_error(self.h, ctypes.byref(st)), "kvs_poll_error")
         return st.value
+
+
+class HostArray:
+    """Page-locked, device-mapped host memory for the KV history, backed by transparent huge
+    pages: an anonymous mmap aligned to 512 MiB and advised MADV_HUGEPAGE, then registered with
+    cudaHostRegister (portable | mapped).  Large pages keep the GPU's translations of scattered
+    block fetches cheap.  Fill it (first touch) before calling register()."""
+
+    HUGE_ALIGN = 1 << 29
+
+    def __init__(self, shape, dtype=None, huge: bool = True):
+        import mmap
+        import torch
+        dtype = dtype or torch.int16
+        self.nbytes = int(math.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        align = self.HUGE_ALIGN if huge else mmap.PAGESIZE
+        self._mm = mmap.mmap(-1, self.nbytes + align, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        base = ctypes.addressof(ctypes.c_char.from_buffer(self._mm))
+        off = (-base) % align
+        if huge and hasattr(mmap, "MADV_HUGEPAGE"):
+            self._mm.madvise(mmap.MADV_HUGEPAGE, off, (self.nbytes + mmap.PAGESIZE - 1) // mmap.PAGESIZE * mmap.PAGESIZE)
+        self.tensor = torch.frombuffer(self._mm, dtype=torch.uint8, count=self.nbytes, offset=off).view(dtype).view(
+            *shape)
+        self._registered = False
+
+    def huge_fraction(self) -> float:
+        """Fraction of this array backed by transparent huge pages (from /proc/self/smaps)."""
+        lo = self.tensor.data_ptr()
+        hi = lo + self.nbytes
+        huge = 0
+        try:
+            with open("/proc/self/smaps") as f:
+                cur = None
+                for ln in f:
+                    head = ln.split()[0]
+                    if "-" in head and ":" not in head:
+                        a, b = (int(x, 16) for x in head.split("-"))
+                        cur = (a, b) if (a < hi and b > lo) else None
+                    elif cur is not None and ln.startswith("AnonHugePages:"):
+                        huge += int(ln.split()[1]) * 1024
+        except OSError:
+            return 0.0
+        return min(1.0, huge / self.nbytes)
+
+    def register(self):
+        import torch
+        rc = torch.cuda.cudart().cudaHostRegister(self.tensor.data_ptr(), self.nbytes, 3)
+        if int(rc) != 0:
+            raise RuntimeError(f"cudaHostRegister failed ({rc})")
+        self._registered = True
+        return self
+
+    def close(self):
+        import torch
+        if self._registered:
+            torch.cuda.cudart().cudaHostUnregister(self.tensor.data_ptr())
+            self._registered = False
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def pinned_host_history(shape, fill, min_huge: float = 0.95):
+    """Host history of the given shape, filled by fill(tensor) and page-locked for the device.
+
+    Prefers a HostArray on transparent huge pages (fewest GPU translation misses on scattered
+    block fetches); when the kernel could not back it with huge pages, falls back to
+    cudaHostAlloc memory (torch pin_memory).  Returns (tensor, keepalive, description)."""
+    import torch
+    arr = HostArray(shape)
+    fill(arr.tensor)
+    frac = arr.huge_fraction()
+    if frac >= min_huge:
+        arr.register()
+        return arr.tensor, arr, f"mmap + transparent huge pages ({frac:.0%}) + cudaHostRegister"
+    t = torch.empty(shape, dtype=arr.tensor.dtype, pin_memory=True)
+    t.copy_(arr.tensor)
+    del arr
+    return t, None, f"cudaHostAlloc (huge pages covered only {frac:.0%})"
 
 
 def version() -> str:

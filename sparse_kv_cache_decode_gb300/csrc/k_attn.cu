@@ -402,6 +402,8 @@ cudaError_t launch_attention(const Dims& d, const Layer& L, const __nv_bfloat16*
                              const int* slot_of_sel, const int* nsel, const int* ctx_len, float* out,
                              cudaStream_t s) {
   if (!attention_supported(d)) return cudaErrorInvalidValue;
+  if (attention_tma_supported(d) && L.tmK && L.tmV)
+    return launch_attention_tma(d, L, L.tmK, L.tmV, q, sel, slot_of_sel, nsel, ctx_len, out, s);
   if (d.v_shares_k) {
     if (d.G <= 16) return launch_attn_t<576, 1, true>(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, s);
     return launch_attn_t<576, 8, true>(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, s);

@@ -1,0 +1,344 @@
+// Decode attention over the selected cache slots, TMA-pipelined (GQA groups of up to 16 q heads,
+// head dim 128, block size a multiple of 16).
+//
+// The (unit, selected block, 16-row sub-tile) sequence of a layer is cut into equal contiguous
+// ranges, one per CTA, with exactly 2 CTAs per SM (room for a fetch CTA beside them).  In each CTA one producer thread streams the
+// K and V tiles of its range into an 8-stage shared-memory ring with 2D tensor loads (128-byte
+// swizzle, completion on an mbarrier per stage); 4 consumer warps take the tiles round-robin,
+// each keeping an online softmax per q head on tensor-core tiles:
+//   S  = Q (16 heads x 128) . K^T (128 x 16 tokens)
+//   O += P (16 x 16) . V (16 x 128), P split into bf16 high and low parts.
+// A warp writes its (unnormalised O, max, sum) for every unit its CTA touches; a second kernel
+// merges the partials of a unit: o = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p.
+// Every mbarrier wait is bounded by the context's wait timeout (KVS_ERR_TIMEOUT on expiry).
+#include <cuda.h>
+
+#include "kvs_common.cuh"
+#include "kvs_ptx.cuh"
+
+namespace kvs {
+
+namespace {
+
+constexpr int D = 128;
+constexpr int kStages = 8;
+constexpr int kConsumers = 4;
+constexpr int kCtasPerSm = 2;   // leaves registers for a fetch CTA beside them
+constexpr int kTile = 16 * D * 2;           // bytes of a 16-row K or V tile (two 64-column boxes)
+constexpr int kStage = 2 * kTile;
+constexpr int kSmem = kStages * kStage + 1024 + 2 * kStages * 8 + 64;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Plan {
+  int n_cta, per_cta, max_segs;
+};
+
+__host__ __device__ inline Plan make_plan(const Dims& d, int n_sm) {
+  Plan p;
+  const long long positions = (long long)d.U * d.Kb;
+  int ctas = n_sm * kCtasPerSm;
+  p.per_cta = (int)((positions + ctas - 1) / ctas);
+  if (p.per_cta < 1) p.per_cta = 1;
+  p.n_cta = (int)((positions + p.per_cta - 1) / p.per_cta);
+  p.max_segs = (d.Kb + p.per_cta - 1) / p.per_cta + 1;
+  return p;
+}
+
+__device__ __forceinline__ int rows_present(int len, int blk, int bs) { return min(bs, len - blk * bs); }
+
+template <bool ROWS8>  // G <= 8: fragment rows 8..15 are zero at compile time
+__global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
+    attn_tma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, Dims d,
+                    Layer L, const __nv_bfloat16* __restrict__ q, const int* __restrict__ sel,
+                    const int* __restrict__ slot_of_sel, const int* __restrict__ nsel,
+                    const int* __restrict__ ctx_len, Plan plan) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStage);
+  uint64_t* empty = full + kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x;
+  const long long p0 = (long long)c * plan.per_cta;
+  const long long p1 = min((long long)d.U * d.Kb, p0 + plan.per_cta);
+  const int subs = d.bs / 16;
+  const uint64_t timeout_ns = (uint64_t)d.timeout_us * 1000ull;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumers) {
+    // ------------------------------------------------------------------ producer
+    if (lane != 0) return;
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    int k = 0;
+    bool ok = true;
+    for (long long p = p0; p < p1 && ok; ++p) {
+      const int u = (int)(p / d.Kb), i = (int)(p % d.Kb);
+      if (i >= nsel[u]) continue;
+      const int blk = sel[(size_t)u * d.Kb + i], slot = slot_of_sel[(size_t)u * d.Kb + i];
+      const int rows = rows_present(ctx_len[u / d.Hkv], blk, d.bs);
+      for (int sub = 0; sub < subs && ok; ++sub) {
+        if (sub * 16 >= rows) break;
+        const int s = k % kStages;
+        if (k >= kStages && !mbar_wait(&empty[s], ((k / kStages) & 1) ^ 1, timeout_ns)) {
+          ok = false;
+          break;
+        }
+        if (*abort_flag) { ok = false; break; }
+        const int y = ((u * d.C + slot) * d.bs) + sub * 16;
+        unsigned char* st = smem + s * kStage;
+        mbar_arrive_expect_tx(&full[s], kStage);
+        tma_load_2d(st, &tmK, 0, y, &full[s]);
+        tma_load_2d(st + 16 * 128, &tmK, 64, y, &full[s]);
+        tma_load_2d(st + kTile, &tmV, 0, y, &full[s]);
+        tma_load_2d(st + kTile + 16 * 128, &tmV, 64, y, &full[s]);
+        ++k;
+      }
+    }
+    if (!ok) {
+      set_error(L.err, KVS_ERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    // do not leave while tensor loads into this CTA's shared memory may be in flight
+    for (int j = max(0, k - kStages); j < k; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1, timeout_ns);
+    return;
+  }
+
+  // -------------------------------------------------------------------- consumers
+  const int G = d.G;
+  const float sl2 = d.scale * kLog2e;
+  const int u_first = (int)(p0 / d.Kb), u_last = (int)((p1 - 1) / d.Kb);
+  int k = 0;          // position in the CTA's tile sequence
+  bool ok = true;
+  for (int u = u_first; u <= u_last; ++u) {
+    const int r = u / d.Hkv, h = u % d.Hkv;
+    const int len = ctx_len[r];
+    const int n = nsel[u];
+    // queries of the group as m16n8k16 A fragments (rows >= G are zero)
+    uint32_t qa[D / 16][4];
+    {
+      const int g0 = lane >> 2, g1 = g0 + 8, c2 = (lane & 3) * 2;
+      const uint32_t* q0 = reinterpret_cast<const uint32_t*>(q + ((size_t)r * d.Hq + h * G + g0) * D);
+      const uint32_t* q1 = reinterpret_cast<const uint32_t*>(q + ((size_t)r * d.Hq + h * G + g1) * D);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        qa[ks][0] = g0 < G ? q0[(ks * 16 + c2) >> 1] : 0u;
+        qa[ks][1] = (!ROWS8 && g1 < G) ? q1[(ks * 16 + c2) >> 1] : 0u;
+        qa[ks][2] = g0 < G ? q0[(ks * 16 + 8 + c2) >> 1] : 0u;
+        qa[ks][3] = (!ROWS8 && g1 < G) ? q1[(ks * 16 + 8 + c2) >> 1] : 0u;
+      }
+    }
+    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    float oacc[D / 8][4];
+#pragma unroll
+    for (int x = 0; x < D / 8; ++x) oacc[x][0] = oacc[x][1] = oacc[x][2] = oacc[x][3] = 0.f;
+
+    const long long pu0 = max(p0, (long long)u * d.Kb), pu1 = min(p1, (long long)(u + 1) * d.Kb);
+    for (long long p = pu0; p < pu1 && ok; ++p) {
+      const int i = (int)(p - (long long)u * d.Kb);
+      if (i >= n) continue;
+      const int blk = sel[(size_t)u * d.Kb + i];
+      const int rows = rows_present(len, blk, d.bs);
+      for (int sub = 0; sub < subs; ++sub) {
+        if (sub * 16 >= rows) break;
+        const int kk = k++;
+        if ((kk % kConsumers) != warp) continue;
+        const int s = kk % kStages;
+        if (!mbar_wait(&full[s], (kk / kStages) & 1, timeout_ns)) {
+          ok = false;
+          break;
+        }
+        const unsigned char* kt = smem + s * kStage;
+        const unsigned char* vt = kt + kTile;
+        const int valid_rows = rows - sub * 16;     // tokens of this tile before the context end
+        // S = Q K^T
+        float sacc[2][4];
+#pragma unroll
+        for (int nn = 0; nn < 2; ++nn) sacc[nn][0] = sacc[nn][1] = sacc[nn][2] = sacc[nn][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t b0, b1, b2, b3;
+          const int trow = (lane & 7) + (lane >> 4) * 8;
+          const int kcol = ks * 16 + ((lane >> 3) & 1) * 8;
+          ldmatrix_x4(b0, b1, b2, b3, kt + sw128_offset(trow, kcol, 16));
+          mma_bf16_16816(sacc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+          mma_bf16_16816(sacc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+        }
+        // online softmax in the log2 domain; tokens past the context end are masked
+        float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+        for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int tok = nn * 8 + (lane & 3) * 2 + e;
+            const bool valid = tok < valid_rows;
+            const float slo = valid ? sacc[nn][e] * sl2 : -INFINITY;
+            const float shi = valid ? sacc[nn][2 + e] * sl2 : -INFINITY;
+            sacc[nn][e] = slo;
+            sacc[nn][2 + e] = shi;
+            mx_lo = fmaxf(mx_lo, slo);
+            mx_hi = fmaxf(mx_hi, shi);
+          }
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+        const float al_lo = mn_lo == -INFINITY ? 1.f : exp2f(m_lo - mn_lo);
+        const float al_hi = mn_hi == -INFINITY ? 1.f : exp2f(m_hi - mn_hi);
+        float ps_lo = 0.f, ps_hi = 0.f;
+#pragma unroll
+        for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float plo = mn_lo == -INFINITY ? 0.f : exp2f(sacc[nn][e] - mn_lo);
+            const float phi = mn_hi == -INFINITY ? 0.f : exp2f(sacc[nn][2 + e] - mn_hi);
+            sacc[nn][e] = plo;
+            sacc[nn][2 + e] = phi;
+            ps_lo += plo;
+            ps_hi += phi;
+          }
+        ps_lo += __shfl_xor_sync(0xffffffffu, ps_lo, 1);
+        ps_lo += __shfl_xor_sync(0xffffffffu, ps_lo, 2);
+        ps_hi += __shfl_xor_sync(0xffffffffu, ps_hi, 1);
+        ps_hi += __shfl_xor_sync(0xffffffffu, ps_hi, 2);
+        l_lo = l_lo * al_lo + ps_lo;
+        l_hi = l_hi * al_hi + ps_hi;
+        m_lo = mn_lo;
+        m_hi = mn_hi;
+        uint32_t ph[4], pl[4];
+        auto split2 = [](float a, float b, uint32_t& hi, uint32_t& lo) {
+          hi = pack_bf16x2(a, b);
+          lo = pack_bf16x2(a - bf16_lo(hi), b - bf16_hi(hi));
+        };
+        split2(sacc[0][0], sacc[0][1], ph[0], pl[0]);
+        split2(sacc[0][2], sacc[0][3], ph[1], pl[1]);
+        split2(sacc[1][0], sacc[1][1], ph[2], pl[2]);
+        split2(sacc[1][2], sacc[1][3], ph[3], pl[3]);
+#pragma unroll
+        for (int nd = 0; nd < D / 8; nd += 2) {
+          oacc[nd][0] *= al_lo; oacc[nd][1] *= al_lo; oacc[nd][2] *= al_hi; oacc[nd][3] *= al_hi;
+          oacc[nd + 1][0] *= al_lo; oacc[nd + 1][1] *= al_lo; oacc[nd + 1][2] *= al_hi; oacc[nd + 1][3] *= al_hi;
+          uint32_t b0, b1, b2, b3;
+          const int trow = (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int col = nd * 8 + (lane >> 4) * 8;
+          ldmatrix_x4_trans(b0, b1, b2, b3, vt + sw128_offset(trow, col, 16));
+          mma_bf16_16816(oacc[nd], ph[0], ph[1], ph[2], ph[3], b0, b1);
+          mma_bf16_16816(oacc[nd], pl[0], pl[1], pl[2], pl[3], b0, b1);
+          mma_bf16_16816(oacc[nd + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+          mma_bf16_16816(oacc[nd + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+      }
+    }
+    if (!ok) break;
+    // partial state of this warp for unit u
+    const int seg = c - (int)(((long long)u * d.Kb) / plan.per_cta);
+    const size_t pidx = ((size_t)u * plan.max_segs + seg) * kConsumers + warp;
+    const int row_lo = lane >> 2, row_hi = row_lo + 8;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int row = hh ? row_hi : row_lo;
+      if (row >= G) continue;
+      float* dst = L.attn_part + (pidx * G + row) * D;
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd) {
+        const int col = nd * 8 + (lane & 3) * 2;
+        dst[col] = oacc[nd][hh * 2];
+        dst[col + 1] = oacc[nd][hh * 2 + 1];
+      }
+      if ((lane & 3) == 0) {
+        L.attn_ml[(pidx * G + row) * 2 + 0] = hh ? m_hi : m_lo;
+        L.attn_ml[(pidx * G + row) * 2 + 1] = hh ? l_hi : l_lo;
+      }
+    }
+  }
+  if (!ok) {
+    set_error(L.err, KVS_ERR_TIMEOUT);
+    *abort_flag = 1;
+  }
+}
+
+// Merge the partials of each (unit, q head): one thread per output column.
+__global__ void __launch_bounds__(128) attn_tma_combine(Dims d, Layer L, float* __restrict__ out, Plan plan) {
+  const int u = blockIdx.x, g = blockIdx.y;
+  const int r = u / d.Hkv, h = u % d.Hkv;
+  const int c0 = (int)(((long long)u * d.Kb) / plan.per_cta);
+  const int c1 = min(plan.n_cta - 1, (int)(((long long)(u + 1) * d.Kb - 1) / plan.per_cta));
+  const int np = (c1 - c0 + 1) * kConsumers;
+  const size_t base = (size_t)u * plan.max_segs * kConsumers;
+  float M = -INFINITY;
+  for (int p = 0; p < np; ++p) M = fmaxf(M, L.attn_ml[((base + p) * d.G + g) * 2]);
+  float lsum = 0.f;
+  if (M != -INFINITY)
+    for (int p = 0; p < np; ++p) {
+      const float mp = L.attn_ml[((base + p) * d.G + g) * 2];
+      if (mp != -INFINITY) lsum += exp2f(mp - M) * L.attn_ml[((base + p) * d.G + g) * 2 + 1];
+    }
+  for (int col = threadIdx.x; col < D; col += blockDim.x) {
+    float o = 0.f;
+    if (M != -INFINITY)
+      for (int p = 0; p < np; ++p) {
+        const float mp = L.attn_ml[((base + p) * d.G + g) * 2];
+        if (mp != -INFINITY) o += exp2f(mp - M) * L.attn_part[((base + p) * d.G + g) * D + col];
+      }
+    out[((size_t)r * d.Hq + h * d.G + g) * d.dv + col] = lsum > 0.f ? o / lsum : 0.f;
+  }
+}
+
+int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 152;
+  }
+  return n;
+}
+
+}  // namespace
+
+int attention_tma_supported(const Dims& d) {
+  return !d.v_shares_k && d.dk == D && d.dv == D && d.G <= 16 && d.bs % 16 == 0;
+}
+
+// Partial-result slots per unit the TMA path needs (segments x consumer warps).
+int attention_tma_partials(const Dims& d) { return make_plan(d, sm_count()).max_segs * kConsumers; }
+
+cudaError_t launch_attention_tma(const Dims& d, const Layer& L, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                 const __nv_bfloat16* q, const int* sel, const int* slot_of_sel, const int* nsel,
+                                 const int* ctx_len, float* out, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_tma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  Plan plan = make_plan(d, sm_count());
+  if (d.G <= 8)
+    attn_tma_kernel<true><<<plan.n_cta, (kConsumers + 1) * 32, kSmem, s>>>(*tmK, *tmV, d, L, q, sel, slot_of_sel,
+                                                                         nsel, ctx_len, plan);
+  else
+    attn_tma_kernel<false><<<plan.n_cta, (kConsumers + 1) * 32, kSmem, s>>>(*tmK, *tmV, d, L, q, sel, slot_of_sel,
+                                                                          nsel, ctx_len, plan);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_tma_combine<<<dim3(d.U, d.G), 128, 0, s>>>(d, L, out, plan);
+  return cudaGetLastError();
+}
+
+}  // namespace kvs

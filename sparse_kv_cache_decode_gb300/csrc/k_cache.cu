@@ -328,35 +328,91 @@ __global__ void __launch_bounds__(kCacheThreads) prefetch_kernel(Dims d, Layer L
   }
 }
 
-// Zero-copy fetch: warps walk the (unit, item) list; each item copies the present rows of one
-// block from the mapped host history into its slot with 16-byte loads, 4 in flight per lane.
-__device__ __forceinline__ void copy_rows(const uint4* __restrict__ src, uint4* __restrict__ dst, int nvec, int lane) {
-  int v = lane;
-  for (; v + 96 < nvec; v += 128) {
-    uint4 a = src[v], b = src[v + 32], c = src[v + 64], e = src[v + 96];
-    dst[v] = a; dst[v + 32] = b; dst[v + 64] = c; dst[v + 96] = e;
-  }
-  for (; v < nvec; v += 32) dst[v] = src[v];
-}
+// Zero-copy fetch with a small persistent grid, so that it leaves the SMs to the compute
+// kernels that run beside it: the CTAs flatten the (unit, item) lists with a prefix sum over
+// units; each warp copies batches of whole items (about 256 16-byte vectors per batch), 8 loads
+// in flight per lane, from the mapped host history into the items' slots.  Only rows < L are
+// copied.
+constexpr int kFetchCTAs = 48;
+constexpr int kFetchMaxUnits = 1024;
+constexpr int kFetchUnroll = 8;
 
-__global__ void __launch_bounds__(256) fetch_kernel(Dims d, Layer L, const int* __restrict__ ctx_len, int max_items) {
-  const int lane = threadIdx.x & 31;
-  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
-  const long long total = (long long)d.U * max_items;
-  for (long long w = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += nwarps) {
-    const int u = (int)(w / max_items), j = (int)(w % max_items);
-    if (j >= L.n_fetch[u]) continue;
-    const int b = L.fetch_blk[(size_t)u * d.C + j], s = L.fetch_slot[(size_t)u * d.C + j];
-    const int len = ctx_len[u / d.Hkv];
-    const int rows = min(d.bs, len - b * d.bs);
-    if (rows <= 0) continue;
-    const size_t t0 = (size_t)u * d.max_ctx + (size_t)b * d.bs;
-    const size_t slot_row = ((size_t)u * d.C + s) * d.bs;
-    copy_rows(reinterpret_cast<const uint4*>(L.host_k + t0 * d.dk), reinterpret_cast<uint4*>(L.kpool + slot_row * d.dk),
-              rows * d.dk / 8, lane);
-    if (!d.v_shares_k)
-      copy_rows(reinterpret_cast<const uint4*>(L.host_v + t0 * d.dv),
-                reinterpret_cast<uint4*>(L.vpool + slot_row * d.dv), rows * d.dv / 8, lane);
+__global__ void __launch_bounds__(256) fetch_kernel(Dims d, Layer L, const int* __restrict__ ctx_len) {
+  __shared__ int s_off[kFetchMaxUnits + 1];
+  __shared__ int ws[33];
+  const int tid = threadIdx.x, lane = tid & 31;
+  // prefix sum of the per-unit item counts
+  const int per = (d.U + blockDim.x - 1) / blockDim.x;
+  const int u0 = min(d.U, tid * per), u1 = min(d.U, u0 + per);
+  int mine = 0;
+  for (int u = u0; u < u1; ++u) mine += L.n_fetch[u];
+  int total;
+  int off = block_excl_sum(mine, ws, &total);
+  for (int u = u0; u < u1; ++u) { s_off[u] = off; off += L.n_fetch[u]; }
+  if (tid == 0) s_off[d.U] = total;
+  __syncthreads();
+
+  const int vk = d.bs * d.dk / 8;                         // 16-byte vectors of K in a full block
+  const int vv = d.v_shares_k ? 0 : d.bs * d.dv / 8;
+  const int vpi = vk + vv;
+  const int ipb = max(1, 256 / vpi);                      // items per warp batch
+  const int n_batches = (total + ipb - 1) / ipb;
+  const int gwarp = blockIdx.x * (blockDim.x >> 5) + (tid >> 5);
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int batch = gwarp; batch < n_batches; batch += nwarps) {
+    const int i0 = batch * ipb, ni = min(ipb, total - i0);
+    // lane k < ni locates item i0 + k: unit by binary search over s_off, then its block and slot
+    int my_u = 0, my_rows = 0;
+    size_t my_src = 0, my_dst = 0;
+    if (lane < ni) {
+      int item = i0 + lane;
+      int lo = 0, hi = d.U;                               // s_off[lo] <= item < s_off[hi]
+      while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (s_off[mid] <= item) lo = mid; else hi = mid;
+      }
+      my_u = lo;
+      const int j = item - s_off[lo];
+      const int b = L.fetch_blk[(size_t)lo * d.C + j], s = L.fetch_slot[(size_t)lo * d.C + j];
+      const int len = ctx_len[lo / d.Hkv];
+      my_rows = max(0, min(d.bs, len - b * d.bs));
+      my_src = (size_t)lo * d.max_ctx + (size_t)b * d.bs;   // first host row of the block
+      my_dst = ((size_t)lo * d.C + s) * d.bs;               // first slot row
+    }
+    const int nv = ni * vpi;
+    for (int base = 0; base < nv; base += 32 * kFetchUnroll) {
+      uint4 val[kFetchUnroll];
+      const uint4* src[kFetchUnroll];
+      uint4* dst[kFetchUnroll];
+#pragma unroll
+      for (int k = 0; k < kFetchUnroll; ++k) {
+        const int f = base + k * 32 + lane;
+        const int it = f / vpi, w = f - (f / vpi) * vpi;
+        const int rows = __shfl_sync(0xffffffffu, my_rows, it < ni ? it : 0);
+        const size_t sr = __shfl_sync(0xffffffffu, my_src, it < ni ? it : 0);
+        const size_t dr = __shfl_sync(0xffffffffu, my_dst, it < ni ? it : 0);
+        src[k] = nullptr;
+        dst[k] = nullptr;
+        if (f < nv) {
+          if (w < vk) {
+            if (w < rows * d.dk / 8) {
+              src[k] = reinterpret_cast<const uint4*>(L.host_k + sr * d.dk) + w;
+              dst[k] = reinterpret_cast<uint4*>(L.kpool + dr * d.dk) + w;
+            }
+          } else {
+            const int w2 = w - vk;
+            if (w2 < rows * d.dv / 8) {
+              src[k] = reinterpret_cast<const uint4*>(L.host_v + sr * d.dv) + w2;
+              dst[k] = reinterpret_cast<uint4*>(L.vpool + dr * d.dv) + w2;
+            }
+          }
+        }
+        if (src[k]) val[k] = *src[k];
+      }
+#pragma unroll
+      for (int k = 0; k < kFetchUnroll; ++k)
+        if (dst[k]) *dst[k] = val[k];
+    }
   }
 }
 
@@ -385,10 +441,8 @@ cudaError_t launch_prefetch(const Dims& d, const Layer& L, const int* hint, cons
 }
 
 cudaError_t launch_fetch(const Dims& d, const Layer& L, const int* ctx_len, cudaStream_t s) {
-  int max_items = max_victims(d);
-  long long warps = (long long)d.U * max_items;
-  int blocks = (int)std::min<long long>((warps + 7) / 8, 8 * 152);
-  fetch_kernel<<<blocks, 256, 0, s>>>(d, L, ctx_len, max_items);
+  if (d.U > kFetchMaxUnits) return cudaErrorInvalidValue;
+  fetch_kernel<<<kFetchCTAs, 256, 0, s>>>(d, L, ctx_len);
   return cudaGetLastError();
 }
 

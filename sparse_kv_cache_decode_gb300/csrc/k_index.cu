@@ -116,6 +116,27 @@ cudaError_t launch_append(const Dims& d, const Layer& L, const __nv_bfloat16* k_
   return cudaGetLastError();
 }
 
+// One 16-byte read per 4 KiB page of a mapped host range, so the device's translations of the
+// whole history exist before the first decode step fetches from it.  The loaded words are folded
+// into *sink only to keep the loads.
+__global__ void __launch_bounds__(256) touch_pages_kernel(const uint4* __restrict__ base, size_t n_pages,
+                                                          unsigned* sink) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  unsigned acc = 0;
+  for (size_t p = (size_t)blockIdx.x * blockDim.x + threadIdx.x; p < n_pages; p += stride) {
+    uint4 v = base[p * 256];  // 4096 / 16
+    acc ^= v.x ^ v.w;
+  }
+  if (acc == 0x9e3779b9u) atomicAdd(sink, 1u);
+}
+
+cudaError_t launch_touch_pages(const void* base, size_t bytes, unsigned* sink, cudaStream_t s) {
+  size_t n_pages = bytes / 4096;
+  if (n_pages == 0) return cudaSuccess;
+  touch_pages_kernel<<<4 * 152, 256, 0, s>>>(static_cast<const uint4*>(base), n_pages, sink);
+  return cudaGetLastError();
+}
+
 __global__ void advance_kernel(int B, int* ctx_len) {
   int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r < B) ctx_len[r] += 1;

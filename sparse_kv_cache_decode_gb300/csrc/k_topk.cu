@@ -12,7 +12,7 @@ namespace kvs {
 
 namespace {
 
-constexpr int kTopkThreads = 1024;
+constexpr int kTopkThreads = 512;
 constexpr int kTopkSmemKeys = 16384;  // scores cached in shared memory up to this many blocks
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(Dims d, const float* __restrict__ scores,

@@ -1,10 +1,14 @@
 // libkvs host side: configuration checks, workspace carving and the C-ABI entry points.
 #include <math.h>
+
+#include <algorithm>
 #include <stdio.h>
 #include <string.h>
 
 #include <new>
 #include <vector>
+
+#include <cudaTypedefs.h>
 
 #include "kvs_common.cuh"
 
@@ -22,11 +26,15 @@ struct kvs_ctx {
   std::vector<int> booted;          // lookahead: layer has a pending selection
   std::vector<cudaEvent_t> fetch_done;
   std::vector<int> fetch_pending;
+  std::vector<CUtensorMap> tmaps;   // per layer: K pool, V pool (TMA attention path)
   cudaEvent_t fork;
   // diagnostics
   unsigned long long launches = 0;
-  int timer_kernel = 0, timer_count = 0;
-  std::vector<cudaEvent_t> timer_start, timer_stop;
+  struct Timer {
+    int count = 0;
+    std::vector<cudaEvent_t> start, stop;
+  };
+  Timer timers[KVS_K_INDEX + 1];
 };
 
 namespace {
@@ -40,6 +48,7 @@ bool fill_dims(const kvs_config* c, Dims* d) {
   if (c->n_req < 1 || c->n_layer < 1 || c->n_q_head < 1 || c->n_kv_head < 1) return false;
   if (c->n_q_head % c->n_kv_head) return false;
   if (c->n_req > 4096 || c->n_layer > 1024 || c->n_kv_head > 1024) return false;
+  if ((long long)c->n_req * c->n_kv_head > 1024) return false;   // units per layer
   if (c->d_k < 8 || c->d_k % 8 || c->d_v < 8 || c->d_v % 8) return false;
   if (c->v_shares_k != 0 && c->v_shares_k != 1) return false;
   if (c->v_shares_k && c->d_v > c->d_k) return false;
@@ -107,8 +116,10 @@ Plan plan_of(const Dims& d) {
                 p.nsel + p.sos + p.fblk + p.fslot + p.nfetch;
   p.err = align_up(16);
   p.scores = align_up(U * d.nb_max * 4);
-  p.part = align_up(U * (size_t)kAttnSplitMax * d.G * d.dv * 4);
-  p.ml = align_up(U * (size_t)kAttnSplitMax * d.G * 2 * 4);
+  size_t parts = kAttnSplitMax;
+  if (attention_tma_supported(d)) parts = std::max<size_t>(parts, (size_t)attention_tma_partials(d));
+  p.part = align_up(U * parts * d.G * d.dv * 4);
+  p.ml = align_up(U * parts * d.G * 2 * 4);
   p.total = p.per_layer * d.NL + p.err + p.scores + p.part + p.ml;
   return p;
 }
@@ -120,13 +131,21 @@ inline bool layer_ok(const kvs_ctx* c, int layer) { return c && layer >= 0 && la
 // Brackets one launcher call with the armed timer's events and counts its kernels.
 template <class F>
 cudaError_t timed(kvs_ctx* c, int kernel, cudaStream_t s, int n_kernels, F&& launch) {
-  bool on = c->timer_kernel == kernel && c->timer_count < (int)c->timer_start.size();
+  kvs_ctx::Timer* t = (kernel > 0 && kernel <= KVS_K_INDEX) ? &c->timers[kernel] : nullptr;
+  bool on = t && t->count < (int)t->start.size();
   cudaError_t e = cudaSuccess;
-  if (on) e = cudaEventRecord(c->timer_start[c->timer_count], s);
+  // inside a stream capture the records must be external to become event-record nodes
+  unsigned flags = cudaEventRecordDefault;
+  if (on) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cap);
+    if (cap == cudaStreamCaptureStatusActive) flags = cudaEventRecordExternal;
+  }
+  if (on && e == cudaSuccess) e = cudaEventRecordWithFlags(t->start[t->count], s, flags);
   if (e == cudaSuccess) e = launch();
   if (e == cudaSuccess && on) {
-    e = cudaEventRecord(c->timer_stop[c->timer_count], s);
-    ++c->timer_count;
+    e = cudaEventRecordWithFlags(t->stop[t->count], s, flags);
+    ++t->count;
   }
   if (e == cudaSuccess) c->launches += n_kernels;
   return e;
@@ -134,12 +153,37 @@ cudaError_t timed(kvs_ctx* c, int kernel, cudaStream_t s, int n_kernels, F&& lau
 
 int attn_kernels(const Dims& d) {
   // attention kernel, plus the split combine when the selection is split across CTAs
+  if (attention_tma_supported(d)) return 2;
   int n_split = 1, bps = 0;
   if (!attention_split(d, &n_split, &bps)) return 1;
   return n_split > 1 ? 2 : 1;
 }
 
 inline cudaStream_t S(kvs_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// 2D tensor map over a slot pool viewed as [rows][d] bf16, boxes of 64 columns x 16 rows with
+// the 128-byte swizzle (the layout the TMA attention kernel reads with ldmatrix).
+bool make_pool_map(CUtensorMap* m, void* base, size_t rows, int d) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+      cudaGetLastError();
+      return false;
+    }
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -204,7 +248,10 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
     L.attn_ml = ml;
     L.host_k = L.host_v = nullptr;
     L.err = c->err;
-    cudaError_t e = cudaSuccess;
+    // slot pools start zeroed: rows past a context end that a tile still reads are then zeros
+    // or earlier (finite) history rows, never uninitialised bit patterns
+    cudaError_t e = cudaMemset(L.kpool, 0, p.kpool);
+    if (e == cudaSuccess && L.vpool) e = cudaMemset(L.vpool, 0, p.vpool);
     if (e == cudaSuccess) e = cudaMemset(L.block2slot, 0xff, p.b2s);
     if (e == cudaSuccess) e = cudaMemset(L.slot2block, 0xff, p.s2b);
     if (e == cudaSuccess) e = cudaMemset(L.stamp, 0, p.stamp);
@@ -219,6 +266,21 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   if (cudaMemset(c->err, 0, p.err) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     delete c;
     return KVS_ERR_CUDA;
+  }
+  if (attention_tma_supported(d)) {
+    c->tmaps.resize(2 * (size_t)d.NL);
+    const size_t rows = (size_t)d.U * d.C * d.bs;
+    for (int l = 0; l < d.NL; ++l) {
+      if (!make_pool_map(&c->tmaps[2 * l], c->layers[l].kpool, rows, d.dk) ||
+          !make_pool_map(&c->tmaps[2 * l + 1], c->layers[l].vpool, rows, d.dv)) {
+        c->tmaps.clear();
+        break;
+      }
+    }
+  }
+  for (int l = 0; l < d.NL; ++l) {
+    c->layers[l].tmK = c->tmaps.empty() ? nullptr : &c->tmaps[2 * l];
+    c->layers[l].tmV = c->tmaps.empty() ? nullptr : &c->tmaps[2 * l + 1];
   }
   c->booted.assign(d.NL, 0);
   c->fetch_done.assign(d.NL, nullptr);
@@ -237,34 +299,35 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
 }
 
 kvs_status kvs_kernel_timer_arm(kvs_ctx* c, int kernel, int capacity) {
-  if (!c || capacity < 0 || kernel < 0 || kernel > KVS_K_INDEX) return KVS_ERR_INVALID_ARG;
-  while ((int)c->timer_start.size() < capacity) {
+  if (!c || capacity < 0 || kernel < 1 || kernel > KVS_K_INDEX) return KVS_ERR_INVALID_ARG;
+  kvs_ctx::Timer& t = c->timers[kernel];
+  while ((int)t.start.size() < capacity) {
     cudaEvent_t a, b;
     if (cudaEventCreate(&a) != cudaSuccess) return KVS_ERR_CUDA;
     if (cudaEventCreate(&b) != cudaSuccess) { cudaEventDestroy(a); return KVS_ERR_CUDA; }
-    c->timer_start.push_back(a);
-    c->timer_stop.push_back(b);
+    t.start.push_back(a);
+    t.stop.push_back(b);
   }
-  while ((int)c->timer_start.size() > capacity) {
-    cudaEventDestroy(c->timer_start.back()); c->timer_start.pop_back();
-    cudaEventDestroy(c->timer_stop.back()); c->timer_stop.pop_back();
+  while ((int)t.start.size() > capacity) {
+    cudaEventDestroy(t.start.back()); t.start.pop_back();
+    cudaEventDestroy(t.stop.back()); t.stop.pop_back();
   }
-  c->timer_kernel = capacity ? kernel : 0;
-  c->timer_count = 0;
+  t.count = 0;
   return KVS_OK;
 }
 
-kvs_status kvs_kernel_timer_read(kvs_ctx* c, double* total_ms, int* n_timed) {
-  if (!c || !total_ms || !n_timed) return KVS_ERR_INVALID_ARG;
+kvs_status kvs_kernel_timer_read(kvs_ctx* c, int kernel, double* total_ms, int* n_timed) {
+  if (!c || !total_ms || !n_timed || kernel < 1 || kernel > KVS_K_INDEX) return KVS_ERR_INVALID_ARG;
+  kvs_ctx::Timer& t = c->timers[kernel];
   double tot = 0.0;
-  for (int i = 0; i < c->timer_count; ++i) {
+  for (int i = 0; i < t.count; ++i) {
     float ms = 0.f;
-    if (cudaEventSynchronize(c->timer_stop[i]) != cudaSuccess) return KVS_ERR_CUDA;
-    if (cudaEventElapsedTime(&ms, c->timer_start[i], c->timer_stop[i]) != cudaSuccess) return KVS_ERR_CUDA;
+    if (cudaEventSynchronize(t.stop[i]) != cudaSuccess) return KVS_ERR_CUDA;
+    if (cudaEventElapsedTime(&ms, t.start[i], t.stop[i]) != cudaSuccess) return KVS_ERR_CUDA;
     tot += ms;
   }
   *total_ms = tot;
-  *n_timed = c->timer_count;
+  *n_timed = t.count;
   return KVS_OK;
 }
 
@@ -272,8 +335,10 @@ unsigned long long kvs_launch_count(kvs_ctx* c) { return c ? c->launches : 0ull;
 
 kvs_status kvs_destroy(kvs_ctx* c) {
   if (!c) return KVS_ERR_INVALID_ARG;
-  for (cudaEvent_t e : c->timer_start) cudaEventDestroy(e);
-  for (cudaEvent_t e : c->timer_stop) cudaEventDestroy(e);
+  for (auto& t : c->timers) {
+    for (cudaEvent_t e : t.start) cudaEventDestroy(e);
+    for (cudaEvent_t e : t.stop) cudaEventDestroy(e);
+  }
   for (cudaEvent_t e : c->fetch_done)
     if (e) cudaEventDestroy(e);
   if (c->fork) cudaEventDestroy(c->fork);
@@ -297,6 +362,12 @@ kvs_status kvs_bind_host_kv(kvs_ctx* c, void* h_k, void* h_v) {
   c->host_k_dev = static_cast<const __nv_bfloat16*>(dk);
   c->host_v_dev = static_cast<const __nv_bfloat16*>(dv);
   const Dims& d = c->d;
+  // touch every page once from the device: the first fetches then do not pay for translations
+  const size_t rows = (size_t)d.NL * d.U * d.max_ctx;
+  cudaError_t e = launch_touch_pages(dk, rows * d.dk * 2, c->err + 1, 0);
+  if (e == cudaSuccess && dv) e = launch_touch_pages(dv, rows * d.dv * 2, c->err + 1, 0);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return KVS_ERR_CUDA;
   for (int l = 0; l < d.NL; ++l) {
     size_t unit_rows = (size_t)d.U * d.max_ctx;
     c->layers[l].host_k = c->host_k_dev + (size_t)l * unit_rows * d.dk;

@@ -1,6 +1,7 @@
 // Internal declarations shared by the libkvs translation units (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -45,6 +46,8 @@ struct Layer {
   const __nv_bfloat16* host_k;  // device-mapped host history of this layer [B][Hkv][max_ctx][dk]
   const __nv_bfloat16* host_v;  // [B][Hkv][max_ctx][dv] or nullptr
   unsigned* err;         // sticky status word (shared by all layers)
+  const CUtensorMap* tmK; // host copies of the 2D tensor maps over the K / V slot pools (or nullptr)
+  const CUtensorMap* tmV;
 };
 
 constexpr int kAttnSplitMax = 32;
@@ -70,6 +73,7 @@ cudaError_t launch_index_build(const Dims& d, const Layer& L, __nv_bfloat16* ind
 cudaError_t launch_append(const Dims& d, const Layer& L, const __nv_bfloat16* k_new,
                           const __nv_bfloat16* v_new, __nv_bfloat16* index, const int* ctx_len, cudaStream_t s);
 cudaError_t launch_advance(int B, int* ctx_len, cudaStream_t s);
+cudaError_t launch_touch_pages(const void* base, size_t bytes, unsigned* sink, cudaStream_t s);
 cudaError_t launch_score(const Dims& d, const __nv_bfloat16* index, const __nv_bfloat16* q, int nq,
                          const int* ctx_len, float* scores, unsigned* err, cudaStream_t s);
 cudaError_t launch_topk(const Dims& d, const float* scores, const int* ctx_len, int* sel, int* nsel,
@@ -83,6 +87,11 @@ cudaError_t launch_attention(const Dims& d, const Layer& L, const __nv_bfloat16*
                              const int* slot_of_sel, const int* nsel, const int* ctx_len, float* out,
                              cudaStream_t s);
 int attention_supported(const Dims& d);
+int attention_tma_supported(const Dims& d);
+int attention_tma_partials(const Dims& d);
+cudaError_t launch_attention_tma(const Dims& d, const Layer& L, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                 const __nv_bfloat16* q, const int* sel, const int* slot_of_sel, const int* nsel,
+                                 const int* ctx_len, float* out, cudaStream_t s);
 int attention_split(const Dims& d, int* n_split, int* blocks_per_split);
 int score_supported(const Dims& d);
 
