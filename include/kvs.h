@@ -214,6 +214,27 @@ kvs_status kvs_kernel_timer_read(kvs_ctx* ctx, int kernel, double* total_ms, int
 /* Number of kernels this context has launched (or captured into graphs) so far. */
 unsigned long long kvs_launch_count(kvs_ctx* ctx);
 
+/* Block selection that allocates nothing (no counterpart in the pages: an interface for callers
+ * that cannot allocate device memory, e.g. code running inside an allocator hook or host
+ * callback, or a plug-in in a process whose device memory another runtime owns).  Scores and
+ * selects one layer's blocks exactly as kvs_score_blocks followed by kvs_topk_select, without a
+ * kvs_ctx or workspace: the block scores live in a file-scope device array of
+ * KVS_NOALLOC_MAX_SCORES floats (8 MiB) that every GPU loading the library holds until exit.
+ *   cfg          shape and selection policy (validated like kvs_create)
+ *   d_score_q    [B][nq][H_q][d_k] bf16 scoring queries, 1 <= nq <= cfg->max_score_q
+ *   d_index_layer one layer's index keys [B][H_kv][n_b(max_ctx)][d_k] bf16
+ *   d_ctx_len    [B] int32;  d_sel [B][H_kv][K_b] int32 and d_nsel [B][H_kv] int32 outputs
+ *   d_status     optional device word that receives device-side errors (sticky; NULL: a word of
+ *                the library's own, not readable by the caller)
+ * Returns KVS_ERR_INVALID_ARG when B * H_kv * n_b(max_ctx) > KVS_NOALLOC_MAX_SCORES.  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress); make that first
+ * call before any stream capture.  All calls share the array, so calls that overlap on the GPU
+ * (other streams, other threads) race; every score a call reads is written by that same call. */
+#define KVS_NOALLOC_MAX_SCORES (1 << 21)
+kvs_status kvs_select_blocks_noalloc(const kvs_config* cfg, const void* d_score_q, int nq,
+                                     const void* d_index_layer, const int* d_ctx_len, int* d_sel, int* d_nsel,
+                                     unsigned* d_status, kvs_stream_t stream);
+
 /* Library version string. */
 const char* kvs_version(void);
 

@@ -68,6 +68,7 @@ _SIGS = {
     "kvs_kernel_timer_arm": (_I, [_P, _I, _I]),
     "kvs_kernel_timer_read": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "kvs_launch_count": (ctypes.c_ulonglong, [_P]),
+    "kvs_select_blocks_noalloc": (_I, [ctypes.POINTER(KvsConfig), _P, _I, _P, _P, _P, _P, _P, _P]),
 }
 
 KERNEL_IDS = {"score": 1, "topk": 2, "update": 3, "fetch": 4, "attn": 5, "prefetch": 6, "append": 7, "index": 8}
@@ -320,6 +321,15 @@ def pinned_host_history(shape, fill, min_huge: float = 0.95):
     t.copy_(arr.tensor)
     del arr
     return t, None, f"cudaHostAlloc (huge pages covered only {frac:.0%})"
+
+
+def select_blocks_noalloc(cfg: KvsConfig, score_q, nq: int, index_layer, ctx_len, sel, nsel, status=None,
+                          stream=None) -> None:
+    """kvs_select_blocks_noalloc: one layer's block selection with no device allocation (the
+    block scores live in a fixed device array inside the library)."""
+    _check(lib().kvs_select_blocks_noalloc(ctypes.byref(cfg), _ptr(score_q), nq, _ptr(index_layer), _ptr(ctx_len),
+                                           _ptr(sel), _ptr(nsel), _ptr(status), _stream(stream)),
+           "kvs_select_blocks_noalloc")
 
 
 def version() -> str:

@@ -124,6 +124,14 @@ Plan plan_of(const Dims& d) {
   return p;
 }
 
+}  // namespace
+
+namespace kvs {
+bool config_to_dims(const kvs_config* c, Dims* d) { return fill_dims(c, d); }
+}  // namespace kvs
+
+namespace {
+
 inline kvs_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVS_OK : KVS_ERR_CUDA; }
 
 inline bool layer_ok(const kvs_ctx* c, int layer) { return c && layer >= 0 && layer < c->d.NL; }
