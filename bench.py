@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--threads", type=int, default=0, help="generator threads (0: all cores)")
     ap.add_argument("--serial", action="store_true", help="fetch on the compute stream (kernels run one at a time)")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling cases)")
     return ap.parse_args()
 
 
@@ -290,6 +291,8 @@ def run_ours(args, dist):
     kbuild.build()
     torch.cuda.set_device(dist.local)
     w = W.WORKLOADS[args.workload]
+    if args.layers:
+        w = w.with_(n_layer=args.layers)
     if dist.world > 1:
         w = w.with_(seed=w.seed + dist.rank)       # each GPU serves its own batch of requests
     B, NL, Hkv = w.n_req, w.n_layer, w.n_kv_head
