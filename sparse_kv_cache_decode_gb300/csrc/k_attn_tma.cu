@@ -10,6 +10,8 @@
 //   O += P (16 x 16) . V (16 x 128), P split into bf16 high and low parts.
 // A warp writes its (unnormalised O, max, sum) for every unit its CTA touches; a second kernel
 // merges the partials of a unit: o = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p.
+// The CTA's block ids, slots and the units' lengths are staged in shared memory first, so the
+// producer issues tensor loads without waiting on global memory.
 // Every mbarrier wait is bounded by the context's wait timeout (KVS_ERR_TIMEOUT on expiry).
 #include <cuda.h>
 
@@ -26,7 +28,9 @@ constexpr int kConsumers = 4;
 constexpr int kCtasPerSm = 2;   // leaves registers for a fetch CTA beside them
 constexpr int kTile = 16 * D * 2;           // bytes of a 16-row K or V tile (two 64-column boxes)
 constexpr int kStage = 2 * kTile;
-constexpr int kSmem = kStages * kStage + 1024 + 2 * kStages * 8 + 64;
+constexpr int kMaxPos = 1024;               // positions (selected blocks) per CTA
+constexpr int kMaxUnits = 64;               // units one CTA's range may touch
+constexpr int kSmem = kStages * kStage + 1024 + 2 * kStages * 8 + 64 + kMaxPos * 8 + kMaxUnits * 8;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Plan {
@@ -38,7 +42,13 @@ __host__ __device__ inline Plan make_plan(const Dims& d, int n_sm) {
   const long long positions = (long long)d.U * d.Kb;
   int ctas = n_sm * kCtasPerSm;
   p.per_cta = (int)((positions + ctas - 1) / ctas);
+  // the merge kernel takes at most 1024 partials (segments x warps) of a unit
+  const int seg_cap = 1024 / kConsumers - 1;
+  const int min_per = (d.Kb + seg_cap - 1) / seg_cap;
+  if (p.per_cta < min_per) p.per_cta = min_per;
   if (p.per_cta < 1) p.per_cta = 1;
+  if (p.per_cta > kMaxPos) p.per_cta = kMaxPos;
+  if ((long long)p.per_cta > (long long)(kMaxUnits - 2) * d.Kb) p.per_cta = (kMaxUnits - 2) * d.Kb;
   p.n_cta = (int)((positions + p.per_cta - 1) / p.per_cta);
   p.max_segs = (d.Kb + p.per_cta - 1) / p.per_cta + 1;
   return p;
@@ -57,6 +67,10 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStage);
   uint64_t* empty = full + kStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+  int* m_blk = reinterpret_cast<int*>(smem + kStages * kStage + 2 * kStages * 8 + 64);   // [kMaxPos], -1: none
+  int* m_slot = m_blk + kMaxPos;                                                       // [kMaxPos]
+  int* u_len = m_slot + kMaxPos;                                                       // [kMaxUnits]
+  int* u_n = u_len + kMaxUnits;                                                        // [kMaxUnits]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x;
@@ -65,6 +79,7 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
   const int subs = d.bs / 16;
   const uint64_t timeout_ns = (uint64_t)d.timeout_us * 1000ull;
 
+  const int u_first = (int)(p0 / d.Kb), u_last = (int)((p1 - 1) / d.Kb);
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -72,6 +87,18 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
     }
     *abort_flag = 0;
     mbar_fence_init();
+  }
+  for (int j = tid; j <= u_last - u_first; j += blockDim.x) {
+    u_len[j] = ctx_len[(u_first + j) / d.Hkv];
+    u_n[j] = nsel[u_first + j];
+  }
+  __syncthreads();
+  for (int i = tid; i < (int)(p1 - p0); i += blockDim.x) {
+    const long long p = p0 + i;
+    const int u = (int)(p / d.Kb), ii = (int)(p % d.Kb);
+    const bool live = ii < u_n[u - u_first];
+    m_blk[i] = live ? sel[(size_t)u * d.Kb + ii] : -1;
+    m_slot[i] = live ? slot_of_sel[(size_t)u * d.Kb + ii] : 0;
   }
   __syncthreads();
 
@@ -83,10 +110,10 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
     int k = 0;
     bool ok = true;
     for (long long p = p0; p < p1 && ok; ++p) {
-      const int u = (int)(p / d.Kb), i = (int)(p % d.Kb);
-      if (i >= nsel[u]) continue;
-      const int blk = sel[(size_t)u * d.Kb + i], slot = slot_of_sel[(size_t)u * d.Kb + i];
-      const int rows = rows_present(ctx_len[u / d.Hkv], blk, d.bs);
+      const int u = (int)(p / d.Kb);
+      const int blk = m_blk[p - p0], slot = m_slot[p - p0];
+      if (blk < 0) continue;
+      const int rows = rows_present(u_len[u - u_first], blk, d.bs);
       for (int sub = 0; sub < subs && ok; ++sub) {
         if (sub * 16 >= rows) break;
         const int s = k % kStages;
@@ -117,13 +144,11 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
   // -------------------------------------------------------------------- consumers
   const int G = d.G;
   const float sl2 = d.scale * kLog2e;
-  const int u_first = (int)(p0 / d.Kb), u_last = (int)((p1 - 1) / d.Kb);
   int k = 0;          // position in the CTA's tile sequence
   bool ok = true;
   for (int u = u_first; u <= u_last; ++u) {
     const int r = u / d.Hkv, h = u % d.Hkv;
-    const int len = ctx_len[r];
-    const int n = nsel[u];
+    const int len = u_len[u - u_first];
     // queries of the group as m16n8k16 A fragments (rows >= G are zero)
     uint32_t qa[D / 16][4];
     {
@@ -145,9 +170,8 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
 
     const long long pu0 = max(p0, (long long)u * d.Kb), pu1 = min(p1, (long long)(u + 1) * d.Kb);
     for (long long p = pu0; p < pu1 && ok; ++p) {
-      const int i = (int)(p - (long long)u * d.Kb);
-      if (i >= n) continue;
-      const int blk = sel[(size_t)u * d.Kb + i];
+      const int blk = m_blk[p - p0];
+      if (blk < 0) continue;
       const int rows = rows_present(len, blk, d.bs);
       for (int sub = 0; sub < subs; ++sub) {
         if (sub * 16 >= rows) break;
@@ -270,29 +294,62 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
   }
 }
 
-// Merge the partials of each (unit, q head): one thread per output column.
-__global__ void __launch_bounds__(128) attn_tma_combine(Dims d, Layer L, float* __restrict__ out, Plan plan) {
-  const int u = blockIdx.x, g = blockIdx.y;
+// Merge the partials of one (unit, q head): load every partial's (max, sum) at once, then
+// o = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p with one thread per column.
+constexpr int kMergeThreads = 128;
+constexpr int kMergeMaxParts = 1024;
+
+__global__ void __launch_bounds__(kMergeThreads) attn_tma_merge(Dims d, Layer L, float* __restrict__ out, Plan plan) {
+  __shared__ float s_w[kMergeMaxParts];
+  __shared__ float s_red[kMergeThreads / 32];
+  __shared__ float s_M, s_L;
+  const int u = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
   const int r = u / d.Hkv, h = u % d.Hkv;
   const int c0 = (int)(((long long)u * d.Kb) / plan.per_cta);
   const int c1 = min(plan.n_cta - 1, (int)(((long long)(u + 1) * d.Kb - 1) / plan.per_cta));
-  const int np = (c1 - c0 + 1) * kConsumers;
+  const int np = min(kMergeMaxParts, (c1 - c0 + 1) * kConsumers);
   const size_t base = (size_t)u * plan.max_segs * kConsumers;
-  float M = -INFINITY;
-  for (int p = 0; p < np; ++p) M = fmaxf(M, L.attn_ml[((base + p) * d.G + g) * 2]);
-  float lsum = 0.f;
-  if (M != -INFINITY)
-    for (int p = 0; p < np; ++p) {
-      const float mp = L.attn_ml[((base + p) * d.G + g) * 2];
-      if (mp != -INFINITY) lsum += exp2f(mp - M) * L.attn_ml[((base + p) * d.G + g) * 2 + 1];
-    }
-  for (int col = threadIdx.x; col < D; col += blockDim.x) {
+  float mx = -INFINITY;
+  for (int p = tid; p < np; p += kMergeThreads) {
+    const float m = L.attn_ml[((base + p) * d.G + g) * 2];
+    s_w[p] = m;
+    mx = fmaxf(mx, m);
+  }
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((tid & 31) == 0) s_red[tid >> 5] = mx;
+  __syncthreads();
+  if (tid == 0) {
+    float M = -INFINITY;
+    for (int i = 0; i < kMergeThreads / 32; ++i) M = fmaxf(M, s_red[i]);
+    s_M = M;
+  }
+  __syncthreads();
+  const float M = s_M;
+  float ls = 0.f;
+  for (int p = tid; p < np; p += kMergeThreads) {
+    const float w = (M == -INFINITY || s_w[p] == -INFINITY) ? 0.f : exp2f(s_w[p] - M);
+    s_w[p] = w;
+    ls += w * L.attn_ml[((base + p) * d.G + g) * 2 + 1];
+  }
+  for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+  __syncthreads();
+  if ((tid & 31) == 0) s_red[tid >> 5] = ls;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    for (int i = 0; i < kMergeThreads / 32; ++i) t += s_red[i];
+    s_L = t;
+  }
+  __syncthreads();
+  const float lsum = s_L;
+  for (int col = tid; col < D; col += kMergeThreads) {
     float o = 0.f;
-    if (M != -INFINITY)
-      for (int p = 0; p < np; ++p) {
-        const float mp = L.attn_ml[((base + p) * d.G + g) * 2];
-        if (mp != -INFINITY) o += exp2f(mp - M) * L.attn_part[((base + p) * d.G + g) * D + col];
-      }
+#pragma unroll 8
+    for (int p = 0; p < np; ++p) {
+      const float w = s_w[p];
+      const float x = L.attn_part[((base + p) * d.G + g) * D + col];
+      o += w * x;
+    }
     out[((size_t)r * d.Hq + h * d.G + g) * d.dv + col] = lsum > 0.f ? o / lsum : 0.f;
   }
 }
@@ -337,7 +394,7 @@ cudaError_t launch_attention_tma(const Dims& d, const Layer& L, const CUtensorMa
                                                                           nsel, ctx_len, plan);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_tma_combine<<<dim3(d.U, d.G), 128, 0, s>>>(d, L, out, plan);
+  attn_tma_merge<<<dim3(d.U, d.G), kMergeThreads, 0, s>>>(d, L, out, plan);
   return cudaGetLastError();
 }
 

@@ -330,14 +330,15 @@ __global__ void __launch_bounds__(kCacheThreads) prefetch_kernel(Dims d, Layer L
 
 // Zero-copy fetch with a small persistent grid, so that it leaves the SMs to the compute
 // kernels that run beside it: the CTAs flatten the (unit, item) lists with a prefix sum over
-// units; each warp copies batches of whole items (about 256 16-byte vectors per batch), 8 loads
+// units; each warp copies batches of whole items (about 512 16-byte vectors per batch), 16 loads
 // in flight per lane, from the mapped host history into the items' slots.  Only rows < L are
 // copied.
-constexpr int kFetchCTAs = 48;
+constexpr int kFetchCTAs = 96;
+constexpr int kFetchThreads = 128;   // 10K registers per CTA: fits beside two attention CTAs
 constexpr int kFetchMaxUnits = 1024;
-constexpr int kFetchUnroll = 8;
+constexpr int kFetchUnroll = 16;
 
-__global__ void __launch_bounds__(256) fetch_kernel(Dims d, Layer L, const int* __restrict__ ctx_len) {
+__global__ void __launch_bounds__(kFetchThreads) fetch_kernel(Dims d, Layer L, const int* __restrict__ ctx_len) {
   __shared__ int s_off[kFetchMaxUnits + 1];
   __shared__ int ws[33];
   const int tid = threadIdx.x, lane = tid & 31;
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(256) fetch_kernel(Dims d, Layer L, const int* 
   const int vk = d.bs * d.dk / 8;                         // 16-byte vectors of K in a full block
   const int vv = d.v_shares_k ? 0 : d.bs * d.dv / 8;
   const int vpi = vk + vv;
-  const int ipb = max(1, 256 / vpi);                      // items per warp batch
+  const int ipb = max(1, 512 / vpi);                      // items per warp batch
   const int n_batches = (total + ipb - 1) / ipb;
   const int gwarp = blockIdx.x * (blockDim.x >> 5) + (tid >> 5);
   const int nwarps = gridDim.x * (blockDim.x >> 5);
@@ -442,7 +443,7 @@ cudaError_t launch_prefetch(const Dims& d, const Layer& L, const int* hint, cons
 
 cudaError_t launch_fetch(const Dims& d, const Layer& L, const int* ctx_len, cudaStream_t s) {
   if (d.U > kFetchMaxUnits) return cudaErrorInvalidValue;
-  fetch_kernel<<<kFetchCTAs, 256, 0, s>>>(d, L, ctx_len);
+  fetch_kernel<<<kFetchCTAs, kFetchThreads, 0, s>>>(d, L, ctx_len);
   return cudaGetLastError();
 }
 

@@ -90,7 +90,7 @@ bool fill_dims(const kvs_config* c, Dims* d) {
 struct Plan {
   size_t kpool, vpool, b2s, s2b, stamp, clock, pend_sel, pend_slot, pend_n, sel, nsel, sos, fblk, fslot, nfetch;
   size_t per_layer;
-  size_t err, scores, part, ml;
+  size_t err, scores, part, ml, done;
   size_t total;
 };
 
@@ -120,7 +120,8 @@ Plan plan_of(const Dims& d) {
   if (attention_tma_supported(d)) parts = std::max<size_t>(parts, (size_t)attention_tma_partials(d));
   p.part = align_up(U * parts * d.G * d.dv * 4);
   p.ml = align_up(U * parts * d.G * 2 * 4);
-  p.total = p.per_layer * d.NL + p.err + p.scores + p.part + p.ml;
+  p.done = align_up(U * 4);
+  p.total = p.per_layer * d.NL + p.err + p.scores + p.part + p.ml + p.done;
   return p;
 }
 
@@ -232,6 +233,7 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   float* scores = reinterpret_cast<float*>(shared + p.err);
   float* part = reinterpret_cast<float*>(shared + p.err + p.scores);
   float* ml = reinterpret_cast<float*>(shared + p.err + p.scores + p.part);
+  unsigned* done = reinterpret_cast<unsigned*>(shared + p.err + p.scores + p.part + p.ml);
   for (int l = 0; l < d.NL; ++l) {
     unsigned char* b = base + p.per_layer * l;
     Layer& L = c->layers[l];
@@ -254,6 +256,7 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
     L.scores = scores;
     L.attn_part = part;
     L.attn_ml = ml;
+    L.unit_done = done;
     L.host_k = L.host_v = nullptr;
     L.err = c->err;
     // slot pools start zeroed: rows past a context end that a tile still reads are then zeros
@@ -271,7 +274,8 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
       return KVS_ERR_CUDA;
     }
   }
-  if (cudaMemset(c->err, 0, p.err) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+  if (cudaMemset(c->err, 0, p.err) != cudaSuccess || cudaMemset(done, 0, p.done) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
     delete c;
     return KVS_ERR_CUDA;
   }

@@ -43,6 +43,7 @@ struct Layer {
   int* n_fetch;          // [U]
   float* attn_part;      // [U][n_split_max][Hq/Hkv][dv] partial outputs
   float* attn_ml;        // [U][n_split_max][Hq/Hkv][2] partial (max, sum)
+  unsigned* unit_done;   // [U] CTAs finished per unit in the current attention launch (0 between launches)
   const __nv_bfloat16* host_k;  // device-mapped host history of this layer [B][Hkv][max_ctx][dk]
   const __nv_bfloat16* host_v;  // [B][Hkv][max_ctx][dv] or nullptr
   unsigned* err;         // sticky status word (shared by all layers)
