@@ -25,10 +25,24 @@ class GpuCase:
         self.w = w
         self.K = K
         B, NL, Hkv = w.n_req, w.n_layer, w.n_kv_head
-        self.k_host = torch.empty((NL, B, Hkv, w.max_ctx, w.d_k), dtype=torch.int16, pin_memory=True)
-        self.v_host = None if w.v_shares_k else torch.empty((NL, B, Hkv, w.max_ctx, w.d_v), dtype=torch.int16,
-                                                            pin_memory=True)
-        W.fill_kv(w, self.k_host, self.v_host, n_threads)
+        kshape = (NL, B, Hkv, w.max_ctx, w.d_k)
+        vshape = None if w.v_shares_k else (NL, B, Hkv, w.max_ctx, w.d_v)
+        self._arrays = []
+        if w.host_kv_bytes >= (1 << 30):
+            # large histories: huge-page host arrays, released by close() (torch keeps freed
+            # pinned blocks cached, which would exhaust host memory across full-size tests)
+            ka = K.HostArray(kshape)
+            va = None if vshape is None else K.HostArray(vshape)
+            self.k_host, self.v_host = ka.tensor, None if va is None else va.tensor
+            W.fill_kv(w, self.k_host, self.v_host, n_threads)
+            ka.register()
+            if va is not None:
+                va.register()
+            self._arrays = [a for a in (ka, va) if a is not None]
+        else:
+            self.k_host = torch.empty(kshape, dtype=torch.int16, pin_memory=True)
+            self.v_host = None if vshape is None else torch.empty(vshape, dtype=torch.int16, pin_memory=True)
+            W.fill_kv(w, self.k_host, self.v_host, n_threads)
         self.k_np = self.k_host.numpy().view(np.uint16)
         self.v_np = None if self.v_host is None else self.v_host.numpy().view(np.uint16)
         self.ctx_lens = list(ctx_lens) if ctx_lens is not None else [w.ctx0] * B
@@ -48,6 +62,18 @@ class GpuCase:
         self.qs = W.QueryStream(w)
         self.t = 0
         torch.cuda.synchronize()
+
+    def close(self):
+        """Release the context and the host history now (full-size cases hold tens of GiB)."""
+        import gc
+        torch = torch_mod()
+        torch.cuda.synchronize()
+        self.ctx.close()
+        for a in self._arrays:
+            a.close()
+        self._arrays = []
+        self.k_host = self.v_host = self.k_np = self.v_np = None
+        gc.collect()
 
     def oracle(self, reqs=None) -> OracleDecoder:
         """Oracle on the same inputs (copies the host rows now, before any GPU append)."""
@@ -111,3 +137,52 @@ def selection_is_valid(sel, s_ref, a_ref, nb, budget, n_sink, n_recent) -> bool:
     worst_chosen = min(s_ref[b] + tol[b] for b in chosen)
     best_rest = np.max(s_ref[rest] - tol[rest])
     return worst_chosen >= best_rest
+
+
+STAT_KEYS = ["hits", "misses", "evictions", "prefetched", "prefetch_hits", "pin_fallbacks", "bytes_fetched"]
+
+
+def compare_step(g, o, out_ref, recs, cum, exact=True, frozen=None):
+    """Compare one GPU step with the oracle's on the oracle's requests: selection, cache state
+    and attention output per unit.  exact: selections must match (and per-layer counters, when
+    the oracle covers every request).  Otherwise a differing selection must be a valid top-K under
+    the score tolerance (a near tie), and that unit is frozen (its state diverges from then on)."""
+    w = g.w
+    sel = g.sel.cpu().numpy()
+    nsel = g.nsel.cpu().numpy()
+    out = g.out.cpu().numpy()
+    for l in range(w.n_layer):
+        b2s, s2b, st, clk = g.ctx.cache_export(l)
+        for ri, r in enumerate(o.reqs):
+            for h in range(w.n_kv_head):
+                u = r * w.n_kv_head + h
+                rec = recs[(l, r, h)]
+                heads = slice(h * w.group, (h + 1) * w.group)
+                if frozen is not None and (l, r, h) in frozen:
+                    continue
+                if frozen is not None and w.layer_prefetch and (l - 1, r, h) in frozen:
+                    frozen.add((l, r, h))      # its prefetch hint came from a diverged layer
+                    continue
+                got_sel = sel[l, r, h, : nsel[l, r, h]]
+                same = got_sel.tolist() == rec.sel.tolist()
+                if not same:
+                    assert not exact, f"layer {l} unit {(r, h)}: selection differs"
+                    nb = o.n_blocks(r)
+                    assert selection_is_valid(got_sel, rec.scores.astype(np.float64), rec.bound, nb,
+                                              w.budget_blocks, w.n_sink, w.n_recent), f"invalid selection {(l, r, h)}"
+                    frozen.add((l, r, h))
+                    continue
+                c = o.cache[(l, r, h)]
+                np.testing.assert_array_equal(s2b[u], c.slot2block, err_msg=f"slot2block {(l, r, h)}")
+                np.testing.assert_array_equal(st[u].astype(np.int64), c.stamp, err_msg=f"stamp {(l, r, h)}")
+                assert int(clk[u]) == c.clock
+                err = np.abs(out[l, r, heads] - out_ref[l, ri, heads]).max()
+                assert err <= 2e-3, f"layer {l} unit {(r, h)}: attention max abs err {err}"
+    if exact:
+        st_ref = o.stats(recs)
+        for l in range(w.n_layer):
+            for k in STAT_KEYS:
+                cum[l][k] += st_ref[l][k]
+        got = g.stats.cpu().numpy()
+        for l in range(w.n_layer):
+            assert [int(x) for x in got[l]] == [cum[l][k] for k in STAT_KEYS], f"stats layer {l}"

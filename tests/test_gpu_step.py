@@ -9,12 +9,10 @@ import numpy as np
 import pytest
 
 import workload as W
-from kvs_harness import GpuCase, selection_is_valid
+from kvs_harness import STAT_KEYS, GpuCase, compare_step as _compare_step
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
-
-STAT_KEYS = ["hits", "misses", "evictions", "prefetched", "prefetch_hits", "pin_fallbacks", "bytes_fetched"]
 
 INT_CASES = [
     (W.TINY.with_(name="tiny_int", n_req=2, int_scale=2.0), [4096, 3001], False),
@@ -27,48 +25,6 @@ INT_CASES = [
     (W.TINY.with_(name="tiny_bs64_int", n_req=2, block_size=64, ctx0=4000, budget_blocks=8, cap_blocks=10,
                   int_scale=2.0), [4000, 3900], False),
 ]
-
-
-def _compare_step(g, o, out_ref, recs, cum, exact=True, frozen=None):
-    w = g.w
-    sel = g.sel.cpu().numpy()
-    nsel = g.nsel.cpu().numpy()
-    out = g.out.cpu().numpy()
-    for l in range(w.n_layer):
-        b2s, s2b, st, clk = g.ctx.cache_export(l)
-        for ri, r in enumerate(o.reqs):
-            for h in range(w.n_kv_head):
-                u = r * w.n_kv_head + h
-                rec = recs[(l, r, h)]
-                heads = slice(h * w.group, (h + 1) * w.group)
-                if frozen is not None and (l, r, h) in frozen:
-                    continue
-                if frozen is not None and w.layer_prefetch and (l - 1, r, h) in frozen:
-                    frozen.add((l, r, h))      # its prefetch hint came from a diverged layer
-                    continue
-                got_sel = sel[l, r, h, : nsel[l, r, h]]
-                same = got_sel.tolist() == rec.sel.tolist()
-                if not same:
-                    assert not exact, f"layer {l} unit {(r, h)}: selection differs"
-                    nb = o.n_blocks(r)
-                    assert selection_is_valid(got_sel, rec.scores.astype(np.float64), rec.bound, nb,
-                                              w.budget_blocks, w.n_sink, w.n_recent), f"invalid selection {(l, r, h)}"
-                    frozen.add((l, r, h))
-                    continue
-                c = o.cache[(l, r, h)]
-                np.testing.assert_array_equal(s2b[u], c.slot2block, err_msg=f"slot2block {(l, r, h)}")
-                np.testing.assert_array_equal(st[u].astype(np.int64), c.stamp, err_msg=f"stamp {(l, r, h)}")
-                assert int(clk[u]) == c.clock
-                err = np.abs(out[l, r, heads] - out_ref[l, ri, heads]).max()
-                assert err <= 2e-3, f"layer {l} unit {(r, h)}: attention max abs err {err}"
-    if exact:
-        st_ref = o.stats(recs)
-        for l in range(w.n_layer):
-            for k in STAT_KEYS:
-                cum[l][k] += st_ref[l][k]
-        got = g.stats.cpu().numpy()
-        for l in range(w.n_layer):
-            assert [int(x) for x in got[l]] == [cum[l][k] for k in STAT_KEYS], f"stats layer {l}"
 
 
 @pytest.mark.parametrize("w,lens,copy_stream", INT_CASES, ids=[c[0].name for c in INT_CASES])
