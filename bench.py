@@ -255,7 +255,7 @@ def oracle_sample_time(w, steps_warm: int, steps_timed: int, n_layers: int):
 def run_reference(args, dist):
     if dist.rank != 0:
         return 0
-    w = W.WORKLOADS[args.workload]
+    w = W.get(args.workload)
     total_units = w.n_req * w.n_layer * w.n_kv_head
     n_layers = max(1, min(w.n_layer, 2))
     per_step, units, cores, desc = oracle_sample_time(w, max(1, args.warmup), max(1, args.steps), n_layers)
@@ -290,7 +290,7 @@ def run_ours(args, dist):
 
     kbuild.build()
     torch.cuda.set_device(dist.local)
-    w = W.WORKLOADS[args.workload]
+    w = W.get(args.workload)
     if args.layers:
         w = w.with_(n_layer=args.layers)
     if dist.world > 1:
@@ -369,7 +369,7 @@ def run_ours(args, dist):
             ctx.advance_ctx(ctx_len)
         for l in range(NL):
             if w.layer_prefetch and l > 0:
-                ctx.layer_prefetch(l, sel[l - 1], nsel[l - 1], ctx_len, stats, stream=cs)
+                ctx.layer_prefetch(l, sel[l - 1], nsel[l - 1], ctx_len, stats, stream=s if args.serial else cs)
             ctx.decode_step(l, qt[l], None if dt is None else dt[l], nq if dt is not None else 1, index, ctx_len,
                             out[l], stats, None if tok is None else tok[0][l],
                             None if tok is None or tok[1] is None else tok[1][l], sel[l], nsel[l], stream=s,
@@ -383,6 +383,27 @@ def run_ours(args, dist):
     with torch.cuda.stream(s):
         step(q_dev[0], None if d_dev is None else d_dev[0], tok_dev[0] if w.append else None)
     s.synchronize()
+    # On some hosts the first scattered device reads of the mapped history split part of its
+    # transparent huge pages; the device then translates 64 KiB pages on every later fetch into
+    # them, and fetches slow down many times over.  Move the history to driver-pinned memory
+    # when that happened, before the graph captures the host pointers.
+    huge_arrays = [a for a in (k_keep, v_keep) if isinstance(a, K.HostArray)]
+    if huge_arrays:
+        left = min(a.huge_fraction() for a in huge_arrays)
+        if left < 0.999:
+            k_new = torch.empty(k_host.shape, dtype=torch.int16, pin_memory=True)
+            k_new.copy_(k_host)
+            v_new = None
+            if v_host is not None:
+                v_new = torch.empty(v_host.shape, dtype=torch.int16, pin_memory=True)
+                v_new.copy_(v_host)
+            ctx.bind_host_kv(k_new, v_new)
+            for a in huge_arrays:
+                a.close()
+            k_host, v_host, k_keep, v_keep = k_new, v_new, None, None
+            host_desc = (f"cudaHostAlloc (the first step split huge pages of the mapped history: "
+                         f"{left:.0%} left)")
+            log(f"host memory: {host_desc}")
     q_fix = torch.empty_like(q_dev[0])
     d_fix = torch.empty_like(d_dev[0]) if d_dev is not None else None
     tok_fix = None

@@ -84,7 +84,7 @@ typedef struct {
   int lookahead;       /* 1: attention uses the selection made by the previous step [SPEC 3.1] */
   int max_prefetch;    /* per-unit cap of kvs_layer_prefetch; 0 -> C - K_b */
   float softmax_scale; /* 0 -> 1/sqrt(d_k) rounded to fp32 */
-  unsigned wait_timeout_us; /* bound on device waits (0 -> 20000 us) */
+  unsigned wait_timeout_us; /* bound on device waits (0 -> 2000000 us) */
 } kvs_config;
 
 /* Per-layer counters, accumulated with atomics into a caller buffer kvs_stats[N_l]. */
@@ -165,14 +165,16 @@ kvs_status kvs_decode_step(kvs_ctx* ctx, int layer, const void* d_q, const void*
                            float* d_out, kvs_stats* d_stats, int* d_sel_out, int* d_nsel_out,
                            kvs_stream_t stream, kvs_stream_t copy_stream);
 
-/* Make `stream` wait for every fetch issued on copy streams by kvs_decode_step. */
+/* Make `stream` wait for every fetch issued on copy streams by kvs_decode_step and every
+ * kvs_layer_prefetch not yet consumed by an update. */
 kvs_status kvs_join(kvs_ctx* ctx, kvs_stream_t stream);
 
 /* Cross-layer prefetch [HISP insight 3] into dst_layer (>= 1) with the hint sel/nsel of the layer
  * below: for each hint block, ascending, not resident, at most max_prefetch per unit: the victim
  * is the least recently used slot that is empty or (stamp < 2*clock and holds no hint block);
  * it is mapped, fetched from host and stamped 2*clock + 1.  Call it before dst_layer's update
- * of the same step. */
+ * of the same step; it may run on another stream: it waits for the top-K of the layer below made
+ * by kvs_decode_step, and kvs_decode_step(dst_layer) waits for it before its update. */
 kvs_status kvs_layer_prefetch(kvs_ctx* ctx, int dst_layer, const int* d_hint_sel, const int* d_hint_nsel,
                               const int* d_ctx_len, kvs_stats* d_stats, kvs_stream_t stream);
 

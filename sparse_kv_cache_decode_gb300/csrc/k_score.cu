@@ -167,11 +167,12 @@ cudaError_t launch_score_t(const Dims& d, const __nv_bfloat16* index, const __nv
 }  // namespace
 
 int score_supported(const Dims& d) {
-  return (d.dk == 128 || d.dk == 576) && d.max_nq * d.G <= kScoreMaxRows;
+  return ((d.dk == 128 || d.dk == 576) && d.max_nq * d.G <= kScoreMaxRows) || score_tc_supported(d, d.max_nq);
 }
 
 cudaError_t launch_score(const Dims& d, const __nv_bfloat16* index, const __nv_bfloat16* q, int nq,
                              const int* ctx_len, float* scores, unsigned* err, cudaStream_t s) {
+  if (score_tc_supported(d, nq)) return launch_score_tc(d, index, q, nq, ctx_len, scores, err, s);
   int R = nq * d.G;
   int np = (R + 7) / 8;
   if (np > 16 || nq < 1) return cudaErrorInvalidValue;

@@ -26,6 +26,10 @@ struct kvs_ctx {
   std::vector<int> booted;          // lookahead: layer has a pending selection
   std::vector<cudaEvent_t> fetch_done;
   std::vector<int> fetch_pending;
+  // cross-layer prefetch ordering: a layer's selection is ready (after its top-K), and the
+  // prefetch into a layer is done (before that layer's update); flags cleared by kvs_join
+  std::vector<cudaEvent_t> sel_ready, pf_done;
+  std::vector<int> sel_pending, pf_pending;
   std::vector<CUtensorMap> tmaps;   // per layer: K pool, V pool (TMA attention path)
   cudaEvent_t fork;
   // diagnostics
@@ -81,7 +85,7 @@ bool fill_dims(const kvs_config* c, Dims* d) {
   d->max_prefetch = c->max_prefetch ? c->max_prefetch : c->cap_blocks - c->budget_blocks;
   d->U = c->n_req * c->n_kv_head;
   d->scale = c->softmax_scale > 0.f ? c->softmax_scale : (float)(1.0 / sqrt((double)c->d_k));
-  d->timeout_us = c->wait_timeout_us ? c->wait_timeout_us : 20000u;
+  d->timeout_us = c->wait_timeout_us ? c->wait_timeout_us : 2000000u;
   d->row_bytes = 2 * (c->d_k + (c->v_shares_k ? 0 : c->d_v));
   return true;
 }
@@ -170,9 +174,12 @@ int attn_kernels(const Dims& d) {
 
 inline cudaStream_t S(kvs_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// 2D tensor map over a slot pool viewed as [rows][d] bf16, boxes of 64 columns x 16 rows with
-// the 128-byte swizzle (the layout the TMA attention kernel reads with ldmatrix).
-bool make_pool_map(CUtensorMap* m, void* base, size_t rows, int d) {
+}  // namespace
+
+namespace kvs {
+// 2D tensor map over a row-major bf16 matrix [rows][inner], boxes of box_inner x box_rows with the
+// 128-byte swizzle (box_inner * 2 must be 128).
+bool make_tmap_2d(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -184,14 +191,22 @@ bool make_pool_map(CUtensorMap* m, void* base, size_t rows, int d) {
     }
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-  cuuint32_t box[2] = {64, 16};
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+}  // namespace kvs
+
+namespace {
+
+// The slot pools as [U*C*bs][d] with 64 x 16 boxes (the TMA attention kernel's tiles).
+bool make_pool_map(CUtensorMap* m, void* base, size_t rows, int d) {
+  return kvs::make_tmap_2d(m, base, (uint64_t)d, (uint64_t)rows, 64, 16);
 }
 
 }  // namespace
@@ -297,6 +312,16 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   c->booted.assign(d.NL, 0);
   c->fetch_done.assign(d.NL, nullptr);
   c->fetch_pending.assign(d.NL, 0);
+  c->sel_ready.assign(d.NL, nullptr);
+  c->pf_done.assign(d.NL, nullptr);
+  c->sel_pending.assign(d.NL, 0);
+  c->pf_pending.assign(d.NL, 0);
+  for (int l = 0; l < d.NL; ++l)
+    if (cudaEventCreateWithFlags(&c->sel_ready[l], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->pf_done[l], cudaEventDisableTiming) != cudaSuccess) {
+      delete c;
+      return KVS_ERR_CUDA;
+    }
   for (int l = 0; l < d.NL; ++l)
     if (cudaEventCreateWithFlags(&c->fetch_done[l], cudaEventDisableTiming) != cudaSuccess) {
       delete c;
@@ -352,6 +377,10 @@ kvs_status kvs_destroy(kvs_ctx* c) {
     for (cudaEvent_t e : t.stop) cudaEventDestroy(e);
   }
   for (cudaEvent_t e : c->fetch_done)
+    if (e) cudaEventDestroy(e);
+  for (cudaEvent_t e : c->sel_ready)
+    if (e) cudaEventDestroy(e);
+  for (cudaEvent_t e : c->pf_done)
     if (e) cudaEventDestroy(e);
   if (c->fork) cudaEventDestroy(c->fork);
   delete c;
@@ -443,10 +472,18 @@ kvs_status kvs_layer_prefetch(kvs_ctx* c, int dst_layer, const int* d_hint_sel, 
     return KVS_ERR_INVALID_ARG;
   if (!c->host_k_dev) return KVS_ERR_HOST_MEM;
   const Layer& L = c->layers[dst_layer];
-  cudaError_t e = timed(c, KVS_K_PREFETCH, S(stream), 1, [&] {
-    return launch_prefetch(c->d, L, d_hint_sel, d_hint_nsel, d_ctx_len, d_stats, S(stream));
-  });
+  cudaError_t e = cudaSuccess;
+  // the hint is the layer below's selection of this step: wait for its top-K when that ran on
+  // another stream
+  if (c->sel_pending[dst_layer - 1]) e = cudaStreamWaitEvent(S(stream), c->sel_ready[dst_layer - 1], 0);
+  if (e == cudaSuccess)
+    e = timed(c, KVS_K_PREFETCH, S(stream), 1, [&] {
+      return launch_prefetch(c->d, L, d_hint_sel, d_hint_nsel, d_ctx_len, d_stats, S(stream));
+    });
   if (e == cudaSuccess) e = timed(c, KVS_K_FETCH, S(stream), 1, [&] { return launch_fetch(c->d, L, d_ctx_len, S(stream)); });
+  // the destination layer's next update waits for this
+  if (e == cudaSuccess) e = cudaEventRecord(c->pf_done[dst_layer], S(stream));
+  if (e == cudaSuccess) c->pf_pending[dst_layer] = 1;
   return cuda_status(e);
 }
 
@@ -494,9 +531,18 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
     return timed(c, KVS_K_SCORE, s, 1, [&] { return launch_score(d, idx, rows, n, d_ctx_len, L.scores, c->err, s); });
   };
   auto topk = [&](int* so, int* no) {
-    return timed(c, KVS_K_TOPK, s, 1, [&] { return launch_topk(d, L.scores, d_ctx_len, so, no, c->err, s); });
+    cudaError_t r = timed(c, KVS_K_TOPK, s, 1, [&] { return launch_topk(d, L.scores, d_ctx_len, so, no, c->err, s); });
+    if (r == cudaSuccess) r = cudaEventRecord(c->sel_ready[layer], s);   // hint for a prefetch into layer + 1
+    if (r == cudaSuccess) c->sel_pending[layer] = 1;
+    return r;
   };
   auto update = [&](const int* so, const int* no) {
+    cudaError_t r = cudaSuccess;
+    if (c->pf_pending[layer]) {       // a prefetch into this layer ran on another stream
+      r = cudaStreamWaitEvent(s, c->pf_done[layer], 0);
+      c->pf_pending[layer] = 0;
+    }
+    if (r != cudaSuccess) return r;
     return timed(c, KVS_K_UPDATE, s, 1,
                  [&] { return launch_cache_update(d, L, so, no, d_ctx_len, L.slot_of_sel, d_stats, s); });
   };
@@ -544,9 +590,15 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
 kvs_status kvs_join(kvs_ctx* c, kvs_stream_t stream) {
   if (!c) return KVS_ERR_INVALID_ARG;
   for (int l = 0; l < c->d.NL; ++l) {
-    if (!c->fetch_pending[l]) continue;
-    if (cudaStreamWaitEvent(S(stream), c->fetch_done[l], 0) != cudaSuccess) return KVS_ERR_CUDA;
-    c->fetch_pending[l] = 0;
+    if (c->fetch_pending[l]) {
+      if (cudaStreamWaitEvent(S(stream), c->fetch_done[l], 0) != cudaSuccess) return KVS_ERR_CUDA;
+      c->fetch_pending[l] = 0;
+    }
+    if (c->pf_pending[l]) {
+      if (cudaStreamWaitEvent(S(stream), c->pf_done[l], 0) != cudaSuccess) return KVS_ERR_CUDA;
+      c->pf_pending[l] = 0;
+    }
+    c->sel_pending[l] = 0;
   }
   return KVS_OK;
 }

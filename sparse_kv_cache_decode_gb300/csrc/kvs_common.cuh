@@ -88,6 +88,10 @@ cudaError_t launch_attention(const Dims& d, const Layer& L, const __nv_bfloat16*
                              const int* slot_of_sel, const int* nsel, const int* ctx_len, float* out,
                              cudaStream_t s);
 int attention_supported(const Dims& d);
+bool make_tmap_2d(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows);
+int score_tc_supported(const Dims& d, int nq);
+cudaError_t launch_score_tc(const Dims& d, const __nv_bfloat16* index, const __nv_bfloat16* q, int nq,
+                            const int* ctx_len, float* scores, unsigned* err, cudaStream_t s);
 int attention_tma_supported(const Dims& d);
 int attention_tma_partials(const Dims& d);
 cudaError_t launch_attention_tma(const Dims& d, const Layer& L, const CUtensorMap* tmK, const CUtensorMap* tmV,

@@ -100,13 +100,13 @@ class GpuCase:
             self.ctx.advance_ctx(self.ctx_len)
         for l in range(w.n_layer):
             if w.layer_prefetch and l > 0:
-                self.ctx.layer_prefetch(l, self.sel[l - 1], self.nsel[l - 1], self.ctx_len, self.stats)
+                self.ctx.layer_prefetch(l, self.sel[l - 1], self.nsel[l - 1], self.ctx_len, self.stats,
+                                        stream=self.copy_stream)
             self.ctx.decode_step(l, qd[l], None if dd is None else dd[l], w.n_score_q if dd is not None else 1,
                                  self.index, self.ctx_len, self.out[l], self.stats,
                                  None if nkd is None else nkd[l], None if nvd is None else nvd[l],
                                  self.sel[l], self.nsel[l], copy_stream=self.copy_stream)
-        if self.copy_stream is not None:
-            self.ctx.join()
+        self.ctx.join()
         torch.cuda.synchronize()
         self.t += 1
 

@@ -21,6 +21,8 @@ MLA_G128 = W.MLA_128K.with_(name="mla_g128_small", n_req=2, n_layer=1, ctx0=2048
 TINY3 = W.TINY.with_(name="tiny3", n_req=3)
 TINY_G8 = W.TINY.with_(name="tiny_g8", n_req=2, n_q_head=16, n_kv_head=2)
 TINY_BS64 = W.TINY.with_(name="tiny_bs64", n_req=2, block_size=64, ctx0=3000, budget_blocks=8, cap_blocks=12)
+# 16 query heads per kv head x 5 scoring queries: 80 rows per unit (the tensor-memory scoring path)
+TINY_LA_G16 = W.TINY_LOOKAHEAD.with_(name="tiny_la_g16", n_req=3, n_q_head=32, n_kv_head=2)
 
 
 def _dev(a):
@@ -53,7 +55,10 @@ def _score_rows(w, q, d, l, r, h):
 
 @pytest.mark.parametrize("w,lens", [(TINY3, [4096, 1000, 17]), (W.TINY_LOOKAHEAD.with_(n_req=2), [4096, 2222]),
                                     (TINY_G8, [4096, 4000]), (W.TINY_MLA, [4096]), (MLA_G128, [2048, 1500]),
-                                    (TINY3.with_(int_scale=2.0), [4096, 1000, 17])])
+                                    (TINY3.with_(int_scale=2.0), [4096, 1000, 17]),
+                                    (TINY_LA_G16, [4096, 1000, 17]),
+                                    (TINY_LA_G16.with_(int_scale=2.0), [4096, 2049, 129]),
+                                    (MLA_G128.with_(int_scale=1.0), [2048, 1500])])
 def test_score_blocks(w, lens):
     g = GpuCase(w, lens)
     scores = torch.full((w.n_req, w.n_kv_head, g.nb_max), float("nan"), dtype=torch.float32, device="cuda")

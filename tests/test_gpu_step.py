@@ -20,6 +20,7 @@ INT_CASES = [
     (W.TINY_LOOKAHEAD.with_(name="tiny_la_int_cs", n_req=2, int_scale=2.0), [4096, 2050], True),
     (W.TINY_APPEND.with_(name="tiny_app_int", n_req=2, int_scale=2.0), [4096, 1000], False),
     (W.TINY_PREFETCH.with_(name="tiny_pf_int", n_req=2, int_scale=2.0), [4096, 4095], False),
+    (W.TINY_PREFETCH.with_(name="tiny_pf_int_cs", n_req=2, n_layer=3, int_scale=2.0), [4096, 3333], True),
     (W.TINY_MLA.with_(name="tiny_mla_int", n_layer=2, layer_prefetch=True, rho_layer=0.8, int_scale=2.0,
                       steps=12), [4096], False),
     (W.TINY.with_(name="tiny_bs64_int", n_req=2, block_size=64, ctx0=4000, budget_blocks=8, cap_blocks=10,

@@ -216,6 +216,17 @@ WORKLOADS = {w.name: w for w in (TINY, TINY_LOOKAHEAD, TINY_APPEND, TINY_PREFETC
                                  MLA_128K)}
 
 
+def get(name: str) -> Workload:
+    """A named workload, or a sweep case named sweep_bs<B>_b<tokens>_rho<r>[_l<layers>]."""
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    import re
+    m = re.fullmatch(r"sweep_bs(\d+)_b(\d+)_rho([0-9.]+)(?:_l(\d+))?", name)
+    if not m:
+        raise KeyError(f"unknown workload {name!r}")
+    return sweep_workload(int(m.group(1)), int(m.group(2)), float(m.group(3)), int(m.group(4) or 8))
+
+
 # --------------------------------------------------------------------------- fills
 
 def _ptr(a) -> int:
