@@ -46,7 +46,9 @@
  * kvs_poll_error, kvs_destroy).  The return value reports argument and launch errors only.
  * Errors found on the device (capacity overflow, bad block id, a wait that ran out of time)
  * set a sticky status word that kvs_poll_error reads after the caller synchronises; no
- * kernel traps.  Calls on the same layer must not overlap on the GPU.
+ * kernel traps.  Calls on the same layer must not overlap on the GPU; nor may kvs_decode_step
+ * and kvs_topk_select calls on different layers, which share the workspace's block-score and
+ * top-K candidate scratch (issue them on one stream; kvs_layer_prefetch may run beside them).
  */
 #ifndef KVS_H_
 #define KVS_H_
@@ -128,7 +130,8 @@ kvs_status kvs_score_blocks(kvs_ctx* ctx, int layer, const void* d_score_q, int 
 /* Selection [SPEC 2.3, 3 step 1]: with nb = n_b(ctx_len[r]), all blocks when nb <= K_b; else the
  * sink blocks [0, n_sink), the recent blocks [nb - n_recent, nb) and the top K_b - |forced| other
  * blocks by (score desc, block asc), NaN below -inf, -0.0 == +0.0.  Output ascending in
- * sel[r][h][0 .. nsel-1]; nsel = min(K_b, nb). */
+ * sel[r][h][0 .. nsel-1]; nsel = min(K_b, nb).  When n_b(max_ctx) exceeds 16384 blocks the
+ * selection runs in two phases over chunks of 16384 blocks (same result). */
 kvs_status kvs_topk_select(kvs_ctx* ctx, const float* d_scores, const int* d_ctx_len, int* d_sel, int* d_nsel,
                            kvs_stream_t stream);
 

@@ -63,6 +63,6 @@ extern "C" kvs_status kvs_select_blocks_noalloc(const kvs_config* cfg, const voi
   unsigned* err = d_status ? d_status : status;
   cudaError_t e = kvs::launch_score(d, static_cast<const __nv_bfloat16*>(d_index_layer),
                                     static_cast<const __nv_bfloat16*>(d_score_q), nq, d_ctx_len, scores, err, s);
-  if (e == cudaSuccess) e = kvs::launch_topk(d, scores, d_ctx_len, d_sel, d_nsel, err, s);
+  if (e == cudaSuccess) e = kvs::launch_topk(d, scores, d_ctx_len, d_sel, d_nsel, err, s, nullptr);
   return e == cudaSuccess ? KVS_OK : KVS_ERR_CUDA;
 }

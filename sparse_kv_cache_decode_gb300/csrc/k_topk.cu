@@ -5,6 +5,13 @@
 // threshold key T of the k-th best candidate and how many candidates equal to T are needed;
 // an ordered compaction (prefix sums in block order) then takes every candidate above T and
 // the lowest-index candidates equal to T.
+//
+// Long contexts (more blocks than one CTA caches in shared memory) select in two phases so that
+// the work spreads over the SMs: (1) a grid of (chunk, unit) CTAs keeps, per chunk of 16384
+// blocks, the chunk's own top-k candidates under the same order, in block order; (2) one CTA
+// per unit selects the top-k among the kept candidates.  Every candidate of the unit's top-k is
+// within the top-k of its own chunk (the candidates that precede it in the order are fewer
+// than k), so the two phases select exactly the single-pass result.
 #include "kvs_block.cuh"
 #include "kvs_common.cuh"
 
@@ -14,6 +21,8 @@ namespace {
 
 constexpr int kTopkThreads = 512;
 constexpr int kTopkSmemKeys = 16384;  // scores cached in shared memory up to this many blocks
+constexpr int kTopkMaxChunks = 64;
+constexpr size_t kTopkMergeSmemMax = 160 * 1024;  // kept candidates (key + block) of one unit
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(Dims d, const float* __restrict__ scores,
                                                             const int* __restrict__ ctx_len, int* __restrict__ sel,
@@ -114,10 +123,202 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(Dims d, const float*
   }
 }
 
+// Histogram of one 8-bit digit over the keys in shared memory that match `prefix` under
+// `mask`.  Lanes of a warp that hit the same bin add once (scores of one unit share their high
+// key bytes, so per-lane atomics would serialise on a few bins).
+__device__ __forceinline__ void digit_histogram(const uint32_t* keys, int n, uint32_t prefix, uint32_t mask,
+                                                int shift, int* hist) {
+  const int lane = threadIdx.x & 31;
+  const int n_round = (n + blockDim.x - 1) / blockDim.x * blockDim.x;
+  for (int i = threadIdx.x; i < n_round; i += blockDim.x) {
+    uint32_t bin = 256u + lane;                         // unique per lane: never grouped
+    if (i < n) {
+      const uint32_t key = keys[i];
+      if ((key & mask) == prefix) bin = (key >> shift) & 255u;
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, bin);
+    if (bin < 256u && lane == __ffs(same) - 1) atomicAdd(&hist[bin], __popc(same));
+  }
+}
+
+// Top k of keys[0, n) in shared memory by (key desc, position asc); emit(rank, i) is called for
+// each selected position i, ranks 0..k-1 in ascending position order.  Every thread of the CTA
+// must call it.  Requires 0 < k < n.
+template <class Emit>
+__device__ void select_ordered(const uint32_t* keys, int n, int k, int* hist, int* ws, int* pick, Emit emit) {
+  const int tid = threadIdx.x, NT = blockDim.x;
+  uint32_t prefix = 0, mask = 0;
+  int remaining = k;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 256; i += NT) hist[i] = 0;
+    __syncthreads();
+    digit_histogram(keys, n, prefix, mask, shift, hist);
+    __syncthreads();
+    if (tid < 32) radix_pick_digit(hist, remaining, true, pick);
+    __syncthreads();
+    prefix |= (uint32_t)pick[0] << shift;
+    mask |= 255u << shift;
+    remaining -= pick[1];
+    __syncthreads();
+  }
+  const uint32_t T = prefix;
+  const int need_eq = remaining;
+  const int per = (n + NT - 1) / NT;
+  const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+  int my_eq = 0, my_gt = 0;
+  for (int i = i0; i < i1; ++i) {
+    my_eq += keys[i] == T;
+    my_gt += keys[i] > T;
+  }
+  int tot;
+  int er = block_excl_sum(my_eq, ws, &tot);
+  const int my_take = my_gt + max(0, min(my_eq, need_eq - er));
+  int pos = block_excl_sum(my_take, ws, &tot);
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = keys[i];
+    if (key > T || (key == T && er++ < need_eq)) emit(pos++, i);
+  }
+}
+
+constexpr int kChunk = kTopkSmemKeys;   // blocks per phase-1 CTA
+
+// Phase 1: CTA (c, u) keeps the top-k candidates of blocks [c*kChunk, (c+1)*kChunk) of unit u
+// (candidates: not sink, not recent), in block order, with their keys.
+__global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(Dims d, const float* __restrict__ scores,
+                                                                  const int* __restrict__ ctx_len, int P,
+                                                                  uint32_t* __restrict__ ckey, int* __restrict__ cidx,
+                                                                  int* __restrict__ ccnt) {
+  extern __shared__ uint32_t skeys[];
+  __shared__ int hist[256];
+  __shared__ int ws[33];
+  __shared__ int pick[2];
+  const int c = blockIdx.x, u = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int len = ctx_len[u / d.Hkv];
+  const int nb = (len < 0 || len > d.max_ctx) ? 0 : n_blocks_of(len, d.bs);
+  const int k = d.Kb - d.n_sink - d.n_recent;
+  const size_t slot = (size_t)u * P + c;
+  const int b0 = max(c * kChunk, d.n_sink), b1 = min((c + 1) * kChunk, nb - d.n_recent);
+  const int n = (nb <= d.Kb || k <= 0) ? 0 : max(0, b1 - b0);
+  const float* s = scores + (size_t)u * d.nb_max + b0;
+  uint32_t* okey = ckey + slot * d.Kb;
+  int* oidx = cidx + slot * d.Kb;
+  if (n <= k) {                                         // every candidate of the chunk is kept
+    for (int i = tid; i < n; i += blockDim.x) {
+      okey[i] = score_key(s[i]);
+      oidx[i] = b0 + i;
+    }
+    if (tid == 0) ccnt[slot] = n;
+    return;
+  }
+  for (int i = tid; i < n; i += blockDim.x) skeys[i] = score_key(s[i]);
+  __syncthreads();
+  select_ordered(skeys, n, k, hist, ws, pick, [&](int r, int i) {
+    okey[r] = skeys[i];
+    oidx[r] = b0 + i;
+  });
+  if (tid == 0) ccnt[slot] = k;
+}
+
+// Phase 2: one CTA per unit selects the top-k among its chunks' kept candidates and frames them
+// with the sink and recent blocks, in ascending block order.
+__global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(Dims d, const int* __restrict__ ctx_len, int P,
+                                                                  const uint32_t* __restrict__ ckey,
+                                                                  const int* __restrict__ cidx,
+                                                                  const int* __restrict__ ccnt, int* __restrict__ sel,
+                                                                  int* __restrict__ nsel, unsigned* err) {
+  extern __shared__ uint32_t smem[];
+  __shared__ int hist[256];
+  __shared__ int ws[33];
+  __shared__ int pick[2];
+  __shared__ int off[kTopkMaxChunks + 1];
+  const int u = blockIdx.x;
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int len = ctx_len[u / d.Hkv];
+  if (len < 0 || len > d.max_ctx) {
+    if (tid == 0) set_error(err, KVS_ERR_BAD_INDEX);
+    return;
+  }
+  const int nb = n_blocks_of(len, d.bs);
+  int* out = sel + (size_t)u * d.Kb;
+  if (nb <= d.Kb) {
+    for (int i = tid; i < nb; i += NT) out[i] = i;
+    if (tid == 0) nsel[u] = nb;
+    return;
+  }
+  const int k = d.Kb - d.n_sink - d.n_recent;
+  for (int i = tid; i < d.n_sink; i += NT) out[i] = i;
+  for (int i = tid; i < d.n_recent; i += NT) out[d.n_sink + k + i] = nb - d.n_recent + i;
+  if (tid == 0) {
+    int o = 0;
+    for (int c = 0; c < P; ++c) {
+      off[c] = o;
+      o += ccnt[(size_t)u * P + c];
+    }
+    off[P] = o;
+  }
+  __syncthreads();
+  const int n = off[P];
+  uint32_t* keys = smem;
+  int* idx = reinterpret_cast<int*>(smem + (size_t)P * d.Kb);
+  for (int c = 0; c < P; ++c) {
+    const size_t slot = (size_t)u * P + c;
+    const int m = off[c + 1] - off[c];
+    for (int i = tid; i < m; i += NT) {
+      keys[off[c] + i] = ckey[slot * d.Kb + i];
+      idx[off[c] + i] = cidx[slot * d.Kb + i];
+    }
+  }
+  __syncthreads();
+  if (k > 0) {
+    // nb > Kb leaves more than k candidates, so at least k were kept; exactly k when a single
+    // chunk held more than k of them (all kept ones are then the answer)
+    if (n < k) {
+      if (tid == 0) set_error(err, KVS_ERR_BAD_INDEX);
+      return;
+    }
+    if (n == k) {
+      for (int i = tid; i < n; i += NT) out[d.n_sink + i] = idx[i];
+    } else {
+      select_ordered(keys, n, k, hist, ws, pick, [&](int r, int i) { out[d.n_sink + r] = idx[i]; });
+    }
+  }
+  if (tid == 0) nsel[u] = d.Kb;
+}
+
 }  // namespace
 
+int topk_chunks(const Dims& d) {
+  if (d.nb_max <= kTopkSmemKeys) return 0;
+  const int P = (d.nb_max + kChunk - 1) / kChunk;
+  const size_t merge_smem = (size_t)P * d.Kb * 8;
+  if (P > kTopkMaxChunks || merge_smem > kTopkMergeSmemMax) return 0;   // single pass
+  return P;
+}
+
 cudaError_t launch_topk(const Dims& d, const float* scores, const int* ctx_len, int* sel, int* nsel, unsigned* err,
-                        cudaStream_t s) {
+                        cudaStream_t s, const TopkScratch* scratch) {
+  const int P = scratch ? topk_chunks(d) : 0;
+  if (P > 0) {
+    static bool attr2 = false;
+    if (!attr2) {
+      cudaError_t e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)(kChunk * sizeof(uint32_t)));
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kTopkMergeSmemMax);
+      if (e != cudaSuccess) return e;
+      attr2 = true;
+    }
+    topk_chunk_kernel<<<dim3(P, d.U), kTopkThreads, kChunk * sizeof(uint32_t), s>>>(d, scores, ctx_len, P, scratch->key,
+                                                                                  scratch->idx, scratch->cnt);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    topk_merge_kernel<<<d.U, kTopkThreads, (size_t)P * d.Kb * 8, s>>>(d, ctx_len, P, scratch->key, scratch->idx,
+                                                                     scratch->cnt, sel, nsel, err);
+    return cudaGetLastError();
+  }
   size_t smem = (size_t)kTopkSmemKeys * sizeof(uint32_t);
   static bool attr_set = false;
   if (!attr_set) {

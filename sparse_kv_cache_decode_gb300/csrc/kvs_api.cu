@@ -31,6 +31,7 @@ struct kvs_ctx {
   std::vector<cudaEvent_t> sel_ready, pf_done;
   std::vector<int> sel_pending, pf_pending;
   std::vector<CUtensorMap> tmaps;   // per layer: K pool, V pool (TMA attention path)
+  kvs::TopkScratch tk{};            // two-phase top-K candidates (long contexts), shared by layers
   cudaEvent_t fork;
   // diagnostics
   unsigned long long launches = 0;
@@ -94,7 +95,7 @@ bool fill_dims(const kvs_config* c, Dims* d) {
 struct Plan {
   size_t kpool, vpool, b2s, s2b, stamp, clock, pend_sel, pend_slot, pend_n, sel, nsel, sos, fblk, fslot, nfetch;
   size_t per_layer;
-  size_t err, scores, part, ml, done;
+  size_t err, scores, part, ml, done, tk_key, tk_idx, tk_cnt;
   size_t total;
 };
 
@@ -125,7 +126,11 @@ Plan plan_of(const Dims& d) {
   p.part = align_up(U * parts * d.G * d.dv * 4);
   p.ml = align_up(U * parts * d.G * 2 * 4);
   p.done = align_up(U * 4);
-  p.total = p.per_layer * d.NL + p.err + p.scores + p.part + p.ml + p.done;
+  const size_t P = (size_t)topk_chunks(d);
+  p.tk_key = align_up(U * P * d.Kb * 4);
+  p.tk_idx = align_up(U * P * d.Kb * 4);
+  p.tk_cnt = align_up(U * P * 4);
+  p.total = p.per_layer * d.NL + p.err + p.scores + p.part + p.ml + p.done + p.tk_key + p.tk_idx + p.tk_cnt;
   return p;
 }
 
@@ -249,6 +254,10 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   float* part = reinterpret_cast<float*>(shared + p.err + p.scores);
   float* ml = reinterpret_cast<float*>(shared + p.err + p.scores + p.part);
   unsigned* done = reinterpret_cast<unsigned*>(shared + p.err + p.scores + p.part + p.ml);
+  unsigned char* tk = shared + p.err + p.scores + p.part + p.ml + p.done;
+  c->tk.key = p.tk_key ? reinterpret_cast<uint32_t*>(tk) : nullptr;
+  c->tk.idx = p.tk_key ? reinterpret_cast<int*>(tk + p.tk_key) : nullptr;
+  c->tk.cnt = p.tk_key ? reinterpret_cast<int*>(tk + p.tk_key + p.tk_idx) : nullptr;
   for (int l = 0; l < d.NL; ++l) {
     unsigned char* b = base + p.per_layer * l;
     Layer& L = c->layers[l];
@@ -440,7 +449,7 @@ kvs_status kvs_score_blocks(kvs_ctx* c, int layer, const void* d_score_q, int nq
 kvs_status kvs_topk_select(kvs_ctx* c, const float* d_scores, const int* d_ctx_len, int* d_sel, int* d_nsel,
                            kvs_stream_t stream) {
   if (!c || !d_scores || !d_ctx_len || !d_sel || !d_nsel) return KVS_ERR_INVALID_ARG;
-  return cuda_status(timed(c, KVS_K_TOPK, S(stream), 1, [&] { return launch_topk(c->d, d_scores, d_ctx_len, d_sel, d_nsel, c->err, S(stream)); }));
+  return cuda_status(timed(c, KVS_K_TOPK, S(stream), 1, [&] { return launch_topk(c->d, d_scores, d_ctx_len, d_sel, d_nsel, c->err, S(stream), c->tk.key ? &c->tk : nullptr); }));
 }
 
 kvs_status kvs_cache_update(kvs_ctx* c, int layer, const int* d_sel, const int* d_nsel, const int* d_ctx_len,
@@ -531,7 +540,7 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
     return timed(c, KVS_K_SCORE, s, 1, [&] { return launch_score(d, idx, rows, n, d_ctx_len, L.scores, c->err, s); });
   };
   auto topk = [&](int* so, int* no) {
-    cudaError_t r = timed(c, KVS_K_TOPK, s, 1, [&] { return launch_topk(d, L.scores, d_ctx_len, so, no, c->err, s); });
+    cudaError_t r = timed(c, KVS_K_TOPK, s, 1, [&] { return launch_topk(d, L.scores, d_ctx_len, so, no, c->err, s, c->tk.key ? &c->tk : nullptr); });
     if (r == cudaSuccess) r = cudaEventRecord(c->sel_ready[layer], s);   // hint for a prefetch into layer + 1
     if (r == cudaSuccess) c->sel_pending[layer] = 1;
     return r;

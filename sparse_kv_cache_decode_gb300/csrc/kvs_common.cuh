@@ -77,8 +77,15 @@ cudaError_t launch_advance(int B, int* ctx_len, cudaStream_t s);
 cudaError_t launch_touch_pages(const void* base, size_t bytes, unsigned* sink, cudaStream_t s);
 cudaError_t launch_score(const Dims& d, const __nv_bfloat16* index, const __nv_bfloat16* q, int nq,
                          const int* ctx_len, float* scores, unsigned* err, cudaStream_t s);
+// Scratch of the two-phase top-K (long contexts): per (unit, chunk) up to K_b kept candidates.
+struct TopkScratch {
+  uint32_t* key;  // [U][P][Kb]
+  int* idx;       // [U][P][Kb]
+  int* cnt;       // [U][P]
+};
+int topk_chunks(const Dims& d);   // P, or 0 when one pass per unit is used
 cudaError_t launch_topk(const Dims& d, const float* scores, const int* ctx_len, int* sel, int* nsel,
-                        unsigned* err, cudaStream_t s);
+                        unsigned* err, cudaStream_t s, const TopkScratch* scratch);
 cudaError_t launch_cache_update(const Dims& d, const Layer& L, const int* sel, const int* nsel, const int* ctx_len,
                                 int* slot_of_sel, kvs_stats* stats, cudaStream_t s);
 cudaError_t launch_prefetch(const Dims& d, const Layer& L, const int* hint, const int* hint_n, const int* ctx_len,

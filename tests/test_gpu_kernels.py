@@ -93,15 +93,18 @@ def _special_scores(seed, n):
     return s
 
 
-@pytest.mark.parametrize("lens,budget,sink,recent", [
-    ([4096, 1000, 17], 16, 1, 2),        # ragged, one context below the budget
-    ([4096, 4096], 2, 1, 1),              # budget == forced set
-    ([300000, 123457], 128, 1, 2),        # > 16384 blocks: scores read from global memory
-    ([65536, 65536], 256, 0, 0),          # pure top-k
+@pytest.mark.parametrize("lens,budget,sink,recent,bs", [
+    ([4096, 1000, 17], 16, 1, 2, 16),        # ragged, one context below the budget
+    ([4096, 4096], 2, 1, 1, 16),              # budget == forced set
+    ([300000, 123457], 128, 1, 2, 16),        # > 16384 blocks: two phases over 2 chunks
+    ([65536, 65536], 256, 0, 0, 16),          # pure top-k
+    ([131072, 70001, 1500], 2048, 0, 0, 1),   # token blocks: 8 chunks, ragged, one below the budget
+    ([200000, 16385], 512, 4, 8, 1),          # 13 chunks framed by sink and recent blocks
+    ([131072], 4096, 1, 1, 1),                # candidates too many to merge: one pass from global memory
 ])
-def test_topk_select_bit_exact(lens, budget, sink, recent):
+def test_topk_select_bit_exact(lens, budget, sink, recent, bs):
     w = W.TINY.with_(name="topk", n_req=len(lens), ctx0=max(lens), budget_blocks=budget, n_sink=sink,
-                     n_recent=recent, cap_blocks=budget, n_heavy=0, n_layer=1)
+                     n_recent=recent, cap_blocks=budget, n_heavy=0, n_layer=1, block_size=bs)
     g = GpuCase(w, lens)
     nbm = g.nb_max
     host = np.stack([np.stack([_special_scores(17 + r * 7 + h, nbm) for h in range(w.n_kv_head)])
