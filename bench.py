@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--threads", type=int, default=0, help="generator threads (0: all cores)")
     ap.add_argument("--serial", action="store_true", help="fetch on the compute stream (kernels run one at a time)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling cases)")
+    ap.add_argument("--batch", type=int, default=0, help="override the request count (smaller profiling cases)")
     return ap.parse_args()
 
 
@@ -293,6 +294,8 @@ def run_ours(args, dist):
     w = W.get(args.workload)
     if args.layers:
         w = w.with_(n_layer=args.layers)
+    if args.batch:
+        w = w.with_(n_req=args.batch)
     if dist.world > 1:
         w = w.with_(seed=w.seed + dist.rank)       # each GPU serves its own batch of requests
     B, NL, Hkv = w.n_req, w.n_layer, w.n_kv_head
