@@ -291,6 +291,28 @@ class HostArray:
         self._registered = True
         return self
 
+    MADV_COLLAPSE = 25   # Linux >= 6.1: map the range with huge pages again, synchronously
+
+    def recollapse(self) -> float:
+        """Map the array with huge pages again after some of its huge-page mappings were split
+        (the pages stay in place and keep their contents): unregister, advise MADV_COLLAPSE,
+        register again.  Returns the huge fraction afterwards; callers bind the history anew."""
+        import mmap
+        import torch
+        was = self._registered
+        if was:
+            torch.cuda.cudart().cudaHostUnregister(self.tensor.data_ptr())
+            self._registered = False
+        base = ctypes.addressof(ctypes.c_char.from_buffer(self._mm))
+        off = self.tensor.data_ptr() - base
+        try:
+            self._mm.madvise(self.MADV_COLLAPSE, off, (self.nbytes + mmap.PAGESIZE - 1) // mmap.PAGESIZE * mmap.PAGESIZE)
+        except OSError:
+            pass
+        if was:
+            self.register()
+        return self.huge_fraction()
+
     def close(self):
         import torch
         if self._registered:

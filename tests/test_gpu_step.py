@@ -60,3 +60,27 @@ def test_decode_step_gaussian_inputs(w):
     n_units = w.n_layer * w.n_req * w.n_kv_head
     assert len(frozen) <= max(1, n_units // 2)
     assert g.ctx.poll_error() == 0
+
+
+def test_rebind_after_recollapse_keeps_parity():
+    """The host history can be re-registered and bound again between steps (what a caller does
+    after remapping split huge pages): the cache state stays valid and steps stay bit-exact."""
+    import sparse_kv_cache_decode_gb300 as K
+    # 1 GiB of history, so it lives in a huge-page HostArray; 32768 blocks per unit: two-phase top-K
+    w = W.TINY.with_(name="tiny_rebind", n_req=2, ctx0=524288, steps=6, int_scale=2.0)
+    g = GpuCase(w, [524288, 400001])
+    assert g._arrays, "expected a huge-page host array"
+    o = g.oracle()
+    cum = {l: {k: 0 for k in STAT_KEYS} for l in range(w.n_layer)}
+    for t in range(w.steps):
+        if t == 3:
+            for a in g._arrays:
+                assert isinstance(a, K.HostArray)
+                a.recollapse()
+            g.ctx.bind_host_kv(g.k_host, g.v_host)
+        q, d, nk, nv = g.step_inputs(t)
+        g.gpu_step(q, d, nk, nv)
+        out_ref, recs = o.step(q, d, nk, nv)
+        _compare_step(g, o, out_ref, recs, cum, exact=True)
+    assert g.ctx.poll_error() == 0
+    g.close()
