@@ -377,9 +377,24 @@ cudaError_t launch_attn_t(const Dims& d, const Layer& L, const __nv_bfloat16* q,
 
 int attention_split(const Dims& d, int* n_split_out, int* bps_out) {
   const int nz = d.dv / kDVC;
-  // enough CTAs for ~2 per SM; at least 2 blocks per split, at most 512 staged block ids
-  int n_split = (2 * 152 + d.U * nz - 1) / (d.U * nz);
-  n_split = max(1, min(n_split, min(kAttnSplitMax, (d.Kb + 1) / 2)));
+  // CTAs of the launched configuration that fit on one SM (shared memory bound)
+  int smem = AttnCfg<128, 1, false>::SMEM;
+  if (d.v_shares_k) smem = d.G <= 16 ? AttnCfg<576, 1, true>::SMEM : AttnCfg<576, 8, true>::SMEM;
+  const int per_sm = max(1, min(2, (227 * 1024) / (smem + 1024)));
+  const int slots = 152 * per_sm;
+  // split count with the least time: waves (rounded up) x (selection share of a CTA + a fixed
+  // per-CTA cost, ~3% of a whole selection); at least 2 blocks per split
+  const int cap = max(1, min(kAttnSplitMax, (d.Kb + 1) / 2));
+  int n_split = 1;
+  double best = 1e30;
+  for (int n = 1; n <= cap; ++n) {
+    const long long ctas = (long long)d.U * nz * n;
+    const double cost = (double)((ctas + slots - 1) / slots) * (1.0 / n + 0.03);
+    if (cost < best) {
+      best = cost;
+      n_split = n;
+    }
+  }
   int bps = (d.Kb + n_split - 1) / n_split;
   const int max_blocks_cta = 4 * 1024 / 8;
   if (bps > max_blocks_cta) {
