@@ -33,7 +33,7 @@
  *   sel         [B][H_kv][K_b] int32              selected block ids, ascending; nsel [B][H_kv]
  *   slot_of_sel [B][H_kv][K_b] int32              cache slot of each selected block
  *   out         [B][H_q][d_v] fp32                one layer's attention output
- *   k_new/v_new [B][H_kv][d_k] / [d_v] bf16       one layer's appended token
+ *   k_new/v_new [B][H_kv][d_k] / [d_v] bf16       one layer's appended token (16-byte aligned)
  *   ctx_len     [B] int32 (device)
  *
  * Ownership.  The caller owns every buffer.  The device workspace (kvs_workspace_bytes) holds

@@ -69,8 +69,10 @@ cudaError_t launch_index_build(const Dims& d, const Layer& L, __nv_bfloat16* ind
 }
 
 // One CTA per unit.  Writes the token at position len-1 to the host history and, when its block
-// is resident, to the block's slot; then recomputes the block's index key from its present
-// tokens, taking the new token's values from k_new (not read back from host memory).
+// is resident, to the block's slot (16-byte vectors); then recomputes the block's index key from
+// its present tokens, in token order, taking the new token's values from k_new and the earlier
+// rows from the block's slot when it is resident (the same bf16 values as the host rows, read
+// from HBM instead of over the host link), else from the host history.
 __global__ void __launch_bounds__(128) append_kernel(Dims d, Layer L, const __nv_bfloat16* __restrict__ k_new,
                                                      const __nv_bfloat16* __restrict__ v_new,
                                                      __nv_bfloat16* __restrict__ index,
@@ -85,27 +87,45 @@ __global__ void __launch_bounds__(128) append_kernel(Dims d, Layer L, const __nv
   const int p = len - 1;
   const int b = p / d.bs, row_in_blk = p - b * d.bs;
   const int slot = L.block2slot[(size_t)u * d.nb_max + b];
-  __nv_bfloat16* hk = const_cast<__nv_bfloat16*>(L.host_k) + ((size_t)u * d.max_ctx + p) * d.dk;
-  const __nv_bfloat16* kn = k_new + (size_t)u * d.dk;
-  for (int i = threadIdx.x; i < d.dk; i += blockDim.x) {
-    hk[i] = kn[i];
-    if (slot >= 0) L.kpool[(((size_t)u * d.C + slot) * d.bs + row_in_blk) * d.dk + i] = kn[i];
-  }
-  if (!d.v_shares_k) {
-    __nv_bfloat16* hv = const_cast<__nv_bfloat16*>(L.host_v) + ((size_t)u * d.max_ctx + p) * d.dv;
-    const __nv_bfloat16* vn = v_new + (size_t)u * d.dv;
-    for (int i = threadIdx.x; i < d.dv; i += blockDim.x) {
-      hv[i] = vn[i];
-      if (slot >= 0) L.vpool[(((size_t)u * d.C + slot) * d.bs + row_in_blk) * d.dv + i] = vn[i];
+  {
+    uint4* hk = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(L.host_k) + ((size_t)u * d.max_ctx + p) * d.dk);
+    const uint4* kn = reinterpret_cast<const uint4*>(k_new + (size_t)u * d.dk);
+    uint4* sk = slot >= 0 ? reinterpret_cast<uint4*>(L.kpool + (((size_t)u * d.C + slot) * d.bs + row_in_blk) * d.dk)
+                          : nullptr;
+    for (int i = threadIdx.x; i < d.dk / 8; i += blockDim.x) {
+      const uint4 x = kn[i];
+      hk[i] = x;
+      if (sk) sk[i] = x;
     }
   }
-  // index key of block b over tokens [b*bs, len)
-  const __nv_bfloat16* rows = L.host_k + (size_t)u * d.max_ctx * d.dk;
-  const float n = (float)(len - b * d.bs);
+  if (!d.v_shares_k) {
+    uint4* hv = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(L.host_v) + ((size_t)u * d.max_ctx + p) * d.dv);
+    const uint4* vn = reinterpret_cast<const uint4*>(v_new + (size_t)u * d.dv);
+    uint4* sv = slot >= 0 ? reinterpret_cast<uint4*>(L.vpool + (((size_t)u * d.C + slot) * d.bs + row_in_blk) * d.dv)
+                          : nullptr;
+    for (int i = threadIdx.x; i < d.dv / 8; i += blockDim.x) {
+      const uint4 x = vn[i];
+      hv[i] = x;
+      if (sv) sv[i] = x;
+    }
+  }
+  // index key of block b over tokens [b*bs, len): earlier rows in token order, then the new one
+  const __nv_bfloat16* rows = slot >= 0 ? L.kpool + ((size_t)u * d.C + slot) * d.bs * d.dk
+                                        : L.host_k + ((size_t)u * d.max_ctx + (size_t)b * d.bs) * d.dk;
+  const int nt = row_in_blk;                                // earlier rows of the block
+  const float n = (float)(nt + 1);
   for (int i = threadIdx.x; i < d.dk; i += blockDim.x) {
     float acc = 0.f;
-    for (int t = b * d.bs; t < p; ++t) acc = __fadd_rn(acc, __bfloat162float(rows[(size_t)t * d.dk + i]));
-    acc = __fadd_rn(acc, __bfloat162float(kn[i]));
+    int t = 0;
+    for (; t + 8 <= nt; t += 8) {
+      float x[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = __bfloat162float(rows[(size_t)(t + j) * d.dk + i]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc = __fadd_rn(acc, x[j]);
+    }
+    for (; t < nt; ++t) acc = __fadd_rn(acc, __bfloat162float(rows[(size_t)t * d.dk + i]));
+    acc = __fadd_rn(acc, __bfloat162float(k_new[(size_t)u * d.dk + i]));
     index[((size_t)u * d.nb_max + b) * d.dk + i] = __float2bfloat16_rn(__fdiv_rn(acc, n));
   }
 }

@@ -46,6 +46,9 @@ namespace {
 
 constexpr size_t kAlign = 256;
 
+// the appended token's rows are read and written as 16-byte vectors
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool fill_dims(const kvs_config* c, Dims* d) {
@@ -505,6 +508,7 @@ kvs_status kvs_append(kvs_ctx* c, int layer, const void* d_k_new, const void* d_
                       const int* d_ctx_len, kvs_stream_t stream) {
   if (!layer_ok(c, layer) || !d_k_new || !d_index || !d_ctx_len) return KVS_ERR_INVALID_ARG;
   if (!c->d.v_shares_k && !d_v_new) return KVS_ERR_INVALID_ARG;
+  if (!aligned16(d_k_new) || !aligned16(d_v_new)) return KVS_ERR_INVALID_ARG;
   if (!c->host_k_dev) return KVS_ERR_HOST_MEM;
   const Dims& d = c->d;
   __nv_bfloat16* idx = static_cast<__nv_bfloat16*>(d_index) + (size_t)layer * d.U * d.nb_max * d.dk;
@@ -525,6 +529,7 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
   if (d_score_q == nullptr) nq = 1;
   if (nq < 1 || nq > d.max_nq) return KVS_ERR_INVALID_ARG;
   if (d_k_new && !d.v_shares_k && !d_v_new) return KVS_ERR_INVALID_ARG;
+  if (!aligned16(d_k_new) || !aligned16(d_v_new)) return KVS_ERR_INVALID_ARG;
   cudaStream_t s = S(stream);
   cudaStream_t cs = copy_stream ? S(copy_stream) : s;
   Layer& L = c->layers[layer];

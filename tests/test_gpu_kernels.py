@@ -286,3 +286,21 @@ def test_sparse_decode_attention(w, lens):
         worst = max(worst, err)
         assert err <= 2e-3, f"unit {u}: max abs err {err}"
     assert g.ctx.poll_error() == 0
+
+
+def test_append_rejects_misaligned_token_rows():
+    """The appended rows are moved as 16-byte vectors: a misaligned k_new / v_new is refused on the
+    host (KVS_ERR_INVALID_ARG) before anything is launched."""
+    import sparse_kv_cache_decode_gb300 as K
+    w = W.TINY_APPEND
+    g = GpuCase(w, [w.ctx0])
+    n = w.n_req * w.n_kv_head * w.d_k
+    buf = torch.zeros(2 * n + 16, dtype=torch.int16, device="cuda")
+    good_k, good_v = buf[:n], buf[n + 8:2 * n + 8]
+    bad_k = buf[1:n + 1]                                   # 2 bytes past a 16-byte boundary
+    for kk, vv in ((bad_k, good_v), (good_k, buf[n + 9:2 * n + 9])):
+        with pytest.raises(K.KvsError) as e:
+            g.ctx.append(0, kk, vv, g.index, g.ctx_len)
+        assert K.STATUS[e.value.status] == "KVS_ERR_INVALID_ARG"
+    torch.cuda.synchronize()
+    assert g.ctx.poll_error() == 0

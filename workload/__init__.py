@@ -212,7 +212,10 @@ TINY_MLA = Workload(name="tiny_mla", n_req=1, n_layer=1, n_q_head=16, n_kv_head=
                     v_shares_k=True, block_size=1, ctx0=4096, steps=32, budget_blocks=256, n_sink=0, n_recent=0,
                     cap_blocks=384, rho=0.9, n_heavy=32, heavy_scale=4.0)
 
-WORKLOADS = {w.name: w for w in (TINY, TINY_LOOKAHEAD, TINY_APPEND, TINY_PREFETCH, TINY_MLA, LLAMA8B_32K, LONG_128K,
+# the 128K shape without the per-step append (history fixed): isolates the append's effect
+LONG_128K_SYNC = LONG_128K.with_(name="llama8b_128k_sync", append=False)
+
+WORKLOADS = {w.name: w for w in (TINY, TINY_LOOKAHEAD, TINY_APPEND, TINY_PREFETCH, TINY_MLA, LLAMA8B_32K, LONG_128K, LONG_128K_SYNC,
                                  MLA_128K)}
 
 
