@@ -322,6 +322,224 @@ __global__ void __launch_bounds__(AttnCfg<DK, MT, VSHARE>::NW * 32)
   }
 }
 
+// MLA decode attention (d_k = 576 latent + rope dims, V = the first 512 dims of each K row,
+// heads in groups of 32).  Grid (split, unit, head group).  The 8 warps are 2 head tiles x 4
+// quarters: warp (ht, qq) computes the q.k product over dims [144 qq, 144 qq + 144) for its 16
+// heads, the four partial 16 x 16 score tiles of a head tile are summed through shared memory
+// in a fixed order (named barrier of the tile's 4 warps), then every warp runs the online
+// softmax of its head tile and accumulates P.V for value columns [128 qq, 128 qq + 128).  So
+// the q.k product is computed once per (head, token), and 32 heads of queries (36 KiB) leave
+// room for two CTAs per SM.
+namespace mla {
+constexpr int DK = 576, DV = 512, HEADS = 32, NW = 8, QDIMS = DK / 4;
+constexpr int KRS = DK * 2 + 16;                 // row stride of query and token rows (bytes)
+constexpr int TILE = 16 * KRS;                   // 16 token rows
+constexpr int Q_BYTES = HEADS * KRS;
+constexpr int RED_BYTES = 2 * 4 * 256 * 4;       // [head tile][quarter][256 fragment floats]
+constexpr int LIST_ENTRIES = 512;                // staged (block, slot) pairs per CTA
+constexpr int SMEM = Q_BYTES + 2 * TILE + RED_BYTES + LIST_ENTRIES * 8;
+}  // namespace mla
+
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
+
+__global__ void __launch_bounds__(mla::NW * 32, 2)
+    attn_mla_kernel(Dims d, Layer L, const __nv_bfloat16* __restrict__ q, const int* __restrict__ sel,
+                    const int* __restrict__ slot_of_sel, const int* __restrict__ nsel,
+                    const int* __restrict__ ctx_len, float* __restrict__ out, int n_split, int blocks_per_split) {
+  using namespace mla;
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char* qs = smem;
+  unsigned char* bufs = smem + Q_BYTES;
+  float* red = reinterpret_cast<float*>(bufs + 2 * TILE);
+  int* s_slot = reinterpret_cast<int*>(bufs + 2 * TILE + RED_BYTES);
+  int* s_blk = s_slot + LIST_ENTRIES;
+
+  const int split = blockIdx.x, u = blockIdx.y, hg = blockIdx.z;
+  const int r = u / d.Hkv, h = u % d.Hkv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ht = warp >> 2, qq = warp & 3;
+  const int len = ctx_len[r];
+  const int n = nsel[u];
+  const int i0 = min(n, split * blocks_per_split), i1 = min(n, i0 + blocks_per_split);
+  const int nblk = i1 - i0;
+  const int n_tiles = (nblk * d.bs + 15) / 16;
+  const int head0 = h * d.G + hg * HEADS;          // first q head of the CTA
+
+  for (int i = tid; i < HEADS * (DK / 8); i += NW * 32) {
+    const int row = i / (DK / 8), ch = i % (DK / 8);
+    *reinterpret_cast<uint4*>(qs + row * KRS + ch * 16) =
+        reinterpret_cast<const uint4*>(q + ((size_t)r * d.Hq + head0 + row) * DK)[ch];
+  }
+  for (int i = tid; i < nblk; i += NW * 32) {
+    s_slot[i] = slot_of_sel[(size_t)u * d.Kb + i0 + i];
+    s_blk[i] = sel[(size_t)u * d.Kb + i0 + i];
+  }
+  __syncthreads();
+
+  const __nv_bfloat16* kbase = L.kpool + (size_t)u * d.C * d.bs * DK;
+  auto tok_ptr = [&](int k, bool& valid, size_t& row_index) {
+    const int bi = k / d.bs, rr = k - bi * d.bs;
+    valid = false;
+    row_index = 0;
+    if (bi < nblk) {
+      const int pos = s_blk[bi] * d.bs + rr;
+      const int slot = s_slot[bi];
+      valid = pos < len && slot >= 0 && slot < d.C;
+      row_index = valid ? (size_t)slot * d.bs + rr : 0;
+    }
+  };
+  auto load_tile = [&](int t, unsigned char* dst) {
+    constexpr int KCH = DK * 2 / 16;
+    for (int i = tid; i < 16 * KCH; i += NW * 32) {
+      const int row = i / KCH, ch = i % KCH;
+      bool valid;
+      size_t ri;
+      tok_ptr(t * 16 + row, valid, ri);
+      const __nv_bfloat16* src = kbase + ri * DK + ch * 8;
+      cp_async16(dst + row * KRS + ch * 16, valid ? (const void*)src : (const void*)kbase, valid ? 16 : 0);
+    }
+    cp_async_commit();
+  };
+
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+  float oacc[kDVC / 8][4];
+#pragma unroll
+  for (int i = 0; i < kDVC / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+  const float sl2 = d.scale * kLog2e;
+  const int vcol0 = qq * kDVC;
+  float* my_red = red + (ht * 4 + qq) * 256 + lane * 8;
+
+  auto process_tile = [&](int t, const unsigned char* kt) {
+    float sacc[2][4];
+#pragma unroll
+    for (int nn = 0; nn < 2; ++nn) sacc[nn][0] = sacc[nn][1] = sacc[nn][2] = sacc[nn][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < QDIMS / 16; ++ks) {
+      uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+      const int kc = qq * QDIMS + ks * 16;
+      ldmatrix_x4(a0, a1, a2, a3, qs + (ht * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * KRS + (kc + (lane >> 4) * 8) * 2);
+      ldmatrix_x4(b0, b1, b2, b3, kt + ((lane & 7) + (lane >> 4) * 8) * KRS + (kc + ((lane >> 3) & 1) * 8) * 2);
+      mma_bf16_16816(sacc[0], a0, a1, a2, a3, b0, b1);
+      mma_bf16_16816(sacc[1], a0, a1, a2, a3, b2, b3);
+    }
+    // sum the head tile's four quarter products (fragment layouts are identical), fixed order
+#pragma unroll
+    for (int j = 0; j < 8; ++j) my_red[j] = sacc[j >> 2][j & 3];
+    named_barrier(1 + ht, 128);
+    const float* tile_red = red + ht * 4 * 256 + lane * 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      sacc[j >> 2][j & 3] = ((tile_red[j] + tile_red[256 + j]) + tile_red[512 + j]) + tile_red[768 + j];
+    float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+    for (int nn = 0; nn < 2; ++nn) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        bool valid;
+        size_t ri;
+        tok_ptr(t * 16 + nn * 8 + (lane & 3) * 2 + e, valid, ri);
+        const float s_lo = valid ? sacc[nn][e] * sl2 : -INFINITY;
+        const float s_hi = valid ? sacc[nn][2 + e] * sl2 : -INFINITY;
+        sacc[nn][e] = s_lo;
+        sacc[nn][2 + e] = s_hi;
+        mx_lo = fmaxf(mx_lo, s_lo);
+        mx_hi = fmaxf(mx_hi, s_hi);
+      }
+    }
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+    const float al_lo = mn_lo == -INFINITY ? 1.f : exp2f(m_lo - mn_lo);
+    const float al_hi = mn_hi == -INFINITY ? 1.f : exp2f(m_hi - mn_hi);
+    float ps_lo = 0.f, ps_hi = 0.f;
+#pragma unroll
+    for (int nn = 0; nn < 2; ++nn) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float p_lo = mn_lo == -INFINITY ? 0.f : exp2f(sacc[nn][e] - mn_lo);
+        const float p_hi = mn_hi == -INFINITY ? 0.f : exp2f(sacc[nn][2 + e] - mn_hi);
+        sacc[nn][e] = p_lo;
+        sacc[nn][2 + e] = p_hi;
+        ps_lo += p_lo;
+        ps_hi += p_hi;
+      }
+    }
+    ps_lo += __shfl_xor_sync(0xffffffffu, ps_lo, 1);
+    ps_lo += __shfl_xor_sync(0xffffffffu, ps_lo, 2);
+    ps_hi += __shfl_xor_sync(0xffffffffu, ps_hi, 1);
+    ps_hi += __shfl_xor_sync(0xffffffffu, ps_hi, 2);
+    l_lo = l_lo * al_lo + ps_lo;
+    l_hi = l_hi * al_hi + ps_hi;
+    m_lo = mn_lo;
+    m_hi = mn_hi;
+    uint32_t ph[4], pl[4];
+    auto split2 = [](float a, float b, uint32_t& hi, uint32_t& lo) {
+      hi = pack_bf16x2(a, b);
+      lo = pack_bf16x2(a - bf16_lo(hi), b - bf16_hi(hi));
+    };
+    split2(sacc[0][0], sacc[0][1], ph[0], pl[0]);
+    split2(sacc[0][2], sacc[0][3], ph[1], pl[1]);
+    split2(sacc[1][0], sacc[1][1], ph[2], pl[2]);
+    split2(sacc[1][2], sacc[1][3], ph[3], pl[3]);
+#pragma unroll
+    for (int nd = 0; nd < kDVC / 8; nd += 2) {
+      oacc[nd][0] *= al_lo; oacc[nd][1] *= al_lo; oacc[nd][2] *= al_hi; oacc[nd][3] *= al_hi;
+      oacc[nd + 1][0] *= al_lo; oacc[nd + 1][1] *= al_lo; oacc[nd + 1][2] *= al_hi; oacc[nd + 1][3] *= al_hi;
+      uint32_t b0, b1, b2, b3;
+      const int trow = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int col = vcol0 + nd * 8 + (lane >> 4) * 8;
+      ldmatrix_x4_trans(b0, b1, b2, b3, kt + trow * KRS + col * 2);
+      mma_bf16_16816(oacc[nd], ph[0], ph[1], ph[2], ph[3], b0, b1);
+      mma_bf16_16816(oacc[nd], pl[0], pl[1], pl[2], pl[3], b0, b1);
+      mma_bf16_16816(oacc[nd + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+      mma_bf16_16816(oacc[nd + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+    }
+  };
+
+  int stage = 0;
+  if (n_tiles > 0) load_tile(0, bufs);
+  for (int t = 0; t < n_tiles; ++t, stage ^= 1) {
+    if (t + 1 < n_tiles) {
+      load_tile(t + 1, bufs + (stage ^ 1) * TILE);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    process_tile(t, bufs + stage * TILE);
+    __syncthreads();        // the buffer and the score-reduction tiles are reused next
+  }
+
+  const int row_lo = ht * 16 + (lane >> 2), row_hi = row_lo + 8;     // within the CTA's 32 heads
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int row = hg * HEADS + (hh ? row_hi : row_lo);              // within the group of G
+    const float m = hh ? m_hi : m_lo, l = hh ? l_hi : l_lo;
+#pragma unroll
+    for (int nd = 0; nd < kDVC / 8; ++nd) {
+      const int c = vcol0 + nd * 8 + (lane & 3) * 2;
+      const float o0 = oacc[nd][hh * 2], o1 = oacc[nd][hh * 2 + 1];
+      if (n_split == 1) {
+        float* dst = out + ((size_t)r * d.Hq + h * d.G + row) * d.dv + c;
+        dst[0] = l > 0.f ? o0 / l : 0.f;
+        dst[1] = l > 0.f ? o1 / l : 0.f;
+      } else {
+        float* dst = L.attn_part + (((size_t)u * n_split + split) * d.G + row) * d.dv + c;
+        dst[0] = o0;
+        dst[1] = o1;
+      }
+    }
+    if (n_split > 1 && qq == 0 && (lane & 3) == 0) {
+      L.attn_ml[(((size_t)u * n_split + split) * d.G + row) * 2 + 0] = m;
+      L.attn_ml[(((size_t)u * n_split + split) * d.G + row) * 2 + 1] = l;
+    }
+  }
+}
+
 // out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s over the splits of a (unit, q head).
 __global__ void __launch_bounds__(128) attn_combine_kernel(Dims d, Layer L, float* __restrict__ out, int n_split) {
   const int u = blockIdx.x, g = blockIdx.y;
@@ -373,13 +591,36 @@ cudaError_t launch_attn_t(const Dims& d, const Layer& L, const __nv_bfloat16* q,
   return cudaGetLastError();
 }
 
+bool mla_path(const Dims& d) { return d.v_shares_k && d.dk == 576 && d.dv == 512 && d.G % mla::HEADS == 0; }
+
+cudaError_t launch_attn_mla(const Dims& d, const Layer& L, const __nv_bfloat16* q, const int* sel,
+                            const int* slot_of_sel, const int* nsel, const int* ctx_len, float* out, cudaStream_t s) {
+  static bool attr_set = false;
+  cudaError_t e;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int n_split, bps;
+  if (!attention_split(d, &n_split, &bps)) return cudaErrorInvalidValue;
+  dim3 grid(n_split, d.U, d.G / mla::HEADS);
+  attn_mla_kernel<<<grid, mla::NW * 32, mla::SMEM, s>>>(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, n_split, bps);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || n_split == 1) return e;
+  attn_combine_kernel<<<dim3(d.U, d.G), 128, 0, s>>>(d, L, out, n_split);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int attention_split(const Dims& d, int* n_split_out, int* bps_out) {
-  const int nz = d.dv / kDVC;
+  // grid z: value chunks, or head groups on the MLA path
+  const int nz = mla_path(d) ? d.G / mla::HEADS : d.dv / kDVC;
   // CTAs of the launched configuration that fit on one SM (shared memory bound)
   int smem = AttnCfg<128, 1, false>::SMEM;
   if (d.v_shares_k) smem = d.G <= 16 ? AttnCfg<576, 1, true>::SMEM : AttnCfg<576, 8, true>::SMEM;
+  if (mla_path(d)) smem = mla::SMEM;
   const int per_sm = max(1, min(2, (227 * 1024) / (smem + 1024)));
   const int slots = 152 * per_sm;
   // split count with the least time: waves (rounded up) x (selection share of a CTA + a fixed
@@ -421,6 +662,7 @@ cudaError_t launch_attention(const Dims& d, const Layer& L, const __nv_bfloat16*
     return launch_attention_tma(d, L, L.tmK, L.tmV, q, sel, slot_of_sel, nsel, ctx_len, out, s);
   if (d.v_shares_k) {
     if (d.G <= 16) return launch_attn_t<576, 1, true>(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, s);
+    if (mla_path(d)) return launch_attn_mla(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, s);
     return launch_attn_t<576, 8, true>(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, s);
   }
   return launch_attn_t<128, 1, false>(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, s);
