@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(mla::NW * 32, 2)
   for (int i = 0; i < kDVC / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
   const float sl2 = d.scale * kLog2e;
   const int vcol0 = qq * kDVC;
-  float* my_red = red + (ht * 4 + qq) * 256 + lane * 8;
+  float* my_red = red + (ht * 4 + qq) * 256 + lane;     // fragment value j of the lane at [j * 32]
 
   auto process_tile = [&](int t, const unsigned char* kt) {
     float sacc[2][4];
@@ -426,12 +426,13 @@ __global__ void __launch_bounds__(mla::NW * 32, 2)
     }
     // sum the head tile's four quarter products (fragment layouts are identical), fixed order
 #pragma unroll
-    for (int j = 0; j < 8; ++j) my_red[j] = sacc[j >> 2][j & 3];
+    for (int j = 0; j < 8; ++j) my_red[j * 32] = sacc[j >> 2][j & 3];
     named_barrier(1 + ht, 128);
-    const float* tile_red = red + ht * 4 * 256 + lane * 8;
+    const float* tile_red = red + ht * 4 * 256 + lane;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      sacc[j >> 2][j & 3] = ((tile_red[j] + tile_red[256 + j]) + tile_red[512 + j]) + tile_red[768 + j];
+      sacc[j >> 2][j & 3] =
+          ((tile_red[j * 32] + tile_red[256 + j * 32]) + tile_red[512 + j * 32]) + tile_red[768 + j * 32];
     float mx_lo = -INFINITY, mx_hi = -INFINITY;
 #pragma unroll
     for (int nn = 0; nn < 2; ++nn) {
