@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--serial", action="store_true", help="fetch on the compute stream (kernels run one at a time)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling cases)")
     ap.add_argument("--batch", type=int, default=0, help="override the request count (smaller profiling cases)")
+    ap.add_argument("--no-io", action="store_true",
+                    help="control run: every step replays the first step's inputs, so the selection repeats, every "
+                         "selected block is resident and the timed steps fetch nothing over the host link")
     return ap.parse_args()
 
 
@@ -298,6 +301,9 @@ def run_ours(args, dist):
         w = w.with_(n_layer=args.layers)
     if args.batch:
         w = w.with_(n_req=args.batch)
+    if args.no_io:
+        w = w.with_(name=w.name + "_no_io")
+        args.no_e2e = True          # the end-to-end pass streams fresh inputs, which would miss
     if dist.world > 1:
         w = w.with_(seed=w.seed + dist.rank)       # each GPU serves its own batch of requests
     B, NL, Hkv = w.n_req, w.n_layer, w.n_kv_head
@@ -425,6 +431,8 @@ def run_ours(args, dist):
                    None if tok_dev[0][1] is None else torch.empty_like(tok_dev[0][1]))
 
     def stage_inputs(t):
+        if args.no_io:
+            t = 0
         q_fix.copy_(q_dev[t], non_blocking=True)
         if d_fix is not None:
             d_fix.copy_(d_dev[t], non_blocking=True)

@@ -13,7 +13,7 @@
  * with round-to-nearest-even.
  *
  * Streams: 1 = K (or the MLA latent row), 2 = V, 3 = query innovations,
- *          4 = draft-query noise, 5 = heavy-position shuffle.
+ *          4 = draft-query noise, 5 = heavy-position shuffle, 6 = heavy-position carry-over.
  *
  * Build: gcc -O2 -ffp-contract=off -shared -fPIC -pthread (no fused multiply-add,
  * so results do not depend on the host ISA's contraction choices).
@@ -99,30 +99,62 @@ typedef struct {
   int32_t n_threads;
   float int_scale;                             /* > 0: integer-valued mode (see gen_store) */
   float int_clip;
+  double heavy_keep;                           /* per-layer sets: share of layer l-1's heavy positions
+                                                  layer l keeps (0: independent sets) */
 } kvs_gen_kv_params;
 
-/* Heavy positions of one set: the first n_heavy entries of a partial Fisher-Yates
- * shuffle of [0, ctx0) driven by stream 5. */
-static void gen_heavy_set(const kvs_gen_kv_params* p, int req, int layer, int head, int32_t* perm, uint8_t* mask) {
+/* Heavy positions of one set.  Each position of `prev` (the layer below's set, or NULL) is kept
+ * when its stream-6 draw falls below heavy_keep; the set is then filled up to n_heavy with the
+ * entries of a partial Fisher-Yates shuffle of [0, ctx0) driven by stream 5, in shuffle order,
+ * skipping positions already in the set.  With prev == NULL (or heavy_keep == 0) the set is the
+ * first n_heavy shuffle entries. */
+static void gen_heavy_set(const kvs_gen_kv_params* p, int req, int layer, int head, int32_t* perm, uint8_t* mask,
+                          const uint8_t* prev) {
   int64_t n = p->ctx0;
   if (n <= 0) return;
-  for (int64_t i = 0; i < n; ++i) perm[i] = (int32_t)i;
   int64_t k = p->n_heavy < n ? p->n_heavy : n;
-  for (int64_t i = 0; i < k; ++i) {
+  memset(mask, 0, (size_t)n);
+  int64_t cnt = 0;
+  if (prev && p->heavy_keep > 0.0) {
+    const double keep = p->heavy_keep >= 1.0 ? 1.0 : p->heavy_keep;
+    for (int64_t pos = 0; pos < n && cnt < k; ++pos) {
+      if (!prev[pos]) continue;
+      uint64_t x = gen_at(p->seed, gen_ctr(6, req, layer, head, pos, 0));
+      if ((double)(x >> 11) * (1.0 / 9007199254740992.0) < keep) {
+        mask[pos] = 1;
+        ++cnt;
+      }
+    }
+  }
+  for (int64_t i = 0; i < n; ++i) perm[i] = (int32_t)i;
+  for (int64_t i = 0; i < n && cnt < k; ++i) {
     uint64_t x = gen_at(p->seed, gen_ctr(5, req, layer, head, i, 0));
     uint64_t range = (uint64_t)(n - i);
     int64_t j = i + (int64_t)(((unsigned __int128)x * range) >> 64);
     int32_t t = perm[i]; perm[i] = perm[j]; perm[j] = t;
+    if (!mask[perm[i]]) {
+      mask[perm[i]] = 1;
+      ++cnt;
+    }
   }
-  memset(mask, 0, (size_t)n);
-  for (int64_t i = 0; i < k; ++i) mask[perm[i]] = 1;
 }
 
 int kvs_gen_heavy_positions(const kvs_gen_kv_params* p, int req, int layer, int head, int32_t* out) {
   int32_t* perm = (int32_t*)malloc(sizeof(int32_t) * (size_t)(p->ctx0 > 0 ? p->ctx0 : 1));
   uint8_t* mask = (uint8_t*)malloc((size_t)(p->ctx0 > 0 ? p->ctx0 : 1));
   if (!perm || !mask) { free(perm); free(mask); return -1; }
-  gen_heavy_set(p, req, p->heavy_shared_layers ? 0 : layer, head, perm, mask);
+  if (p->heavy_shared_layers) {
+    gen_heavy_set(p, req, 0, head, perm, mask, NULL);
+  } else {
+    /* chained sets: build layers 0..layer in order */
+    uint8_t* prev = (uint8_t*)malloc((size_t)(p->ctx0 > 0 ? p->ctx0 : 1));
+    if (!prev) { free(perm); free(mask); return -1; }
+    for (int l = 0; l <= layer; ++l) {
+      gen_heavy_set(p, req, l, head, perm, mask, l > 0 ? prev : NULL);
+      if (l < layer) memcpy(prev, mask, (size_t)p->ctx0);
+    }
+    free(prev);
+  }
   int c = 0;
   for (int64_t i = 0; i < p->ctx0; ++i) if (mask[i]) out[c++] = (int32_t)i;
   free(perm); free(mask);
@@ -218,7 +250,11 @@ int kvs_gen_fill_kv(const kvs_gen_kv_params* p, uint16_t* k, uint16_t* v) {
       for (int l = 0; l < (p->heavy_shared_layers ? 1 : p->n_layer); ++l)
         for (int h = 0; h < p->n_kv_head; ++h) {
           size_t set = ((size_t)req * (size_t)(p->heavy_shared_layers ? 1 : p->n_layer) + (size_t)l) * (size_t)p->n_kv_head + (size_t)h;
-          gen_heavy_set(p, req, l, h, perm, heavy + set * (size_t)p->ctx0);
+          const uint8_t* prev = NULL;
+          if (!p->heavy_shared_layers && l > 0)
+            prev = heavy + (((size_t)req * (size_t)p->n_layer + (size_t)(l - 1)) * (size_t)p->n_kv_head + (size_t)h) *
+                               (size_t)p->ctx0;
+          gen_heavy_set(p, req, l, h, perm, heavy + set * (size_t)p->ctx0, prev);
         }
     free(perm);
   }
