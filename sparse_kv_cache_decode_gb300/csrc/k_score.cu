@@ -167,7 +167,12 @@ cudaError_t launch_score_t(const Dims& d, const __nv_bfloat16* index, const __nv
 }  // namespace
 
 int score_supported(const Dims& d) {
-  return ((d.dk == 128 || d.dk == 576) && d.max_nq * d.G <= kScoreMaxRows) || score_tc_supported(d, d.max_nq);
+  // every call width 1..max_nq must have a kernel: tcgen05 for wide rows, mma.sync otherwise
+  for (int nq = 1; nq <= d.max_nq; ++nq) {
+    const bool mma = (d.dk == 128 || d.dk == 576) && nq * d.G <= kScoreMaxRows;
+    if (!mma && !score_tc_supported(d, nq)) return 0;
+  }
+  return 1;
 }
 
 cudaError_t launch_score(const Dims& d, const __nv_bfloat16* index, const __nv_bfloat16* q, int nq,
