@@ -1,10 +1,12 @@
 // Block selection: forced sink/recent blocks plus the top (K_b - |forced|) other blocks by
-// (score desc, block asc), emitted in ascending block order.  One CTA per unit.
+// (score desc, block asc), emitted in ascending block order.
 //
 // Radix selection over orderable 32-bit keys (8-bit digits, most significant first) finds the
 // threshold key T of the k-th best candidate and how many candidates equal to T are needed;
-// an ordered compaction (prefix sums in block order) then takes every candidate above T and
-// the lowest-index candidates equal to T.
+// an ordered compaction then takes every candidate above T and the lowest-index candidates
+// equal to T: warp ballots over contiguous segments when the keys sit in shared memory
+// (select_ordered), per-thread runs with block prefix sums when they are read from global memory.
+// Contexts up to 16384 blocks: one CTA per unit.
 //
 // Long contexts (more blocks than one CTA caches in shared memory) select in two phases so that
 // the work spreads over the SMs: (1) a grid of (chunk, unit) CTAs keeps, per chunk of 16384
