@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kCacheThreads) prefetch_kernel(Dims d, Layer L
 // units; each warp copies batches of whole items (about 512 16-byte vectors per batch), 16 loads
 // in flight per lane, from the mapped host history into the items' slots.  Only rows < L are
 // copied.
-constexpr int kFetchCTAs = 96;
+constexpr int kFetchCTAs = 64;
 constexpr int kFetchThreads = 128;   // 10K registers per CTA: fits beside two attention CTAs
 constexpr int kFetchMaxUnits = 1024;
 constexpr int kFetchUnroll = 16;
