@@ -287,6 +287,21 @@ def config_of(w):
             "parallelism": "one replica per GPU (requests are independent)"}
 
 
+def check_host_memory(history_bytes: int):
+    """Refuse to start when the host cannot hold every local rank's page-locked history (with 10%
+    slack): page-locking more than the host has would end in the OOM killer, not in an error."""
+    ranks = int(os.environ.get("LOCAL_WORLD_SIZE", "1"))
+    try:
+        with open("/proc/meminfo") as f:
+            avail = next(int(ln.split()[1]) * 1024 for ln in f if ln.startswith("MemAvailable:"))
+    except (OSError, StopIteration):
+        return
+    need = int(history_bytes * 1.1) * ranks
+    if need > avail:
+        raise RuntimeError(f"host memory: {ranks} rank(s) x {history_bytes / 2**30:.1f} GiB of history need "
+                           f"{need / 2**30:.1f} GiB, {avail / 2**30:.1f} GiB available")
+
+
 # ----------------------------------------------------------------------------- our path
 
 def run_ours(args, dist):
@@ -312,6 +327,7 @@ def run_ours(args, dist):
     if w.append:   # history capacity for every appended token of the run (timed, measured, e2e)
         w = w.with_(steps=max(w.steps, T + 8 + T_e2e + 1))
     t0 = time.time()
+    check_host_memory(w.host_kv_bytes)
     # K and V histories; each filled by the generator (which draws both in one pass), so fill into
     # a staging pair when V exists
     if w.v_shares_k:

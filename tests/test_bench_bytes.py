@@ -53,3 +53,12 @@ def test_short_contexts_read_only_present_rows():
     rows = (256 + 256 + 17) * w.n_kv_head
     assert per_layer["attn"] == rows * 256 * 2 + 3 * 8 * 128 * 2 + 3 * 8 * 128 * 4
     assert per_layer["index"] == (256 + 63 + 2) * 2 * 128 * 2
+
+
+def test_host_memory_guard(monkeypatch):
+    b = _bench()
+    b.check_host_memory(1 << 20)                                  # 1 MiB always fits
+    monkeypatch.setenv("LOCAL_WORLD_SIZE", "4")
+    import pytest
+    with pytest.raises(RuntimeError, match="host memory"):
+        b.check_host_memory(1 << 50)
