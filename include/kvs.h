@@ -123,7 +123,10 @@ kvs_status kvs_index_build(kvs_ctx* ctx, int layer, void* d_index, const int* d_
 /* Block scores of one layer [SPEC 3 step 3, OASIS module 2]:
  * s[r][h][b] = scale * max over j < nq and q heads g of group h of (score_q[r][j][g] . ik[b]),
  * fp32 with fp32 accumulation of exact bf16 products, for b < n_b(ctx_len[r]); other entries
- * are left untouched.  nq in [1, max_score_q]. */
+ * are left untouched.  nq in [1, max_score_q].  Kernels: tcgen05 tensor cores for 64-256 scoring
+ * rows per unit (nq * G) with d_k a multiple of 64; mma.sync tiles for up to 128 rows with d_k 128
+ * or 576.  A configuration any of whose call widths 1..max_score_q has neither is refused with
+ * KVS_ERR_NOT_SUPPORTED. */
 kvs_status kvs_score_blocks(kvs_ctx* ctx, int layer, const void* d_score_q, int nq, const void* d_index,
                             const int* d_ctx_len, float* d_scores, kvs_stream_t stream);
 
@@ -149,7 +152,10 @@ kvs_status kvs_cache_update(kvs_ctx* ctx, int layer, const int* d_sel, const int
 
 /* Exact decode attention over the selected slots [OASIS module 1, HISP insight 1]:
  * out[r][g] = sum_t softmax_t(scale * q[r][g] . k_t) v_t over the tokens t < ctx_len[r] of the
- * blocks sel[r][h] (h = g / G), read from their slots; fp32 accumulation, fp32 output. */
+ * blocks sel[r][h] (h = g / G), read from their slots; fp32 accumulation, fp32 output.
+ * Shapes: d_k = d_v = 128 with G <= 16 (TMA-fed kernel when block_size is a multiple of 16), or
+ * MLA (v_shares_k, d_k 576, d_v <= 512, a multiple of 128) with G <= 16 or G = 128 (heads in
+ * groups of 32 when d_v = 512); others KVS_ERR_NOT_SUPPORTED. */
 kvs_status kvs_sparse_decode_attn(kvs_ctx* ctx, int layer, const void* d_q, const int* d_sel,
                                   const int* d_slot_of_sel, const int* d_nsel, const int* d_ctx_len,
                                   float* d_out, kvs_stream_t stream);
