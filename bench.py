@@ -287,6 +287,19 @@ def config_of(w):
             "parallelism": "one replica per GPU (requests are independent)"}
 
 
+def prefetch_report(w, dstat, steps: int):
+    """Cross-layer prefetch per step from the device counters (hits, misses, evictions, prefetched,
+    prefetch hits, pin fallbacks, bytes fetched): blocks prefetched, how many of them the layer's own
+    selection then used, and the miss bytes that use hid from the step's critical path."""
+    if not w.layer_prefetch or steps <= 0:
+        return None
+    prefetched, used = float(dstat[3]) / steps, float(dstat[4]) / steps
+    block_bytes = w.block_size * (w.d_k + (0 if w.v_shares_k else w.d_v)) * 2
+    return {"blocks_per_step": round(prefetched, 1), "used_per_step": round(used, 1),
+            "used_fraction": round(used / prefetched, 4) if prefetched else None,
+            "hidden_miss_bytes_per_step": int(used * block_bytes)}
+
+
 def check_host_memory(history_bytes: int):
     """Refuse to start when the host cannot hold every local rank's page-locked history (with 10%
     slack): page-locking more than the host has would end in the OOM killer, not in an error."""
@@ -576,6 +589,7 @@ def run_ours(args, dist):
                               "frac": round(step_roof / t_step, 4),
                               "bound": "host-link" if link_step / link_peak > hbm_step / hbm_peak else "hbm"},
             "miss_fraction": round(misses / max(1.0, misses + hits), 4),
+            "prefetch": prefetch_report(w, dstat, args.steps),
             "roofline": roofline, "rooflines": rooflines, "clocks": clk, "gpu_launches": int(launches),
             "kernel_ms_per_step": {k: round(ms / max(1, n) * per_step_launches[k], 4)
                                    for k, (ms, n) in kernel_times.items()},

@@ -62,3 +62,14 @@ def test_host_memory_guard(monkeypatch):
     import pytest
     with pytest.raises(RuntimeError, match="host memory"):
         b.check_host_memory(1 << 50)
+
+
+def test_prefetch_report():
+    import numpy as np
+    b = _bench()
+    assert b.prefetch_report(W.LLAMA8B_32K, np.zeros(7), 10) is None          # no layer prefetch
+    w = W.MLA_128K
+    dstat = np.array([0, 0, 0, 5000, 2500, 0, 0], dtype=np.int64)            # over 10 steps
+    r = b.prefetch_report(w, dstat, 10)
+    assert r["blocks_per_step"] == 500 and r["used_per_step"] == 250 and r["used_fraction"] == 0.5
+    assert r["hidden_miss_bytes_per_step"] == 250 * 576 * 2                  # token blocks of the latent row
