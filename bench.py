@@ -255,7 +255,30 @@ def oracle_sample_time(w, steps_warm: int, steps_timed: int, n_layers: int):
     desc = (f"oracle (numpy, fp64) on request 0 of {w.n_req}, layers 0-{n_layers - 1} of {w.n_layer}, all "
             f"{w.n_kv_head} kv-heads ({units} of {w.n_req * w.n_layer * w.n_kv_head} units), {steps_timed} step(s) after "
             f"{steps_warm} warm-up; time scaled by units to the full step")
-    return wall / steps_timed, units, cores, desc
+    coverage = dense_softmax_coverage(ws, dec, inputs[-1][0])
+    return wall / steps_timed, units, cores, desc, coverage
+
+
+def dense_softmax_coverage(ws, dec, q):
+    """Share of the exact dense softmax mass (over every present token, fp64) that falls on the
+    tokens the step attended to, for the last oracle step: mean over the q heads of layer 0 of
+    request 0 (outside any timed region)."""
+    from oracle import bf16_to_f64
+    g, bs = ws.group, ws.block_size
+    shares = []
+    for h in range(ws.n_kv_head):
+        u = (0, 0, h)
+        L = dec.L[0]
+        k = bf16_to_f64(dec.k[u][:L])
+        qh = bf16_to_f64(q[0, 0, h * g:(h + 1) * g])
+        logits = float(ws.softmax_scale) * (qh @ k.T)
+        p = np.exp(logits - logits.max(axis=1, keepdims=True))
+        attended = np.zeros(L, bool)
+        for b in dec.records[u].attn_sel:
+            attended[b * bs:min(L, (b + 1) * bs)] = True
+        shares += list(p[:, attended].sum(axis=1) / p.sum(axis=1))
+    return {"value": round(float(np.mean(shares)), 4), "min": round(float(np.min(shares)), 4),
+            "sample": f"oracle, last step of the CPU-baseline sample, layer 0 of request 0, {len(shares)} q heads"}
 
 
 def run_reference(args, dist):
@@ -264,7 +287,7 @@ def run_reference(args, dist):
     w = W.get(args.workload)
     total_units = w.n_req * w.n_layer * w.n_kv_head
     n_layers = max(1, min(w.n_layer, 2))
-    per_step, units, cores, desc = oracle_sample_time(w, max(1, args.warmup), max(1, args.steps), n_layers)
+    per_step, units, cores, desc, coverage = oracle_sample_time(w, max(1, args.warmup), max(1, args.steps), n_layers)
     full_step = per_step * total_units / units
     value = 1.0 / full_step
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
@@ -272,6 +295,7 @@ def run_reference(args, dist):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(w),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+            "dense_softmax_coverage": coverage,
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -598,10 +622,11 @@ def run_ours(args, dist):
     if e2e:
         line["e2e"] = e2e
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        per_step, units, cores, desc = oracle_sample_time(w, 1, 3, min(w.n_layer, 8))
+        per_step, units, cores, desc, coverage = oracle_sample_time(w, 1, 3, min(w.n_layer, 8))
         full = per_step * (w.n_req * w.n_layer * w.n_kv_head) / units
         line["cpu_baseline"] = {"value": round(1.0 / full, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": desc}
+        line["dense_softmax_coverage"] = coverage
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     ctx.close()

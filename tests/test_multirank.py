@@ -63,6 +63,8 @@ def test_reference_arm_prints_on_rank_zero_only():
     assert lines[1] == ""
     j = json.loads(lines[0].splitlines()[-1])
     assert j["impl"] == "reference" and j["value"] > 0 and j["cpu_baseline"]["kind"] == "oracle"
+    cov = j["dense_softmax_coverage"]
+    assert 0.0 < cov["min"] <= cov["value"] <= 1.0
 
 
 def test_ranks_serve_different_requests():
