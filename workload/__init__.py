@@ -79,6 +79,12 @@ def lib():
             _lib.kvs_gen_draft.argtypes = [P(_QParams), ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                            ctypes.c_double, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                            ctypes.c_int64]
+            _lib.kvs_gen_draft_noise_advance.argtypes = [P(_QParams), ctypes.c_void_p, ctypes.c_int64,
+                                                         ctypes.c_int, ctypes.c_double]
+            _lib.kvs_gen_draft_with_noise.argtypes = [P(_QParams), ctypes.c_void_p, ctypes.c_void_p,
+                                                      ctypes.c_double, ctypes.c_void_p, ctypes.c_int64,
+                                                      ctypes.c_int64, ctypes.c_int64]
+            _lib.kvs_gen_draft_with_noise.restype = None
             _lib.kvs_gen_uniform_f32.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                                                  ctypes.c_float, ctypes.c_void_p]
             _lib.kvs_gen_uniform_f32.restype = None
@@ -116,6 +122,7 @@ class Workload:
     lookahead: bool = False
     n_draft: int = 0
     draft_sigma: float = 0.3
+    draft_rho: float = 0.0   # AR(1) coefficient of each draft slot's noise over steps (0: fresh noise every step)
     append: bool = False
     layer_prefetch: bool = False
     rho: float = 0.9
@@ -179,31 +186,66 @@ TINY = Workload(name="tiny", n_req=1, n_layer=1, n_q_head=8, n_kv_head=2, d_k=12
                 ctx0=4096, steps=32, budget_blocks=16, n_sink=1, n_recent=2, cap_blocks=32, rho=0.9,
                 n_heavy=32, heavy_scale=4.0)
 
+# Step-to-step selection overlap |S_t & S_t-1| / |S_t| is set by rho (and, for the drafts, by
+# draft_rho): with N(0,1) keys a block's mean-key score moves with every change of the query, so
+# rho = 0.9-0.95 gives only 62-77% overlap here.  The values below were calibrated on the oracle's
+# selections of request 0 (tests/test_workload_overlap.py checks them): 32K lookahead rho 0.99 with
+# draft noise AR(1) at 0.99 -> 0.87; 128K rho 0.991 -> 0.85; MLA rho 0.97 -> 0.86.
 LLAMA8B_32K = Workload(name="llama8b_32k_lookahead", n_req=8, n_layer=32, n_q_head=32, n_kv_head=8, d_k=128,
                        d_v=128, block_size=16, ctx0=32768, steps=64, budget_blocks=128, n_sink=1, n_recent=2,
-                       cap_blocks=192, lookahead=True, n_draft=4, draft_sigma=0.3, rho=0.9,
+                       cap_blocks=192, lookahead=True, n_draft=4, draft_sigma=0.3, draft_rho=0.99, rho=0.99,
                        n_heavy=_heavy(0.01, 32768), heavy_scale=3.0)
 
 LONG_128K = Workload(name="llama8b_128k_append", n_req=4, n_layer=32, n_q_head=32, n_kv_head=8, d_k=128,
                      d_v=128, block_size=16, ctx0=131072, steps=128, budget_blocks=128, n_sink=1, n_recent=2,
-                     cap_blocks=256, append=True, rho=0.95, n_heavy=_heavy(0.01, 131072), heavy_scale=3.0)
+                     cap_blocks=256, append=True, rho=0.991, n_heavy=_heavy(0.01, 131072), heavy_scale=3.0)
 
 MLA_128K = Workload(name="mla_128k_token_topk", n_req=16, n_layer=16, n_q_head=128, n_kv_head=1, d_k=576,
                     d_v=512, v_shares_k=True, block_size=1, ctx0=131072, steps=32, budget_blocks=2048,
-                    n_sink=0, n_recent=0, cap_blocks=3072, layer_prefetch=True, rho=0.9, rho_layer=0.6,
+                    n_sink=0, n_recent=0, cap_blocks=3072, layer_prefetch=True, rho=0.97, rho_layer=0.6,
                     n_heavy=_heavy(0.01, 131072), heavy_scale=3.0, heavy_keep=0.75)
-# heavy_keep 0.75 (each layer keeps 3/4 of the layer below's heavy positions) gives a 49% mean
-# adjacent-layer selection overlap at step 0 and 5 of requests 0-1 (oracle selections), for the
-# ~50% the workload asks for; rho_layer alone moves it by less than a point
+# heavy_keep 0.75 (each layer keeps 3/4 of the layer below's heavy positions) gives a 50% mean
+# adjacent-layer selection overlap (oracle selections of request 0, layers 0-1), for the ~50% the
+# workload asks for; rho_layer alone moves it by less than a point
+
+# Budget/eviction sweep: rho per (block size, budget tokens, target overlap %), bisected on the
+# oracle's selections of request 0, layer 0, all 8 kv-heads over 10 steps; the comment is the overlap
+# reached there.
+SWEEP_RHO = {
+    (16, 512, 50): 0.884522,   # 0.492
+    (16, 512, 80): 0.986665,   # 0.803
+    (16, 512, 95): 0.999,   # 0.942
+    (16, 1024, 50): 0.884522,   # 0.508
+    (16, 1024, 80): 0.986665,   # 0.809
+    (16, 1024, 95): 0.999,   # 0.948
+    (16, 2048, 50): 0.866648,   # 0.505
+    (16, 2048, 80): 0.979465,   # 0.795
+    (16, 2048, 95): 0.999,   # 0.951
+    (16, 4096, 50): 0.834518,   # 0.499
+    (16, 4096, 80): 0.976286,   # 0.800
+    (16, 4096, 95): 0.999,   # 0.958
+    (64, 512, 50): 0.726158,   # 0.505
+    (64, 512, 80): 0.972616,   # 0.800
+    (64, 512, 95): 0.999438,   # 0.950
+    (64, 1024, 50): 0.834518,   # 0.504
+    (64, 1024, 80): 0.979465,   # 0.798
+    (64, 1024, 95): 0.999,   # 0.944
+    (64, 2048, 50): 0.846007,   # 0.493
+    (64, 2048, 80): 0.982217,   # 0.808
+    (64, 2048, 95): 0.999,   # 0.954
+    (64, 4096, 50): 0.822172,   # 0.503
+    (64, 4096, 80): 0.976286,   # 0.801
+    (64, 4096, 95): 0.999,   # 0.957
+}
 
 
-def sweep_workload(block_size: int, budget_tokens: int, rho: float, n_layer: int = 8) -> Workload:
+def sweep_workload(block_size: int, budget_tokens: int, rho: float, n_layer: int = 8, name: str = "") -> Workload:
     """Budget/eviction sweep case: 8B shape, batch 32, context 65536, cache 1.25x budget.
 
     32 layers would need 256 GiB of pinned host memory; the GPU host has 199 GB, so the
     sweep runs with n_layer = 8 (64 GiB) by default."""
     kb = budget_tokens // block_size
-    return Workload(name=f"sweep_bs{block_size}_b{budget_tokens}_rho{rho:g}", n_req=32, n_layer=n_layer,
+    return Workload(name=name or f"sweep_bs{block_size}_b{budget_tokens}_rho{rho:g}", n_req=32, n_layer=n_layer,
                     n_q_head=32, n_kv_head=8, d_k=128, d_v=128, block_size=block_size, ctx0=65536, steps=64,
                     budget_blocks=kb, n_sink=1, n_recent=2, cap_blocks=(kb * 5) // 4, rho=rho,
                     n_heavy=_heavy(0.01, 65536), heavy_scale=3.0)
@@ -225,14 +267,21 @@ WORKLOADS = {w.name: w for w in (TINY, TINY_LOOKAHEAD, TINY_APPEND, TINY_PREFETC
 
 
 def get(name: str) -> Workload:
-    """A named workload, or a sweep case named sweep_bs<B>_b<tokens>_rho<r>[_l<layers>]."""
+    """A named workload, or a sweep case named sweep_bs<B>_b<tokens>_rho<r>[_l<layers>] (rho given) or
+    sweep_bs<B>_b<tokens>_ov<percent>[_l<layers>] (rho from the calibrated table)."""
     if name in WORKLOADS:
         return WORKLOADS[name]
     import re
     m = re.fullmatch(r"sweep_bs(\d+)_b(\d+)_rho([0-9.]+)(?:_l(\d+))?", name)
-    if not m:
-        raise KeyError(f"unknown workload {name!r}")
-    return sweep_workload(int(m.group(1)), int(m.group(2)), float(m.group(3)), int(m.group(4) or 8))
+    if m:
+        return sweep_workload(int(m.group(1)), int(m.group(2)), float(m.group(3)), int(m.group(4) or 8))
+    m = re.fullmatch(r"sweep_bs(\d+)_b(\d+)_ov(\d+)(?:_l(\d+))?", name)
+    if m:
+        key = (int(m.group(1)), int(m.group(2)), int(m.group(3)))
+        if key not in SWEEP_RHO:
+            raise KeyError(f"no calibrated rho for sweep case {name!r}")
+        return sweep_workload(key[0], key[1], SWEEP_RHO[key], int(m.group(4) or 8), name=name)
+    raise KeyError(f"unknown workload {name!r}")
 
 
 # --------------------------------------------------------------------------- fills
@@ -295,7 +344,10 @@ class QueryStream:
 
     q_t follows an AR(1) over steps per (layer, req, head): q_0 = e_0,
     q_t = rho q_{t-1} + sqrt(1 - rho^2) e_t (fp64, stored bf16).  Draft j of step t is
-    q_{t+j} + N(0, sigma^2), j = 1..n_draft (lookahead drafts predict the next positions)."""
+    q_{t+j} + sigma n_{t,j}, j = 1..n_draft (lookahead drafts predict the next positions), where
+    the noise n_{t,j} ~ N(0, 1) of draft slot j is itself an AR(1) over steps with coefficient
+    draft_rho (0: independent noise every step).  Both are forward-only streams: steps are
+    requested in increasing order (a step may be asked for again)."""
 
     def __init__(self, w: Workload):
         self.w = w
@@ -304,6 +356,7 @@ class QueryStream:
         self._base = {}   # t -> fp64 base state
         self._last_t = -1
         self._state = np.zeros(self.n, np.float64)
+        self._noise = {}   # draft slot j -> [last step, fp64 noise state, {step: bf16 drafts of slot j}]
 
     def _base_at(self, t: int) -> np.ndarray:
         if t in self._base:
@@ -333,6 +386,18 @@ class QueryStream:
         lib().kvs_gen_to_bf16(ctypes.byref(self.p), q.ctypes.data, q.size, out.ctypes.data)
         return out
 
+    def _noise_at(self, t: int, j: int) -> np.ndarray:
+        st = self._noise.setdefault(j, [-1, np.zeros(self.n, np.float64)])
+        if t < st[0]:
+            raise ValueError("QueryStream drafts only move forward")
+        while st[0] < t:
+            st[0] += 1
+            rc = lib().kvs_gen_draft_noise_advance(ctypes.byref(self.p), st[1].ctypes.data, st[0], j,
+                                                   self.w.draft_rho)
+            if rc != 0:
+                raise ValueError("kvs_gen_draft_noise_advance failed")
+        return st[1]
+
     def drafts(self, t: int) -> np.ndarray:
         w = self.w
         nd = w.n_draft
@@ -340,9 +405,14 @@ class QueryStream:
         for j in range(1, nd + 1):
             qf = self._values(t + j)
             sub = out[:, :, j - 1]
-            rc = lib().kvs_gen_draft(ctypes.byref(self.p), qf.ctypes.data, t, j, w.draft_sigma,
-                                     sub.ctypes.data, out.strides[0] // 2, out.strides[1] // 2,
-                                     out.strides[3] // 2)
-            if rc != 0:
-                raise ValueError("kvs_gen_draft failed")
+            strides = (out.strides[0] // 2, out.strides[1] // 2, out.strides[3] // 2)
+            if w.draft_rho == 0.0:
+                rc = lib().kvs_gen_draft(ctypes.byref(self.p), qf.ctypes.data, t, j, w.draft_sigma,
+                                         sub.ctypes.data, *strides)
+                if rc != 0:
+                    raise ValueError("kvs_gen_draft failed")
+            else:
+                noise = self._noise_at(t, j)
+                lib().kvs_gen_draft_with_noise(ctypes.byref(self.p), qf.ctypes.data, noise.ctypes.data,
+                                               w.draft_sigma, sub.ctypes.data, *strides)
         return out

@@ -373,6 +373,40 @@ int kvs_gen_draft(const kvs_gen_q_params* p, const double* q_future, int64_t t, 
   return 0;
 }
 
+/* Draft noise of draft slot j at step t, as an AR(1) over steps with coefficient rho_d:
+ * n_0 = eps_0, n_t = rho_d * n_{t-1} + sqrt(1 - rho_d^2) * eps_t, eps from stream 4 at pos = 8 t + j
+ * (the draws kvs_gen_draft uses), so every n_t is N(0, 1) and rho_d = 0 gives kvs_gen_draft's noise.
+ * state [layer][req][head][d] fp64 holds n_{t-1} on entry (ignored at t = 0) and n_t on return. */
+int kvs_gen_draft_noise_advance(const kvs_gen_q_params* p, double* state, int64_t t, int j, double rho_d) {
+  if (!kvs_gen_counter_limits_ok(p->n_req, p->n_layer, p->n_q_head, 8 * t + j + 1, p->d)) return -1;
+  double s = sqrt(1.0 - rho_d * rho_d);
+  size_t i = 0;
+  for (int l = 0; l < p->n_layer; ++l)
+    for (int r = 0; r < p->n_req; ++r)
+      for (int h = 0; h < p->n_q_head; ++h)
+        for (int pr = 0; pr < p->d / 2; ++pr, i += 2) {
+          double z0, z1;
+          gen_normal_pair(gen_at(p->seed, gen_ctr(4, r, l, h, 8 * t + j, pr)), &z0, &z1);
+          if (t == 0) { state[i] = z0; state[i + 1] = z1; }
+          else { state[i] = rho_d * state[i] + s * z0; state[i + 1] = rho_d * state[i + 1] + s * z1; }
+        }
+  return 0;
+}
+
+/* Draft query from the fp64 future query and a noise state: bf16(q_future + sigma * noise), laid
+ * out like kvs_gen_draft's output. */
+void kvs_gen_draft_with_noise(const kvs_gen_q_params* p, const double* q_future, const double* noise, double sigma,
+                              uint16_t* out, int64_t out_layer_stride, int64_t out_req_stride,
+                              int64_t out_head_stride) {
+  size_t i = 0;
+  for (int l = 0; l < p->n_layer; ++l)
+    for (int r = 0; r < p->n_req; ++r)
+      for (int h = 0; h < p->n_q_head; ++h) {
+        uint16_t* o = out + l * out_layer_stride + r * out_req_stride + h * out_head_stride;
+        for (int k = 0; k < p->d; ++k, ++i) o[k] = gen_store(q_future[i] + sigma * noise[i], p->int_scale, p->int_clip);
+      }
+}
+
 /* Seeded uniform fp32 array in [lo, hi) from stream `stream` (used for stand-alone score arrays). */
 void kvs_gen_uniform_f32(uint64_t seed, int stream, int64_t n, float lo, float hi, float* out) {
   for (int64_t i = 0; i < n; ++i) {
