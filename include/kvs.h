@@ -225,9 +225,22 @@ kvs_status kvs_kernel_timer_read(kvs_ctx* ctx, int kernel, double* total_ms, int
 /* Number of kernels this context has launched (or captured into graphs) so far. */
 unsigned long long kvs_launch_count(kvs_ctx* ctx);
 
+/* Host-link read probe (diagnostics; no counterpart in the pages): n_ctas CTAs of `threads`
+ * threads read n_items items of item_bytes each from page-locked, device-mapped host memory at
+ * h_base + d_offsets[i] (device array, bytes), with the block fetch's access pattern (one item per
+ * warp, 16-byte loads, up to 16 per lane in flight), and write nothing but a sentinel hit count to
+ * d_sink[0]; items outside [0, region_bytes) or not 16-byte aligned are skipped and counted in
+ * d_sink[1] (the caller zeroes both words).  Timing the call gives the link's SM zero-copy read
+ * rate for that pattern.  item_bytes a positive multiple of 16; threads a multiple of 32 in
+ * [32, 1024].  Errors: KVS_ERR_INVALID_ARG, KVS_ERR_HOST_MEM (h_base not device-mapped). */
+kvs_status kvs_probe_host_read(const void* h_base, size_t region_bytes, const long long* d_offsets, int n_items,
+                               int item_bytes, int n_ctas, int threads, unsigned* d_sink, kvs_stream_t stream);
+
 /* Block selection that allocates nothing (no counterpart in the pages: an interface for callers
- * that cannot allocate device memory, e.g. code running inside an allocator hook or host
- * callback, or a plug-in in a process whose device memory another runtime owns).  Scores and
+ * that cannot allocate device memory, e.g. code running inside an allocator hook, or a plug-in in
+ * a process whose device memory another runtime owns).  It makes CUDA API calls (device query,
+ * symbol lookup, kernel launches), so it must not be called from a stream callback or a
+ * cudaLaunchHostFunc host function.  Scores and
  * selects one layer's blocks exactly as kvs_score_blocks followed by kvs_topk_select, without a
  * kvs_ctx or workspace: the block scores live in a file-scope device array of
  * KVS_NOALLOC_MAX_SCORES floats (8 MiB) that every GPU loading the library holds until exit.
@@ -235,9 +248,13 @@ unsigned long long kvs_launch_count(kvs_ctx* ctx);
  *   d_score_q    [B][nq][H_q][d_k] bf16 scoring queries, 1 <= nq <= cfg->max_score_q
  *   d_index_layer one layer's index keys [B][H_kv][n_b(max_ctx)][d_k] bf16
  *   d_ctx_len    [B] int32;  d_sel [B][H_kv][K_b] int32 and d_nsel [B][H_kv] int32 outputs
- *   d_status     optional device word that receives device-side errors (sticky; NULL: a word of
- *                the library's own, not readable by the caller)
- * Returns KVS_ERR_INVALID_ARG when B * H_kv * n_b(max_ctx) > KVS_NOALLOC_MAX_SCORES.  The first
+ *   d_status     optional device word that receives device-side errors (sticky), such as
+ *                KVS_ERR_BAD_INDEX for a ctx_len above max_ctx.  With d_status NULL such errors
+ *                go to a word of the library's own that the caller cannot read, and the units
+ *                they hit leave sel / nsel unwritten (stale values from earlier calls): pass a
+ *                status word wherever ctx_len is not known to be valid.
+ * Returns KVS_ERR_CAPACITY when B * H_kv * n_b(max_ctx) > KVS_NOALLOC_MAX_SCORES (checked before
+ * any pointer), KVS_ERR_INVALID_ARG for a bad config, pointer or nq.  The first
  * call on a device looks up the array's device address (cudaGetSymbolAddress); make that first
  * call before any stream capture.  All calls share the array, so calls that overlap on the GPU
  * (other streams, other threads) race; every score a call reads is written by that same call. */

@@ -69,6 +69,7 @@ _SIGS = {
     "kvs_kernel_timer_read": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_I)]),
     "kvs_launch_count": (ctypes.c_ulonglong, [_P]),
     "kvs_select_blocks_noalloc": (_I, [ctypes.POINTER(KvsConfig), _P, _I, _P, _P, _P, _P, _P, _P]),
+    "kvs_probe_host_read": (_I, [_P, ctypes.c_size_t, _P, _I, _I, _I, _I, _P, _P]),
 }
 
 KERNEL_IDS = {"score": 1, "topk": 2, "update": 3, "fetch": 4, "attn": 5, "prefetch": 6, "append": 7, "index": 8}
@@ -352,6 +353,14 @@ def select_blocks_noalloc(cfg: KvsConfig, score_q, nq: int, index_layer, ctx_len
     _check(lib().kvs_select_blocks_noalloc(ctypes.byref(cfg), _ptr(score_q), nq, _ptr(index_layer), _ptr(ctx_len),
                                            _ptr(sel), _ptr(nsel), _ptr(status), _stream(stream)),
            "kvs_select_blocks_noalloc")
+
+
+def probe_host_read(h_base, region_bytes: int, offsets, item_bytes: int, n_ctas: int, threads: int, sink,
+                    stream=None) -> None:
+    """kvs_probe_host_read: SM zero-copy reads of items at device-resident byte offsets (int64)
+    from page-locked, device-mapped host memory (diagnostics for the host-link peak)."""
+    _check(lib().kvs_probe_host_read(_ptr(h_base), region_bytes, _ptr(offsets), int(offsets.numel()), item_bytes,
+                                     n_ctas, threads, _ptr(sink), _stream(stream)), "kvs_probe_host_read")
 
 
 def version() -> str:

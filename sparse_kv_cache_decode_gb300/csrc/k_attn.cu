@@ -54,8 +54,13 @@ __global__ void __launch_bounds__(AttnCfg<DK, MT, VSHARE>::NW * 32)
   const int split = blockIdx.x, u = blockIdx.y, z = blockIdx.z;
   const int r = u / d.Hkv, h = u % d.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int len = ctx_len[r];
-  const int n = nsel[u];
+  int len = ctx_len[r];
+  int n = nsel[u];
+  if (len < 0 || len > d.max_ctx || n < 0 || n > d.Kb) {   // reported; the unit attends to nothing
+    if (tid == 0) set_error(L.err, KVS_ERR_BAD_INDEX);
+    len = 0;
+    n = 0;
+  }
   const int i0 = min(n, split * blocks_per_split), i1 = min(n, i0 + blocks_per_split);
   const int nblk = i1 - i0;
   const int n_tok = nblk * d.bs;
@@ -71,8 +76,15 @@ __global__ void __launch_bounds__(AttnCfg<DK, MT, VSHARE>::NW * 32)
     *reinterpret_cast<uint4*>(qs + row * KRS + ch * 16) = v;
   }
   for (int i = tid; i < nblk; i += NW * 32) {
-    s_slot[i] = slot_of_sel[(size_t)u * d.Kb + i0 + i];
-    s_blk[i] = sel[(size_t)u * d.Kb + i0 + i];
+    int slot = slot_of_sel[(size_t)u * d.Kb + i0 + i];
+    int blk = sel[(size_t)u * d.Kb + i0 + i];
+    if (blk < 0 || blk >= n_blocks_of(len, d.bs) || slot < 0 || slot >= d.C) {   // reported, then masked
+      set_error(L.err, KVS_ERR_BAD_INDEX);
+      slot = -1;
+      blk = 0;
+    }
+    s_slot[i] = slot;
+    s_blk[i] = blk;
   }
   __syncthreads();
 
@@ -360,8 +372,13 @@ __global__ void __launch_bounds__(mla::NW * 32, 2)
   const int r = u / d.Hkv, h = u % d.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ht = warp >> 2, qq = warp & 3;
-  const int len = ctx_len[r];
-  const int n = nsel[u];
+  int len = ctx_len[r];
+  int n = nsel[u];
+  if (len < 0 || len > d.max_ctx || n < 0 || n > d.Kb) {   // reported; the unit attends to nothing
+    if (tid == 0) set_error(L.err, KVS_ERR_BAD_INDEX);
+    len = 0;
+    n = 0;
+  }
   const int i0 = min(n, split * blocks_per_split), i1 = min(n, i0 + blocks_per_split);
   const int nblk = i1 - i0;
   const int n_tiles = (nblk * d.bs + 15) / 16;
@@ -373,8 +390,15 @@ __global__ void __launch_bounds__(mla::NW * 32, 2)
         reinterpret_cast<const uint4*>(q + ((size_t)r * d.Hq + head0 + row) * DK)[ch];
   }
   for (int i = tid; i < nblk; i += NW * 32) {
-    s_slot[i] = slot_of_sel[(size_t)u * d.Kb + i0 + i];
-    s_blk[i] = sel[(size_t)u * d.Kb + i0 + i];
+    int slot = slot_of_sel[(size_t)u * d.Kb + i0 + i];
+    int blk = sel[(size_t)u * d.Kb + i0 + i];
+    if (blk < 0 || blk >= n_blocks_of(len, d.bs) || slot < 0 || slot >= d.C) {   // reported, then masked
+      set_error(L.err, KVS_ERR_BAD_INDEX);
+      slot = -1;
+      blk = 0;
+    }
+    s_slot[i] = slot;
+    s_blk[i] = blk;
   }
   __syncthreads();
 
@@ -574,13 +598,8 @@ cudaError_t launch_attn_t(const Dims& d, const Layer& L, const __nv_bfloat16* q,
                           const int* slot_of_sel, const int* nsel, const int* ctx_len, float* out, cudaStream_t s) {
   using Cfg = AttnCfg<DK, MT, VSHARE>;
   auto kern = attn_kernel<DK, MT, VSHARE>;
-  static bool attr_set = false;
-  cudaError_t e;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), Cfg::SMEM);
+  if (e != cudaSuccess) return e;
   const int nz = d.dv / kDVC;
   int n_split, bps;
   if (!attention_split(d, &n_split, &bps)) return cudaErrorInvalidValue;
@@ -596,13 +615,8 @@ bool mla_path(const Dims& d) { return d.v_shares_k && d.dk == 576 && d.dv == 512
 
 cudaError_t launch_attn_mla(const Dims& d, const Layer& L, const __nv_bfloat16* q, const int* sel,
                             const int* slot_of_sel, const int* nsel, const int* ctx_len, float* out, cudaStream_t s) {
-  static bool attr_set = false;
-  cudaError_t e;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(attn_mla_kernel), mla::SMEM);
+  if (e != cudaSuccess) return e;
   int n_split, bps;
   if (!attention_split(d, &n_split, &bps)) return cudaErrorInvalidValue;
   dim3 grid(n_split, d.U, d.G / mla::HEADS);
@@ -623,7 +637,7 @@ int attention_split(const Dims& d, int* n_split_out, int* bps_out) {
   if (d.v_shares_k) smem = d.G <= 16 ? AttnCfg<576, 1, true>::SMEM : AttnCfg<576, 8, true>::SMEM;
   if (mla_path(d)) smem = mla::SMEM;
   const int per_sm = max(1, min(2, (227 * 1024) / (smem + 1024)));
-  const int slots = 152 * per_sm;
+  const int slots = device_sm_count() * per_sm;
   // split count with the least time: waves (rounded up) x (selection share of a CTA + a fixed
   // per-CTA cost, ~3% of a whole selection); at least 2 blocks per split
   const int cap = max(1, min(kAttnSplitMax, (d.Kb + 1) / 2));

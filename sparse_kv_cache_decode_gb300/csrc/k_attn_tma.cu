@@ -88,17 +88,34 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
     *abort_flag = 0;
     mbar_fence_init();
   }
+  // stage the units' lengths and the range's (block, slot) pairs; an out-of-range length, count,
+  // block id or slot is reported as KVS_ERR_BAD_INDEX and its tiles are skipped (no tensor load
+  // ever addresses another unit's slots)
   for (int j = tid; j <= u_last - u_first; j += blockDim.x) {
-    u_len[j] = ctx_len[(u_first + j) / d.Hkv];
-    u_n[j] = nsel[u_first + j];
+    int len = ctx_len[(u_first + j) / d.Hkv];
+    int n = nsel[u_first + j];
+    if (len < 0 || len > d.max_ctx || n < 0 || n > d.Kb) {
+      set_error(L.err, KVS_ERR_BAD_INDEX);
+      len = 0;
+      n = 0;
+    }
+    u_len[j] = len;
+    u_n[j] = n;
   }
   __syncthreads();
   for (int i = tid; i < (int)(p1 - p0); i += blockDim.x) {
     const long long p = p0 + i;
     const int u = (int)(p / d.Kb), ii = (int)(p % d.Kb);
     const bool live = ii < u_n[u - u_first];
-    m_blk[i] = live ? sel[(size_t)u * d.Kb + ii] : -1;
-    m_slot[i] = live ? slot_of_sel[(size_t)u * d.Kb + ii] : 0;
+    int blk = live ? sel[(size_t)u * d.Kb + ii] : -1;
+    int slot = live ? slot_of_sel[(size_t)u * d.Kb + ii] : 0;
+    if (live && (blk < 0 || blk >= n_blocks_of(u_len[u - u_first], d.bs) || slot < 0 || slot >= d.C)) {
+      set_error(L.err, KVS_ERR_BAD_INDEX);
+      blk = -1;
+      slot = 0;
+    }
+    m_blk[i] = blk;
+    m_slot[i] = slot;
   }
   __syncthreads();
 
@@ -136,8 +153,9 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
       set_error(L.err, KVS_ERR_TIMEOUT);
       *abort_flag = 1;
     }
-    // do not leave while tensor loads into this CTA's shared memory may be in flight
-    for (int j = max(0, k - kStages); j < k; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1, timeout_ns);
+    // do not leave while tensor loads into this CTA's shared memory may be in flight; this wait has
+    // its own fixed bound, so a short caller timeout cannot retire the CTA under a pending load
+    for (int j = max(0, k - kStages); j < k; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1, kDrainTimeoutNs);
     return;
   }
 
@@ -354,16 +372,7 @@ __global__ void __launch_bounds__(kMergeThreads) attn_tma_merge(Dims d, Layer L,
   }
 }
 
-int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 152;
-  }
-  return n;
-}
+int sm_count() { return device_sm_count(); }
 
 }  // namespace
 
@@ -377,13 +386,10 @@ int attention_tma_partials(const Dims& d) { return make_plan(d, sm_count()).max_
 cudaError_t launch_attention_tma(const Dims& d, const Layer& L, const CUtensorMap* tmK, const CUtensorMap* tmV,
                                  const __nv_bfloat16* q, const int* sel, const int* slot_of_sel, const int* nsel,
                                  const int* ctx_len, float* out, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_tma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(attn_tma_kernel<true>), kSmem);
+    if (e == cudaSuccess) e = set_max_dynamic_smem(reinterpret_cast<const void*>(attn_tma_kernel<false>), kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   Plan plan = make_plan(d, sm_count());
   if (d.G <= 8)

@@ -129,7 +129,10 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
   const int n = nsel[u];
   const int nb = n_blocks_of(len, d.bs);
   if (len < 0 || len > d.max_ctx || n < 0 || n > d.Kb) {
-    if (tid == 0) set_error(L.err, KVS_ERR_BAD_INDEX);
+    if (tid == 0) {
+      set_error(L.err, KVS_ERR_BAD_INDEX);
+      L.n_fetch[u] = 0;
+    }
     return;
   }
   const int* su = sel + (size_t)u * d.Kb;
@@ -137,9 +140,7 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
   int* s2b = L.slot2block + (size_t)u * d.C;
   unsigned* st = L.stamp + (size_t)u * d.C;
   if (tid == 0) {
-    unsigned clk = L.clock[u] + 1u;
-    L.clock[u] = clk;
-    s_now = 2u * clk;
+    s_now = 2u * (L.clock[u] + 1u);   // written back only once the update is accepted
     s_bad = 0;
   }
   if (tid < 4) s_cnt[tid] = 0;
@@ -154,7 +155,8 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
   unsigned long long my_pfh = 0;
   for (int i = i0; i < i1; ++i) {
     int b = su[i];
-    if (b < 0 || b >= nb) { s_bad = 1; continue; }
+    // a selection is strictly ascending (top-K output order); anything else is refused
+    if (b < 0 || b >= nb || (i > 0 && su[i - 1] >= b)) { s_bad = 1; continue; }
     int s = b2s[b];
     if (s >= d.C) { s_bad = 1; continue; }
     if (s >= 0) {
@@ -167,7 +169,10 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
   }
   __syncthreads();
   if (s_bad) {
-    if (tid == 0) set_error(L.err, KVS_ERR_BAD_INDEX);
+    if (tid == 0) {
+      set_error(L.err, KVS_ERR_BAD_INDEX);
+      L.n_fetch[u] = 0;
+    }
     return;
   }
   int m;
@@ -198,9 +203,14 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
   bool fallback = false;
   if (n_el < m && pinned) { fallback = true; n_el = n_el_nopin; }
   if (n_el < m) {
-    if (tid == 0) set_error(L.err, KVS_ERR_CAPACITY);
+    if (tid == 0) {
+      set_error(L.err, KVS_ERR_CAPACITY);
+      L.n_fetch[u] = 0;
+    }
     return;
   }
+  // accepted: a refused update (bad index, capacity) leaves the unit's state as it was
+  if (tid == 0) L.clock[u] = now / 2u;
   const uint8_t emask = fallback ? 1 : 3;
   select_victims(
       d.C, m, [&](int s) { return (sm.flags[s] & emask) == 0; },
@@ -261,7 +271,10 @@ __global__ void __launch_bounds__(kCacheThreads) prefetch_kernel(Dims d, Layer L
   const int nh = hint_n[u];
   const int nb = n_blocks_of(len, d.bs);
   if (len < 0 || len > d.max_ctx || nh < 0 || nh > d.Kb) {
-    if (tid == 0) set_error(L.err, KVS_ERR_BAD_INDEX);
+    if (tid == 0) {
+      set_error(L.err, KVS_ERR_BAD_INDEX);
+      L.n_fetch[u] = 0;
+    }
     return;
   }
   const int* hu = hint + (size_t)u * d.Kb;
@@ -279,14 +292,17 @@ __global__ void __launch_bounds__(kCacheThreads) prefetch_kernel(Dims d, Layer L
   int my_nr = 0;
   for (int i = i0; i < i1; ++i) {
     int b = hu[i];
-    if (b < 0 || b >= nb) { s_bad = 1; continue; }
+    if (b < 0 || b >= nb || (i > 0 && hu[i - 1] >= b)) { s_bad = 1; continue; }
     int s = b2s[b];
     if (s >= d.C) { s_bad = 1; continue; }
     if (s >= 0) sm.flags[s] = 1; else ++my_nr;
   }
   __syncthreads();
   if (s_bad) {
-    if (tid == 0) set_error(L.err, KVS_ERR_BAD_INDEX);
+    if (tid == 0) {
+      set_error(L.err, KVS_ERR_BAD_INDEX);
+      L.n_fetch[u] = 0;
+    }
     return;
   }
   int n_nr;
@@ -423,7 +439,7 @@ cudaError_t launch_cache_update(const Dims& d, const Layer& L, const int* sel, c
                                 int* slot_of_sel, kvs_stats* stats, cudaStream_t s) {
   size_t smem = cache_smem_bytes(d);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(cache_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(cache_update_kernel), (int)smem);
     if (e != cudaSuccess) return e;
   }
   cache_update_kernel<<<d.U, kCacheThreads, smem, s>>>(d, L, sel, nsel, ctx_len, slot_of_sel, stats);
@@ -434,7 +450,7 @@ cudaError_t launch_prefetch(const Dims& d, const Layer& L, const int* hint, cons
                             kvs_stats* stats, cudaStream_t s) {
   size_t smem = cache_smem_bytes(d);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(prefetch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(prefetch_kernel), (int)smem);
     if (e != cudaSuccess) return e;
   }
   prefetch_kernel<<<d.U, kCacheThreads, smem, s>>>(d, L, hint, hint_n, ctx_len, stats);

@@ -1,9 +1,10 @@
 // Block selection for callers that cannot allocate device memory.
 //
 // Some callers cannot call cudaMalloc (or have torch allocate for them): code that runs inside
-// a host callback or an allocator hook where re-entering the allocator deadlocks, plug-ins that
-// live in a process whose device memory is fully budgeted by another runtime, or embedded
-// deployments that forbid allocation after start-up.  kvs_select_blocks_noalloc serves them: it
+// an allocator hook, where re-entering the allocator deadlocks, plug-ins that live in a process
+// whose device memory is fully budgeted by another runtime, or embedded deployments that forbid
+// allocation after start-up.  (It makes CUDA API calls itself, so it must not be called from a
+// stream callback or a cudaLaunchHostFunc host function.)  kvs_select_blocks_noalloc serves them: it
 // scores and selects one layer's blocks (the same kernels as kvs_score_blocks followed by
 // kvs_topk_select) with the block scores kept in the file-scope device array below, so the
 // caller passes only its inputs and outputs.  The array (KVS_NOALLOC_MAX_SCORES floats) is held
@@ -52,9 +53,10 @@ extern "C" kvs_status kvs_select_blocks_noalloc(const kvs_config* cfg, const voi
                                                 int* d_nsel, unsigned* d_status, kvs_stream_t stream) {
   kvs::Dims d;
   if (!kvs::config_to_dims(cfg, &d)) return KVS_ERR_INVALID_ARG;
+  // the size limit first, so an oversized shape is refused whatever else is passed
+  if ((long long)d.U * d.nb_max > (long long)KVS_NOALLOC_MAX_SCORES) return KVS_ERR_CAPACITY;
   if (!d_score_q || !d_index_layer || !d_ctx_len || !d_sel || !d_nsel) return KVS_ERR_INVALID_ARG;
   if (nq < 1 || nq > d.max_nq) return KVS_ERR_INVALID_ARG;
-  if ((long long)d.U * d.nb_max > (long long)KVS_NOALLOC_MAX_SCORES) return KVS_ERR_INVALID_ARG;
   if (!kvs::score_supported(d)) return KVS_ERR_NOT_SUPPORTED;
   float* scores = nullptr;
   unsigned* status = nullptr;

@@ -149,15 +149,13 @@ cudaError_t launch_score_t(const Dims& d, const __nv_bfloat16* index, const __nv
   ScoreSmem sm{NP * 8, DK * 2 + 16, nwarps};
   size_t bytes = sm.bytes();
   auto kern = score_kernel<DK, NP>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)bytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   int max_tiles = (d.nb_max + 15) / 16;
   // about 2 waves of CTAs over 152 SMs, at least 4 tiles per warp
-  int ctas_per_unit = max(1, min((max_tiles + 4 * nwarps - 1) / (4 * nwarps), (2 * 152 + d.U - 1) / d.U));
+  int ctas_per_unit = max(1, min((max_tiles + 4 * nwarps - 1) / (4 * nwarps), (2 * device_sm_count() + d.U - 1) / d.U));
   int tiles_per_cta = (max_tiles + ctas_per_unit - 1) / ctas_per_unit;
   dim3 grid(ctas_per_unit, d.U);
   kern<<<grid, 32 * nwarps, bytes, s>>>(d, index, q, nq, ctx_len, scores, tiles_per_cta, err);

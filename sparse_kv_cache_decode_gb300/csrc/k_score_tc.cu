@@ -151,8 +151,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(a_st + s * kChunkBytes, &tm_idx, kc * kChunk, u * d.nb_max + ti * kTileM, &full[s]);
         }
       }
-      // no tensor load may still be writing this CTA's shared memory when it exits
-      for (int j = max(0, k - S); j < k; ++j) mbar_wait(&full[j % S], (j / S) & 1, timeout_ns);
+      // no tensor load may still be writing this CTA's shared memory when it exits (a fixed bound,
+      // independent of the caller's timeout)
+      for (int j = max(0, k - S); j < k; ++j) mbar_wait(&full[j % S], (j / S) & 1, kDrainTimeoutNs);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every product issued by this thread has finished before the tensor memory is released
       tc_commit(drained);
-      mbar_wait(drained, 0, timeout_ns);
+      mbar_wait(drained, 0, kDrainTimeoutNs);
     }
     __syncwarp();
   } else {
@@ -227,33 +228,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-int sm_count_tc() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 152;
-  }
-  return n;
-}
+int sm_count_tc() { return device_sm_count(); }
 
 }  // namespace
 
 int score_tc_supported(const Dims& d, int nq) {
   // the tensor-memory path pays off for wide contractions (many scoring rows per index row)
   if (d.dk % kChunk != 0 || nq * d.G > 256 || nq * d.G < 64) return 0;
-  TcPlan p = make_tc_plan(d, nq, 152);
+  TcPlan p = make_tc_plan(d, nq, sm_count_tc());
   return p.stages >= 2;
 }
 
 cudaError_t launch_score_tc(const Dims& d, const __nv_bfloat16* index, const __nv_bfloat16* q, int nq,
                             const int* ctx_len, float* scores, unsigned* err, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(score_tc_kernel), kMaxSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   CUtensorMap tm;
   if (!make_tmap_2d(&tm, const_cast<__nv_bfloat16*>(index), (uint64_t)d.dk, (uint64_t)d.U * d.nb_max, kChunk, kTileM))

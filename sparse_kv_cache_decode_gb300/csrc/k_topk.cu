@@ -339,15 +339,11 @@ cudaError_t launch_topk(const Dims& d, const float* scores, const int* ctx_len, 
                         cudaStream_t s, const TopkScratch* scratch) {
   const int P = scratch ? topk_chunks(d) : 0;
   if (P > 0) {
-    static bool attr2 = false;
-    if (!attr2) {
-      cudaError_t e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    {
+      cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(topk_chunk_kernel),
                                            (int)(kChunk * sizeof(uint32_t)));
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kTopkMergeSmemMax);
+      if (e == cudaSuccess) e = set_max_dynamic_smem(reinterpret_cast<const void*>(topk_merge_kernel), (int)kTopkMergeSmemMax);
       if (e != cudaSuccess) return e;
-      attr2 = true;
     }
     topk_chunk_kernel<<<dim3(P, d.U), kTopkThreads, kChunk * sizeof(uint32_t), s>>>(d, scores, ctx_len, P, scratch->key,
                                                                                   scratch->idx, scratch->cnt);
@@ -358,11 +354,9 @@ cudaError_t launch_topk(const Dims& d, const float* scores, const int* ctx_len, 
     return cudaGetLastError();
   }
   size_t smem = (size_t)kTopkSmemKeys * sizeof(uint32_t);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(topk_kernel), (int)smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   topk_kernel<<<d.U, kTopkThreads, smem, s>>>(d, scores, ctx_len, sel, nsel, err);
   return cudaGetLastError();

@@ -5,7 +5,10 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <map>
+#include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include <cudaTypedefs.h>
@@ -141,6 +144,38 @@ Plan plan_of(const Dims& d) {
 
 namespace kvs {
 bool config_to_dims(const kvs_config* c, Dims* d) { return fill_dims(c, d); }
+
+cudaError_t set_max_dynamic_smem(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> set_to;   // (kernel, device) -> bytes allowed
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_pair(kernel, dev);
+  auto it = set_to.find(key);
+  if (it != set_to.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) set_to[key] = bytes;
+  return e;
+}
+
+int device_sm_count() {
+  static std::mutex mu;
+  static std::map<int, int> count;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = count.find(dev);
+  if (it != count.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  count[dev] = n;
+  return n;
+}
 }  // namespace kvs
 
 namespace {

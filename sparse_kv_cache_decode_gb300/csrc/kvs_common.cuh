@@ -107,4 +107,11 @@ cudaError_t launch_attention_tma(const Dims& d, const Layer& L, const CUtensorMa
 int attention_split(const Dims& d, int* n_split, int* blocks_per_split);
 int score_supported(const Dims& d);
 
+// Raise `kernel`'s dynamic shared-memory limit to at least `bytes` on the current device.  The
+// attribute belongs to the current device's context, so it is tracked per (kernel, device); safe
+// to call from several host threads.
+cudaError_t set_max_dynamic_smem(const void* kernel, int bytes);
+// Streaming multiprocessors of the current device (looked up once per device).
+int device_sm_count();
+
 }  // namespace kvs

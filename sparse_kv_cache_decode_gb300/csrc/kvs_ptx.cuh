@@ -84,6 +84,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
       : "memory");
   return ok != 0;
 }
+// Bound of the wait for tensor loads still in flight after an abort, before a CTA may leave
+// (independent of the caller's wait timeout; loads that were issued complete far sooner).
+constexpr uint64_t kDrainTimeoutNs = 500ull * 1000ull * 1000ull;
+
 // Wait for the phase with the given parity to complete; gives up after timeout_ns of
 // %globaltimer time and returns false (the caller reports KVS_ERR_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, uint64_t timeout_ns) {

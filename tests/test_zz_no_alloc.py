@@ -1,7 +1,7 @@
 """kvs_select_blocks_noalloc: the block-selection entry point for callers that cannot allocate
-device memory (for example code running inside an allocator hook or a host callback, or a
-plug-in whose process budgets all device memory elsewhere).  It keeps its block scores in a
-fixed device array inside the library instead of a caller workspace.
+device memory (for example code running inside an allocator hook, or a plug-in whose process
+budgets all device memory elsewhere).  It keeps its block scores in a fixed device array inside
+the library instead of a caller workspace.
 
 Checked through the C ABI against the existing entry points (kvs_score_blocks followed by
 kvs_topk_select) on the same inputs, on two calls in a row with different queries, so the
@@ -20,6 +20,10 @@ torch = pytest.importorskip("torch")
 @pytest.mark.parametrize("w,lens", [
     (W.TINY.with_(name="noalloc_tiny", n_req=3), [4096, 1000, 17]),
     (W.TINY_LOOKAHEAD.with_(name="noalloc_drafts", n_req=2), [4096, 2222]),
+    # token-level MLA shape above 16384 blocks: tensor-core scoring, and a single-pass top-K over
+    # global memory here against the two-phase top-K of the context path
+    (W.MLA_128K.with_(name="noalloc_mla_64k", n_req=2, n_layer=1, ctx0=65536, layer_prefetch=False),
+     [65536, 65536 - 123]),
 ])
 def test_noalloc_selection_matches_existing_entry_points(w, lens):
     import sparse_kv_cache_decode_gb300 as K
@@ -50,10 +54,11 @@ def test_noalloc_selection_matches_existing_entry_points(w, lens):
 
 
 def test_noalloc_rejects_oversized_shapes():
+    """The size limit is checked before anything else: with every device pointer NULL the call
+    still answers KVS_ERR_CAPACITY (no kernel can be launched on a refused shape)."""
     import sparse_kv_cache_decode_gb300 as K
     w = W.MLA_128K.with_(n_req=32)            # 32 x 131072 block scores > the array's 2^21
     cfg = K.make_config(w)
-    dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
     with pytest.raises(K.KvsError) as e:
-        K.select_blocks_noalloc(cfg, dummy, 1, dummy, dummy, dummy, dummy)
-    assert e.value.status == 1
+        K.select_blocks_noalloc(cfg, None, 1, None, None, None, None)
+    assert e.value.status == 3
