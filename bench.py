@@ -3,8 +3,8 @@
 
 Workload (default): Llama-3.1-8B-shaped attention, 32 layers, 32 q / 8 kv heads, d = 128, batch 8,
 context 32768, block 16, budget 2048 tokens (128 blocks, 1 sink + 2 recent), cache cap 192 blocks
-(1.5x budget), 4 lookahead draft queries per step (q_draft = q_{t+j} + N(0, 0.3^2)), full KV history
-(32 GiB) in pinned host memory.  Seeded synthetic data (workload/), no dataset.
+(1.5x budget), 4 lookahead draft queries per step (q_draft = q_{t+j} + N(0, 0.3^2) noise), full KV
+history (32 GiB) in pinned host memory.  Seeded synthetic data (workload/), no dataset.
 
 One step = every layer, in order, for every request: attention over the selection made by the
 previous step, scoring with the drafts, selection, cache update, and the host -> slot fetch on a
@@ -12,14 +12,21 @@ side stream.  The step is captured once as a CUDA graph over fixed input buffers
 step copies its own device-resident inputs into them and replays the graph.  Per-step reads
 (about 3 GiB) exceed the 129 MB L2, so no flush is needed between steps.
 
+The default run also measures the other workloads, each in a child process of its own (its
+history is freed when it ends): the 128K host-resident case with a per-step append, the MLA
+token-level case with cross-layer prefetch, and a reduced budget/eviction sweep (one process,
+one shared history); their lines go under `per_config`.
+
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a bounded sample of the
 same workload on the host cores.
 """
 import argparse
+import hashlib
 import json
 import os
+import re
 import resource
 import statistics
 import subprocess
@@ -37,18 +44,27 @@ import workload as W  # noqa: E402
 METRIC = "sparse decode steps/s (effective KV GB/s and HBM/host-link roofline alongside)"
 UNIT = "steps/s"
 
+# Workloads measured beside the headline by the default run (child processes).
+PER_CONFIG = ["llama8b_128k_append", "mla_128k_token_topk"]
+# Reduced budget/eviction sweep: block size x budget tokens x target step overlap (%).
+SWEEP_POINTS = [f"sweep_bs{bs}_b{b}_ov{ov}" for bs in (16, 64) for b in (512, 2048, 4096) for ov in (50, 80, 95)]
 
-def parse():
+
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama8b_32k_lookahead")
+    ap.add_argument("--workload", default="llama8b_32k_lookahead",
+                    help="a named workload, or 'sweep' (with --sweep-points) for several sweep cases on one history")
+    ap.add_argument("--sweep-points", default=",".join(SWEEP_POINTS))
     ap.add_argument("--timed-kernel", default="auto", choices=["auto", "attn", "score", "fetch"],
                     help="kernel of the roofline object (auto: the one with the most time per step)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="measure the selected workload only")
+    ap.add_argument("--child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--threads", type=int, default=0, help="generator threads (0: all cores)")
     ap.add_argument("--serial", action="store_true", help="fetch on the compute stream (kernels run one at a time)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (smaller profiling cases)")
@@ -56,7 +72,10 @@ def parse():
     ap.add_argument("--no-io", action="store_true",
                     help="control run: every step replays the first step's inputs, so the selection repeats, every "
                          "selected block is resident and the timed steps fetch nothing over the host link")
-    return ap.parse_args()
+    ap.add_argument("--link-peak-only", action="store_true",
+                    help="measure the host link (copy engine and SM zero-copy reads) on the workload's history and "
+                         "print the figures")
+    return ap.parse_args(argv)
 
 
 def log(*a):
@@ -184,23 +203,78 @@ def measured_peaks():
     return 6800.0, "fallback (6.8 TB/s)"
 
 
-def host_link_peak_gbs():
-    """Host -> device copy of 1 GiB of pinned memory (copy engine), best of 3: the measured link."""
+def _time_ms(fn, reps=3):
+    import torch
+    best = None
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    return best
+
+
+def link_peaks(K, host_tensors):
+    """The host link measured three ways; the largest is the link peak of the step roofline.
+      ce_pinned   copy engine, 1 GiB of cudaHostAlloc memory -> device
+      ce_history  copy engine, 1 GiB of the bound history (the memory the fetch reads) -> device
+      sm_seq      SM zero-copy reads of consecutive 8 KiB items of that 1 GiB (kvs_probe_host_read)
+      sm_rand     SM zero-copy reads of 8 KiB items at random 8 KiB-aligned places in the whole history
+    The SM probes take the best of a few grid shapes."""
     import torch
     n = 1 << 30
+    out = {}
     h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
     h.fill_(1)
     d = torch.empty(n, dtype=torch.uint8, device="cuda")
-    best = 0.0
-    for _ in range(4):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        d.copy_(h, non_blocking=True)
-        b.record()
-        b.synchronize()
-        best = max(best, n / (a.elapsed_time(b) * 1e-3) / 1e9)
-    del h, d
-    return best
+    out["ce_pinned"] = n / (_time_ms(lambda: d.copy_(h, non_blocking=True)) * 1e-3) / 1e9
+    del h
+    hist = host_tensors[0]
+    flat = hist.view(-1).view(torch.uint8)
+    region = flat.numel()
+    if region >= n:
+        src = flat[:n]
+        out["ce_history"] = n / (_time_ms(lambda: d.copy_(src, non_blocking=True)) * 1e-3) / 1e9
+    del d
+    item = 8192
+    sink = torch.zeros(2, dtype=torch.int32, device="cuda")
+    seq = torch.arange(0, min(n, region) // item, dtype=torch.int64, device="cuda") * item
+    rng = np.random.default_rng(12345)
+    rnd = torch.from_numpy(rng.integers(0, region // item, size=65536, dtype=np.int64) * item).cuda()
+    for name, offs in (("sm_seq", seq), ("sm_rand", rnd)):
+        best, shape = 0.0, None
+        for ctas, threads in ((152, 256), (304, 256), (608, 128), (1216, 128)):
+            ms = _time_ms(lambda: K.probe_host_read(hist, region, offs, item, ctas, threads, sink))
+            gbs = offs.numel() * item / (ms * 1e-3) / 1e9
+            if gbs > best:
+                best, shape = gbs, f"{ctas}x{threads}"
+        out[name] = best
+        out[name + "_grid"] = shape
+    torch.cuda.synchronize()
+    if int(sink[1].item()) != 0:
+        raise RuntimeError("link probe skipped items")
+    vals = {k: v for k, v in out.items() if not k.endswith("_grid")}
+    best_key = max(vals, key=vals.get)
+    res = {k: (round(v, 1) if isinstance(v, float) else v) for k, v in out.items()}
+    res["peak_gbs"] = round(vals[best_key], 1)
+    res["peak_source"] = f"{best_key} (largest of the measurements in this run; profiles/host_link_peak.md)"
+    res["history_bytes"] = int(region)
+    return res
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        fields = dict(ln.split(":", 1) for ln in out.splitlines() if ":" in ln)
+        name = fields.get("Model name", "").strip()
+        vendor = fields.get("Vendor ID", "").strip()
+        arch = fields.get("Architecture", "").strip()
+        return " ".join(x for x in (vendor, name, f"({arch})" if arch else "") if x) or "unknown"
+    except (OSError, subprocess.SubprocessError, ValueError):
+        return "unknown"
 
 
 # ----------------------------------------------------------------------------- algorithmic bytes
@@ -221,6 +295,53 @@ def algorithmic_bytes(w, lens, link_bytes_per_step):
     per_layer = {"index": idx_b, "attn": attn_b + w.n_req * w.n_q_head * w.d_k * 2 + out_b}
     hbm = w.n_layer * (idx_b + attn_b + q_b + out_b) + link_bytes_per_step   # fetched rows are written to HBM
     return hbm, link_bytes_per_step, per_layer
+
+
+def dependency_bound_ms(w, per_layer, link_per_layer, hbm_peak, link_peak):
+    """Sync-mode bound under the layer dependency: per layer the index scan, then the larger of
+    the attention reads and the layer's own fetch, summed over layers (ms)."""
+    t = 0.0
+    for lb in link_per_layer:
+        t_ik = per_layer["index"] / (hbm_peak * 1e9)
+        t_attn = per_layer["attn"] / (hbm_peak * 1e9)
+        t_fetch = lb / (link_peak * 1e9)
+        t += t_ik + max(t_attn, t_fetch)
+    return t * 1e3
+
+
+# ----------------------------------------------------------------------------- ncu traffic
+
+KERNEL_SOURCES = {"attn": ["k_attn_tma.cu", "k_attn.cu"], "score": ["k_score.cu", "k_score_tc.cu"],
+                  "fetch": ["k_cache.cu"]}
+
+
+def source_sha(kname) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(kname, []):
+        with open(os.path.join(ROOT, "sparse_kv_cache_decode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kname, workload):
+    """DRAM bytes (read + write) per launch of a kernel on a workload, from a committed ncu summary
+    under profiles/ that records them for the current kernel source (a `traffic` block naming the
+    kernel, the workload, the sources' sha256 prefix and the bytes per full launch); None when no
+    summary matches or the kernel changed since the counters were taken."""
+    pdir = os.path.join(ROOT, "profiles")
+    want = source_sha(kname)
+    for f in sorted(os.listdir(pdir)):
+        if not f.endswith(".md"):
+            continue
+        with open(os.path.join(pdir, f)) as fh:
+            text = fh.read()
+        for block in re.findall(r"```traffic\n(.*?)```", text, flags=re.S):
+            kv = dict(ln.split(":", 1) for ln in block.strip().splitlines() if ":" in ln)
+            kv = {k.strip(): v.strip() for k, v in kv.items()}
+            if kv.get("kernel") == kname and kv.get("workload") == workload and kv.get("source_sha") == want:
+                return {"bytes": int(kv["dram_bytes_per_launch"]), "profile": f"profiles/{f}",
+                        "note": kv.get("note", "")}
+    return None
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -294,7 +415,8 @@ def run_reference(args, dist):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": full_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(w),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "cpu": cpu_model(), "kind": "oracle",
+                             "sample": desc},
             "dense_softmax_coverage": coverage,
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -306,8 +428,9 @@ def config_of(w):
             "kv_heads": w.n_kv_head, "d_k": w.d_k, "d_v": w.d_v, "context": w.ctx0, "block": w.block_size,
             "budget_tokens": w.budget_blocks * w.block_size, "cache_blocks_per_head": w.cap_blocks,
             "lookahead_drafts": w.n_draft if w.lookahead else 0, "append": w.append,
-            "layer_prefetch": w.layer_prefetch, "host_kv_gib": round(w.host_kv_bytes / 2**30, 2),
-            "l2": "no flush: each step reads > 3 GiB, far above the 129 MB L2",
+            "layer_prefetch": w.layer_prefetch, "rho": w.rho, "draft_rho": w.draft_rho,
+            "host_kv_gib": round(w.host_kv_bytes / 2**30, 2),
+            "l2": "no flush: each step reads > 1 GiB, far above the 129 MB L2",
             "parallelism": "one replica per GPU (requests are independent)"}
 
 
@@ -339,61 +462,108 @@ def check_host_memory(history_bytes: int):
                            f"{need / 2**30:.1f} GiB, {avail / 2**30:.1f} GiB available")
 
 
+def selection_overlap(prev_sel, prev_n, sel, n):
+    """Mean over units of |S_t & S_t-1| / |S_t| (host arrays [..., K_b] and counts [...])."""
+    a = prev_sel.reshape(-1, prev_sel.shape[-1])
+    b = sel.reshape(-1, sel.shape[-1])
+    na, nb = prev_n.reshape(-1), n.reshape(-1)
+    vals = []
+    for i in range(b.shape[0]):
+        if nb[i] <= 0:
+            continue
+        vals.append(len(np.intersect1d(a[i, :na[i]], b[i, :nb[i]])) / nb[i])
+    return vals
+
+
 # ----------------------------------------------------------------------------- our path
 
-def run_ours(args, dist):
-    import torch
-    import sparse_kv_cache_decode_gb300 as K
-    from sparse_kv_cache_decode_gb300 import build as kbuild
+class History:
+    """The page-locked host history of a workload (huge pages when the kernel gives them)."""
 
-    kbuild.build()
-    torch.cuda.set_device(dist.local)
-    w = W.get(args.workload)
-    if args.layers:
-        w = w.with_(n_layer=args.layers)
-    if args.batch:
-        w = w.with_(n_req=args.batch)
-    if args.no_io:
-        w = w.with_(name=w.name + "_no_io")
-        args.no_e2e = True          # the end-to-end pass streams fresh inputs, which would miss
-    if dist.world > 1:
-        w = w.with_(seed=w.seed + dist.rank)       # each GPU serves its own batch of requests
+    def __init__(self, K, w, threads):
+        import torch
+        NL, B, Hkv = w.n_layer, w.n_req, w.n_kv_head
+        check_host_memory(w.host_kv_bytes)
+        t0 = time.time()
+        self.K = K
+        if w.v_shares_k:
+            self.k, self.k_keep, self.desc = K.pinned_host_history((NL, B, Hkv, w.max_ctx, w.d_k),
+                                                                   lambda t: W.fill_kv(w, t, None, threads))
+            self.v, self.v_keep = None, None
+        else:
+            k_arr = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_k))
+            v_arr = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_v))
+            W.fill_kv(w, k_arr.tensor, v_arr.tensor, threads)
+            fk, fv = k_arr.huge_fraction(), v_arr.huge_fraction()
+            if min(fk, fv) >= 0.95:
+                k_arr.register()
+                v_arr.register()
+                self.k, self.v, self.k_keep, self.v_keep = k_arr.tensor, v_arr.tensor, k_arr, v_arr
+                self.desc = f"mmap + transparent huge pages ({min(fk, fv):.0%}) + cudaHostRegister"
+            else:
+                self.k = torch.empty(k_arr.tensor.shape, dtype=torch.int16, pin_memory=True)
+                self.v = torch.empty(v_arr.tensor.shape, dtype=torch.int16, pin_memory=True)
+                self.k.copy_(k_arr.tensor)
+                self.v.copy_(v_arr.tensor)
+                del k_arr, v_arr
+                self.k_keep = self.v_keep = None
+                self.desc = f"cudaHostAlloc (huge pages covered only {min(fk, fv):.0%})"
+        log(f"host memory: {self.desc}; {w.host_kv_bytes / 2**30:.1f} GiB generated in {time.time() - t0:.1f}s")
+
+    def huge_arrays(self):
+        return [a for a in (self.k_keep, self.v_keep) if isinstance(a, self.K.HostArray)]
+
+    def repair_after_first_step(self, ctx):
+        """On some hosts the first scattered device reads of the mapped history split part of its
+        transparent huge pages; the device then translates 64 KiB pages on every later fetch into
+        them, and fetches slow down many times over.  Collapse the pages again (or, failing that,
+        move the history to driver-pinned memory) and bind again, before any graph captures the
+        host pointers."""
+        import torch
+        arrays = self.huge_arrays()
+        if not arrays:
+            return
+        left = min(a.huge_fraction() for a in arrays)
+        if left >= 0.999:
+            return
+        again = min(a.recollapse() for a in arrays)
+        log(f"host memory: the first step split huge pages ({left:.1%} left); collapsed again: {again:.1%}")
+        if again >= 0.999:
+            ctx.bind_host_kv(self.k, self.v)
+            self.desc += f" (huge pages split by the first step, {left:.0%} left, collapsed again)"
+            return
+        k_new = torch.empty(self.k.shape, dtype=torch.int16, pin_memory=True)
+        k_new.copy_(self.k)
+        v_new = None
+        if self.v is not None:
+            v_new = torch.empty(self.v.shape, dtype=torch.int16, pin_memory=True)
+            v_new.copy_(self.v)
+        ctx.bind_host_kv(k_new, v_new)
+        for a in arrays:
+            a.close()
+        self.k, self.v, self.k_keep, self.v_keep = k_new, v_new, None, None
+        self.desc = f"cudaHostAlloc (the first step split huge pages of the mapped history: {again:.0%} left)"
+        log(f"host memory: {self.desc}")
+
+    def huge_after(self):
+        arrays = self.huge_arrays()
+        return [round(a.huge_fraction(), 4) for a in arrays] if arrays else None
+
+    def close(self):
+        for a in self.huge_arrays():
+            a.close()
+        self.k = self.v = self.k_keep = self.v_keep = None
+
+
+def run_point(args, dist, w, hist, link, e2e: bool, cpu_baseline: bool):
+    """Measure one workload on a bound history; returns its JSON line (a dict)."""
+    import torch
+    K = hist.K
     B, NL, Hkv = w.n_req, w.n_layer, w.n_kv_head
     T = args.warmup + args.steps
-    T_e2e = 0 if args.no_e2e else args.steps
-    if w.append:   # history capacity for every appended token of the run (timed, measured, e2e)
-        w = w.with_(steps=max(w.steps, T + 8 + T_e2e + 1))
-    t0 = time.time()
-    check_host_memory(w.host_kv_bytes)
-    # K and V histories; each filled by the generator (which draws both in one pass), so fill into
-    # a staging pair when V exists
-    if w.v_shares_k:
-        k_host, k_keep, host_desc = K.pinned_host_history((NL, B, Hkv, w.max_ctx, w.d_k),
-                                                          lambda t: W.fill_kv(w, t, None, args.threads))
-        v_host, v_keep = None, None
-    else:
-        k_arr = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_k))
-        v_arr = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_v))
-        W.fill_kv(w, k_arr.tensor, v_arr.tensor, args.threads)
-        fk, fv = k_arr.huge_fraction(), v_arr.huge_fraction()
-        if min(fk, fv) >= 0.95:
-            k_arr.register()
-            v_arr.register()
-            k_host, v_host, k_keep, v_keep = k_arr.tensor, v_arr.tensor, k_arr, v_arr
-            host_desc = f"mmap + transparent huge pages ({min(fk, fv):.0%}) + cudaHostRegister"
-        else:
-            k_host = torch.empty(k_arr.tensor.shape, dtype=torch.int16, pin_memory=True)
-            v_host = torch.empty(v_arr.tensor.shape, dtype=torch.int16, pin_memory=True)
-            k_host.copy_(k_arr.tensor)
-            v_host.copy_(v_arr.tensor)
-            del k_arr, v_arr
-            k_keep = v_keep = None
-            host_desc = f"cudaHostAlloc (huge pages covered only {min(fk, fv):.0%})"
-    log(f"host memory: {host_desc}")
-    log(f"host KV {w.host_kv_bytes / 2**30:.1f} GiB generated in {time.time() - t0:.1f}s")
-
+    T_e2e = args.steps if e2e else 0
     ctx = K.Context(K.make_config(w))
-    ctx.bind_host_kv(k_host, v_host)
+    ctx.bind_host_kv(hist.k, hist.v)
     lens = [w.ctx0] * B
     ctx_len = torch.tensor(lens, dtype=torch.int32, device="cuda")
     index = torch.zeros((NL, B, Hkv, w.max_blocks, w.d_k), dtype=torch.int16, device="cuda")
@@ -405,10 +575,12 @@ def run_ours(args, dist):
     t0 = time.time()
     qs = W.QueryStream(w)
     nq = w.n_score_q
-    q_all = torch.empty((T + T_e2e, NL, B, w.n_q_head, w.d_k), dtype=torch.int16)
-    d_all = torch.empty((T + T_e2e, NL, B, w.n_draft, w.n_q_head, w.d_k), dtype=torch.int16) if w.lookahead else None
+    n_meas = max(2, min(args.steps, 8))
+    T_all = T + n_meas + T_e2e
+    q_all = torch.empty((T_all, NL, B, w.n_q_head, w.d_k), dtype=torch.int16)
+    d_all = torch.empty((T_all, NL, B, w.n_draft, w.n_q_head, w.d_k), dtype=torch.int16) if w.lookahead else None
     tok_all = []
-    for t in range(T + T_e2e):
+    for t in range(T_all):
         q_all[t] = torch.from_numpy(qs.queries(t).view(np.int16))
         if d_all is not None:
             d_all[t] = torch.from_numpy(qs.drafts(t).view(np.int16))
@@ -416,10 +588,11 @@ def run_ours(args, dist):
             nk, nv = W.token(w, w.ctx0 + t)
             tok_all.append((torch.from_numpy(nk.view(np.int16)),
                             None if nv is None else torch.from_numpy(nv.view(np.int16))))
-    log(f"queries for {T + T_e2e} steps generated in {time.time() - t0:.1f}s")
-    q_dev = q_all[:T].cuda()
-    d_dev = d_all[:T].cuda() if d_all is not None else None
-    tok_dev = [(a.cuda(), None if b is None else b.cuda()) for a, b in tok_all[:T]]
+    log(f"{w.name}: queries for {T_all} steps generated in {time.time() - t0:.1f}s")
+    T_dev = T + n_meas
+    q_dev = q_all[:T_dev].cuda()
+    d_dev = d_all[:T_dev].cuda() if d_all is not None else None
+    tok_dev = [(a.cuda(), None if b is None else b.cuda()) for a, b in tok_all[:T_dev]]
 
     out = torch.zeros((NL, B, w.n_q_head, w.d_v), dtype=torch.float32, device="cuda")
     sel = torch.zeros((NL, B, Hkv, w.budget_blocks), dtype=torch.int32, device="cuda")
@@ -428,54 +601,18 @@ def run_ours(args, dist):
     s = torch.cuda.Stream()
     cs = torch.cuda.Stream(priority=-1)   # fetch CTAs are scheduled ahead of compute CTAs
 
-    def step(qt, dt, tok):
+    def step(qt, dt, tok, serial=False):
         if w.append:
             ctx.advance_ctx(ctx_len)
         for l in range(NL):
             if w.layer_prefetch and l > 0:
-                ctx.layer_prefetch(l, sel[l - 1], nsel[l - 1], ctx_len, stats, stream=s if args.serial else cs)
+                ctx.layer_prefetch(l, sel[l - 1], nsel[l - 1], ctx_len, stats, stream=s if serial else cs)
             ctx.decode_step(l, qt[l], None if dt is None else dt[l], nq if dt is not None else 1, index, ctx_len,
                             out[l], stats, None if tok is None else tok[0][l],
                             None if tok is None or tok[1] is None else tok[1][l], sel[l], nsel[l], stream=s,
-                            copy_stream=None if args.serial else cs)
+                            copy_stream=None if serial else cs)
         ctx.join(s)
 
-    # Step 0 eagerly (bootstraps the lookahead selections).  Then one graph over fixed input
-    # buffers; each step copies its device-resident inputs into them (inside the timed region)
-    # and replays the graph.
-    torch.cuda.synchronize()
-    with torch.cuda.stream(s):
-        step(q_dev[0], None if d_dev is None else d_dev[0], tok_dev[0] if w.append else None)
-    s.synchronize()
-    # On some hosts the first scattered device reads of the mapped history split part of its
-    # transparent huge pages; the device then translates 64 KiB pages on every later fetch into
-    # them, and fetches slow down many times over.  Move the history to driver-pinned memory
-    # when that happened, before the graph captures the host pointers.
-    huge_arrays = [a for a in (k_keep, v_keep) if isinstance(a, K.HostArray)]
-    if huge_arrays:
-        left = min(a.huge_fraction() for a in huge_arrays)
-        if left < 0.999:
-            # first remap the same pages with huge pages (MADV_COLLAPSE) and bind them again
-            again = min(a.recollapse() for a in huge_arrays)
-            log(f"host memory: the first step split huge pages ({left:.1%} left); collapsed again: {again:.1%}")
-            if again >= 0.999:
-                ctx.bind_host_kv(k_host, v_host)
-                host_desc += f" (huge pages split by the first step, {left:.0%} left, collapsed again)"
-                left = again
-        if left < 0.999:
-            k_new = torch.empty(k_host.shape, dtype=torch.int16, pin_memory=True)
-            k_new.copy_(k_host)
-            v_new = None
-            if v_host is not None:
-                v_new = torch.empty(v_host.shape, dtype=torch.int16, pin_memory=True)
-                v_new.copy_(v_host)
-            ctx.bind_host_kv(k_new, v_new)
-            for a in huge_arrays:
-                a.close()
-            k_host, v_host, k_keep, v_keep = k_new, v_new, None, None
-            host_desc = (f"cudaHostAlloc (the first step split huge pages of the mapped history: "
-                         f"{left:.0%} left)")
-            log(f"host memory: {host_desc}")
     q_fix = torch.empty_like(q_dev[0])
     d_fix = torch.empty_like(d_dev[0]) if d_dev is not None else None
     tok_fix = None
@@ -494,14 +631,23 @@ def run_ours(args, dist):
             if tok_fix[1] is not None:
                 tok_fix[1].copy_(tok_dev[t][1], non_blocking=True)
 
-    def capture(qt, dt, tok):
+    def capture(serial=False):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
-            step(qt, dt, tok)
+            step(q_fix, d_fix, tok_fix, serial)
         return g
 
+    # Step 0 eagerly (bootstraps the lookahead selections).  Then one graph over fixed input
+    # buffers; each step copies its device-resident inputs into them (inside the timed region)
+    # and replays the graph.
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        stage_inputs(0)
+        step(q_fix, d_fix, tok_fix, args.serial)
+    s.synchronize()
+    hist.repair_after_first_step(ctx)
     launches0 = ctx.launch_count()
-    graph = capture(q_fix, d_fix, tok_fix)
+    graph = capture(args.serial)
     launches_per_step = ctx.launch_count() - launches0
     upload_graphs([graph], s)
     with torch.cuda.stream(s):
@@ -512,7 +658,6 @@ def run_ours(args, dist):
     stats0 = stats.cpu().numpy().copy()
 
     hbm_peak, hbm_src = measured_peaks()
-    link_peak = host_link_peak_gbs()
     clocks = ClockSampler(dist.local)
     clocks.start()
     time.sleep(0.3)
@@ -528,52 +673,60 @@ def run_ours(args, dist):
     torch.cuda.synchronize()
     dist.barrier()
     elapsed = ev0.elapsed_time(ev1) * 1e-3
-    huge_after = ([round(a.huge_fraction(), 4) for a in (k_keep, v_keep) if isinstance(a, K.HostArray)]
-                  if isinstance(k_keep, K.HostArray) else None)
+    huge_after = hist.huge_after()
     clk = clocks.stop()
     elapsed = dist.max(elapsed)
     stats1 = stats.cpu().numpy()
     dstat = (stats1 - stats0).sum(axis=0)
+    link_layers = (stats1 - stats0)[:, 6] / args.steps        # per layer, bytes fetched per step
     launches = launches_per_step * args.steps
     dev_status = ctx.poll_error()
     if dev_status != 0:
         raise RuntimeError(f"device status {K.STATUS.get(dev_status, dev_status)}")
 
-    # Kernel durations: CUDA events around every launch of each kernel, in graphs of their own
-    # (one per step, events recorded as graph nodes) run right after the timed region.  Event
-    # nodes order each kernel after the work before it, so these are the kernels' durations when
-    # they run without a concurrent fetch.
+    # Kernel durations: a measurement pass right after the timed region, with the fetch on the
+    # compute stream so that the kernels run one at a time; CUDA events around every launch of each
+    # kernel, in graphs of their own (one per step, events recorded as graph nodes).  The same pass
+    # snapshots each step's selection for the achieved step-to-step overlap.
     per_step_launches = {"attn": NL, "score": NL, "fetch": NL + (NL - 1 if w.layer_prefetch else 0),
                          "update": NL, "topk": NL}
-    n_meas = min(args.steps, 8, len(tok_all) - T if w.append else 8)
-    n_meas = max(1, n_meas)
+    if w.layer_prefetch:
+        per_step_launches["prefetch"] = NL - 1
     for kname, n in per_step_launches.items():
         ctx.kernel_timer_arm(kname, n_meas * n)
-    meas_graphs = []
-    for i in range(n_meas):
-        meas_graphs.append(capture(q_fix, d_fix, tok_fix))
+    meas_graphs = [capture(serial=True) for _ in range(n_meas)]
     upload_graphs(meas_graphs, s)
-    with torch.cuda.stream(s):
-        for i, g in enumerate(meas_graphs):
-            stage_inputs(args.warmup + i)    # the inputs of timed steps, replayed once more
+    snaps = []
+    for i, g in enumerate(meas_graphs):
+        with torch.cuda.stream(s):
+            stage_inputs(T + i)
             g.replay()
+        s.synchronize()
+        snaps.append((sel.cpu().numpy(), nsel.cpu().numpy()))
     torch.cuda.synchronize()
     kernel_times = {k: ctx.kernel_timer_read(k) for k in per_step_launches}
     for kname in per_step_launches:
         ctx.kernel_timer_arm(kname, 0)
+    if ctx.poll_error() != 0:
+        raise RuntimeError("device status set in the measurement pass")
+    ov = []
+    for (a, na), (b, nb) in zip(snaps, snaps[1:]):
+        ov += selection_overlap(a, na, b, nb)
+    achieved_overlap = round(float(np.mean(ov)), 4) if ov else None
 
     ms_per_step = elapsed / args.steps * 1e3
     value = dist.world * args.steps / elapsed
     link_per_step = float(dstat[6]) / args.steps
     hbm_step, link_step, per_layer = algorithmic_bytes(w, lens, link_per_step)
     t_step = elapsed / args.steps
+    link_peak = link["peak_gbs"]
     step_roof = max(hbm_step / (hbm_peak * 1e9), link_step / (link_peak * 1e9))
     kv_gbs = hbm_step / t_step / 1e9
     misses, hits = float(dstat[1]), float(dstat[0])
 
-    # kernel rooflines: algorithmic bytes per launch / CUDA-event duration per launch, against the
-    # kernel's own bound (HBM for scoring and attention, the host link for the fetch); `roofline`
-    # is the kernel with the most time per step
+    # kernel rooflines: algorithmic bytes per launch / CUDA-event duration per launch (kernels one at
+    # a time), against the kernel's own bound (HBM for scoring and attention, the host link for the
+    # fetch); `roofline` is the kernel with the most time per step
     def kernel_roofline(kname):
         kms, kn = kernel_times[kname]
         per_launch_ms = kms / max(1, kn)
@@ -585,23 +738,24 @@ def run_ours(args, dist):
             alg = link_per_step / max(1, per_step_launches["fetch"])
         achieved = alg / (per_launch_ms * 1e-3) / 1e9 if per_launch_ms > 0 else 0.0
         peak = link_peak if kname == "fetch" else hbm_peak
-        return {"bound": "host-link" if kname == "fetch" else "hbm", "kernel": kname,
-                "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
-                "bytes_per_launch": int(alg), "avg_launch_ms": round(per_launch_ms, 5), "launches_timed": kn,
-                "peak_source": "measured in this run (1 GiB pinned H2D copy)" if kname == "fetch" else hbm_src,
-                "timing": "CUDA events around each launch, measurement pass after the timed region"}
+        tr = profile_traffic(kname, w.name)
+        r = {"bound": "host-link" if kname == "fetch" else "hbm", "kernel": kname,
+             "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "GB/s",
+             "frac": round(achieved / peak, 4), "traffic": tr["bytes"] if tr else None,
+             "bytes_per_launch": int(alg), "avg_launch_ms": round(per_launch_ms, 5), "launches_timed": kn,
+             "peak_source": link["peak_source"] if kname == "fetch" else hbm_src,
+             "timing": "CUDA events around each launch; measurement pass after the timed region with the fetch "
+                       "on the compute stream (kernels one at a time)"}
+        if tr:
+            r["traffic_source"] = f"{tr['profile']} ({tr['note']})" if tr["note"] else tr["profile"]
+        return r
 
     rooflines = {k: kernel_roofline(k) for k in ("attn", "score", "fetch")}
     step_ms = {k: ms / max(1, n) * per_step_launches[k] for k, (ms, n) in kernel_times.items()}
     dominant = args.timed_kernel if args.timed_kernel != "auto" else max(rooflines, key=lambda k: step_ms[k])
     roofline = dict(rooflines[dominant])
-    roofline["dominant_by"] = "most CUDA-event time per step among attn, score, fetch"
-
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(args, w, ctx, ctx_len, index, out, sel, nsel, stats, s, cs, q_all, d_all, tok_all, T,
-                      step, dist)
+    roofline["dominant_by"] = "most CUDA-event time per step among attn, score, fetch (kernels one at a time)"
+    roofline["kernel_ms_per_step"] = round(step_ms[dominant], 4)
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
@@ -609,31 +763,37 @@ def run_ours(args, dist):
             "config": config_of(w),
             "effective_kv_gbs": round(kv_gbs, 1),
             "step_roofline": {"hbm_bytes": hbm_step, "link_bytes": link_step, "hbm_peak_gbs": hbm_peak,
-                              "link_peak_gbs": round(link_peak, 1), "bound_ms": round(step_roof * 1e3, 4),
+                              "link_peak_gbs": link_peak, "bound_ms": round(step_roof * 1e3, 4),
                               "frac": round(step_roof / t_step, 4),
                               "bound": "host-link" if link_step / link_peak > hbm_step / hbm_peak else "hbm"},
+            "achieved_overlap": achieved_overlap,
             "miss_fraction": round(misses / max(1.0, misses + hits), 4),
             "prefetch": prefetch_report(w, dstat, args.steps),
             "roofline": roofline, "rooflines": rooflines, "clocks": clk, "gpu_launches": int(launches),
-            "kernel_ms_per_step": {k: round(ms / max(1, n) * per_step_launches[k], 4)
-                                   for k, (ms, n) in kernel_times.items()},
-            "fetch": "inline" if args.serial else "side stream", "host_memory": host_desc, "host_huge_fraction_after_timing": huge_after,
+            "kernel_ms_per_step": {k: round(v, 4) for k, v in step_ms.items()},
+            "fetch": "inline" if args.serial else "side stream", "host_memory": hist.desc,
+            "host_huge_fraction_after_timing": huge_after,
             "launches_per_step": int(launches_per_step)}
+    if not w.lookahead:
+        dep = dependency_bound_ms(w, per_layer, link_layers, hbm_peak, link_peak)
+        line["dependency_bound"] = {"ms": round(dep, 4), "frac": round(dep / (t_step * 1e3), 4),
+                                    "what": "sum over layers of index scan + max(attention reads, that layer's "
+                                            "fetch), each at its peak: the bound under the layer dependency"}
     if e2e:
-        line["e2e"] = e2e
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        line["e2e"] = run_e2e(args, w, ctx, out, s, q_all, d_all, tok_all, T + n_meas, step, dist)
+    if dist.rank == 0 and dist.world == 1 and cpu_baseline:
         per_step, units, cores, desc, coverage = oracle_sample_time(w, 1, 3, min(w.n_layer, 8))
         full = per_step * (w.n_req * w.n_layer * w.n_kv_head) / units
-        line["cpu_baseline"] = {"value": round(1.0 / full, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": desc}
+        line["cpu_baseline"] = {"value": round(1.0 / full, 6), "unit": UNIT, "cores": cores, "cpu": cpu_model(),
+                                "kind": "oracle", "sample": desc}
         line["dense_softmax_coverage"] = coverage
-    if dist.rank == 0:
-        print(json.dumps(line), flush=True)
     ctx.close()
-    return 0
+    del index, q_dev, d_dev, tok_dev
+    torch.cuda.empty_cache()
+    return line
 
 
-def run_e2e(args, w, ctx, ctx_len, index, out, sel, nsel, stats, s, cs, q_all, d_all, tok_all, T, step, dist):
+def run_e2e(args, w, ctx, out, s, q_all, d_all, tok_all, T, step, dist):
     """The same steps through the public API with host buffers: each step copies its queries
     (and drafts) from pinned host memory into fixed device buffers, runs the step graph, and
     copies the attention output back to pinned host memory."""
@@ -652,7 +812,7 @@ def run_e2e(args, w, ctx, ctx_len, index, out, sel, nsel, stats, s, cs, q_all, d
     out_pin = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        step(q_fix, d_fix, tok_fix)
+        step(q_fix, d_fix, tok_fix, args.serial)
     upload_graphs([g], s)
     torch.cuda.synchronize()
     h2d = q_fix.numel() * 2 + (d_fix.numel() * 2 if d_fix is not None else 0)
@@ -679,6 +839,116 @@ def run_e2e(args, w, ctx, ctx_len, index, out, sel, nsel, stats, s, cs, q_all, d
     el = dist.max(e0.elapsed_time(e1) * 1e-3)
     return {"value": round(dist.world * K_steps / el, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h)}
+
+
+def workload_of(args, name, dist):
+    w = W.get(name)
+    if args.layers:
+        w = w.with_(n_layer=args.layers)
+    if args.batch:
+        w = w.with_(n_req=args.batch)
+    if args.no_io:
+        w = w.with_(name=w.name + "_no_io")
+    if dist.world > 1:
+        w = w.with_(seed=w.seed + dist.rank)       # each GPU serves its own batch of requests
+    if w.append:   # history capacity for every appended token of the run (timed, measured, e2e)
+        T = args.warmup + args.steps
+        w = w.with_(steps=max(w.steps, T + 8 + (0 if args.no_e2e else args.steps) + 1))
+    return w
+
+
+SUMMARY_KEYS = ("value", "ms_per_step", "effective_kv_gbs", "step_roofline", "dependency_bound", "achieved_overlap",
+                "miss_fraction", "prefetch", "roofline", "kernel_ms_per_step", "clocks", "gpu_launches", "host_memory")
+
+
+def run_children(args):
+    """The other workloads, one child process each (the sweep: one process over a shared history)."""
+    res = {}
+    jobs = [(name, ["--workload", name, "--steps", "20", "--warmup", "4"]) for name in PER_CONFIG]
+    jobs.append(("sweep", ["--workload", "sweep", "--steps", "10", "--warmup", "3"]))
+    for name, extra in jobs:
+        cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--child", "--no-e2e", "--no-cpu-baseline",
+               "--no-per-config"] + extra
+        t0 = time.time()
+        try:
+            r = subprocess.run(cmd, capture_output=True, text=True, timeout=900)
+        except subprocess.TimeoutExpired:
+            res[name] = {"error": "timed out after 900 s"}
+            continue
+        sys.stderr.write(r.stderr[-4000:])
+        lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+        if r.returncode != 0 or not lines:
+            tail = (r.stderr.strip().splitlines() or ["no output"])[-1]
+            res[name] = {"error": f"exit {r.returncode}: {tail[:300]}"}
+            continue
+        j = json.loads(lines[-1])
+        log(f"{name}: done in {time.time() - t0:.0f}s")
+        if name == "sweep":
+            res["sweep"] = j
+        else:
+            res[name] = {k: j[k] for k in SUMMARY_KEYS if k in j}
+            res[name]["config"] = j["config"]
+    return res
+
+
+def run_ours(args, dist):
+    import torch
+    import sparse_kv_cache_decode_gb300 as K
+    from sparse_kv_cache_decode_gb300 import build as kbuild
+
+    kbuild.build()
+    torch.cuda.set_device(dist.local)
+    if args.workload == "sweep":
+        return run_sweep(args, dist, K)
+    w = workload_of(args, args.workload, dist)
+    hist = History(K, w, args.threads)
+    link = link_peaks(K, [hist.k])
+    if args.link_peak_only:
+        if dist.rank == 0:
+            print(json.dumps({"workload": w.name, "host_memory": hist.desc, "link": link}), flush=True)
+        hist.close()
+        return 0
+    line = run_point(args, dist, w, hist, link, e2e=not args.no_e2e,
+                     cpu_baseline=not args.no_cpu_baseline and not args.child)
+    line["link_peak"] = link
+    hist.close()
+    del hist
+    torch.cuda.empty_cache()
+    if dist.rank == 0 and dist.world == 1 and not args.child and not args.no_per_config:
+        line["per_config"] = run_children(args)
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_sweep(args, dist, K):
+    """Several budget/eviction sweep cases over one history (the cases differ only in block size,
+    budget and query correlation, none of which changes the stored K/V)."""
+    import torch
+    names = [n for n in args.sweep_points.split(",") if n]
+    ws = [workload_of(args, n, dist) for n in names]
+    base = ws[0]
+    for w in ws:
+        if (w.n_layer, w.n_req, w.n_kv_head, w.max_ctx, w.d_k, w.d_v, w.seed, w.n_heavy) != \
+                (base.n_layer, base.n_req, base.n_kv_head, base.max_ctx, base.d_k, base.d_v, base.seed, base.n_heavy):
+            raise ValueError("sweep cases must share one history shape")
+    hist = History(K, base, args.threads)
+    link = link_peaks(K, [hist.k])
+    points = {}
+    for w in ws:
+        t0 = time.time()
+        try:
+            j = run_point(args, dist, w, hist, link, e2e=False, cpu_baseline=False)
+            points[w.name] = {k: j[k] for k in SUMMARY_KEYS if k in j}
+        except Exception as e:   # one refused case does not end the sweep
+            points[w.name] = {"error": str(e)[:300]}
+        log(f"{w.name}: {time.time() - t0:.0f}s")
+    line = {"metric": METRIC, "unit": UNIT, "workload": "sweep", "n_layer": base.n_layer, "batch": base.n_req,
+            "context": base.ctx0, "host_memory": hist.desc, "link_peak": link, "points": points}
+    hist.close()
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
 
 
 def main():
