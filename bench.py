@@ -72,6 +72,9 @@ def parse(argv=None):
     ap.add_argument("--no-io", action="store_true",
                     help="control run: every step replays the first step's inputs, so the selection repeats, every "
                          "selected block is resident and the timed steps fetch nothing over the host link")
+    ap.add_argument("--numa-local", action="store_true",
+                    help="give the host history an explicit memory policy (preferred node = the local CPU node), "
+                         "which keeps automatic NUMA balancing off it")
     ap.add_argument("--link-peak-only", action="store_true",
                     help="measure the host link (copy engine and SM zero-copy reads) on the workload's history and "
                          "print the figures")
@@ -480,19 +483,21 @@ def selection_overlap(prev_sel, prev_n, sel, n):
 class History:
     """The page-locked host history of a workload (huge pages when the kernel gives them)."""
 
-    def __init__(self, K, w, threads):
+    def __init__(self, K, w, threads, numa_local=False):
         import torch
         NL, B, Hkv = w.n_layer, w.n_req, w.n_kv_head
         check_host_memory(w.host_kv_bytes)
         t0 = time.time()
         self.K = K
+        self.vm0 = K.numa_vmstat()
         if w.v_shares_k:
             self.k, self.k_keep, self.desc = K.pinned_host_history((NL, B, Hkv, w.max_ctx, w.d_k),
-                                                                   lambda t: W.fill_kv(w, t, None, threads))
+                                                                   lambda t: W.fill_kv(w, t, None, threads),
+                                                                   local_node=numa_local)
             self.v, self.v_keep = None, None
         else:
-            k_arr = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_k))
-            v_arr = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_v))
+            k_arr = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_k), local_node=numa_local)
+            v_arr = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_v), local_node=numa_local)
             W.fill_kv(w, k_arr.tensor, v_arr.tensor, threads)
             fk, fv = k_arr.huge_fraction(), v_arr.huge_fraction()
             if min(fk, fv) >= 0.95:
@@ -508,7 +513,14 @@ class History:
                 del k_arr, v_arr
                 self.k_keep = self.v_keep = None
                 self.desc = f"cudaHostAlloc (huge pages covered only {min(fk, fv):.0%})"
+        if numa_local:
+            node = getattr(self.k_keep, "node", None)
+            self.desc += f"; preferred NUMA node {node}" if node is not None else "; NUMA policy not set"
         log(f"host memory: {self.desc}; {w.host_kv_bytes / 2**30:.1f} GiB generated in {time.time() - t0:.1f}s")
+
+    def vmstat_delta(self):
+        now = self.K.numa_vmstat()
+        return {k: now[k] - self.vm0.get(k, 0) for k in now if now[k] != self.vm0.get(k, 0)}
 
     def huge_arrays(self):
         return [a for a in (self.k_keep, self.v_keep) if isinstance(a, self.K.HostArray)]
@@ -524,6 +536,7 @@ class History:
         if not arrays:
             return
         left = min(a.huge_fraction() for a in arrays)
+        log(f"host memory after the first step: huge {left:.2%}; vmstat since allocation {self.vmstat_delta()}")
         if left >= 0.999:
             return
         again = min(a.recollapse() for a in arrays)
@@ -553,6 +566,19 @@ class History:
         for a in self.huge_arrays():
             a.close()
         self.k = self.v = self.k_keep = self.v_keep = None
+
+
+class LinkPeak:
+    """The link peak of a history, measured once, when first asked for (after a timed region, so
+    that the probe's scattered reads of the history never precede one)."""
+
+    def __init__(self, K, hist):
+        self.K, self.hist, self.v = K, hist, None
+
+    def get(self):
+        if self.v is None:
+            self.v = link_peaks(self.K, [self.hist.k])
+        return self.v
 
 
 def run_point(args, dist, w, hist, link, e2e: bool, cpu_baseline: bool):
@@ -714,6 +740,7 @@ def run_point(args, dist, w, hist, link, e2e: bool, cpu_baseline: bool):
         ov += selection_overlap(a, na, b, nb)
     achieved_overlap = round(float(np.mean(ov)), 4) if ov else None
 
+    link = link.get()
     ms_per_step = elapsed / args.steps * 1e3
     value = dist.world * args.steps / elapsed
     link_per_step = float(dstat[6]) / args.steps
@@ -901,16 +928,17 @@ def run_ours(args, dist):
     if args.workload == "sweep":
         return run_sweep(args, dist, K)
     w = workload_of(args, args.workload, dist)
-    hist = History(K, w, args.threads)
-    link = link_peaks(K, [hist.k])
+    hist = History(K, w, args.threads, args.numa_local)
+    link = LinkPeak(K, hist)
     if args.link_peak_only:
         if dist.rank == 0:
-            print(json.dumps({"workload": w.name, "host_memory": hist.desc, "link": link}), flush=True)
+            print(json.dumps({"workload": w.name, "host_memory": hist.desc, "link": link.get()}), flush=True)
         hist.close()
         return 0
     line = run_point(args, dist, w, hist, link, e2e=not args.no_e2e,
                      cpu_baseline=not args.no_cpu_baseline and not args.child)
-    line["link_peak"] = link
+    line["link_peak"] = link.get()
+    line["host_vmstat_delta"] = hist.vmstat_delta()
     hist.close()
     del hist
     torch.cuda.empty_cache()
@@ -932,8 +960,8 @@ def run_sweep(args, dist, K):
         if (w.n_layer, w.n_req, w.n_kv_head, w.max_ctx, w.d_k, w.d_v, w.seed, w.n_heavy) != \
                 (base.n_layer, base.n_req, base.n_kv_head, base.max_ctx, base.d_k, base.d_v, base.seed, base.n_heavy):
             raise ValueError("sweep cases must share one history shape")
-    hist = History(K, base, args.threads)
-    link = link_peaks(K, [hist.k])
+    hist = History(K, base, args.threads, args.numa_local)
+    link = LinkPeak(K, hist)
     points = {}
     for w in ws:
         t0 = time.time()
@@ -944,7 +972,8 @@ def run_sweep(args, dist, K):
             points[w.name] = {"error": str(e)[:300]}
         log(f"{w.name}: {time.time() - t0:.0f}s")
     line = {"metric": METRIC, "unit": UNIT, "workload": "sweep", "n_layer": base.n_layer, "batch": base.n_req,
-            "context": base.ctx0, "host_memory": hist.desc, "link_peak": link, "points": points}
+            "context": base.ctx0, "host_memory": hist.desc, "link_peak": link.get(), "points": points,
+            "host_vmstat_delta": hist.vmstat_delta()}
     hist.close()
     if dist.rank == 0:
         print(json.dumps(line), flush=True)

@@ -110,8 +110,9 @@ kvs_status kvs_destroy(kvs_ctx* ctx);
 /* Bind the pinned host history [HISP insight 1]: h_k, h_v in the layouts above (h_v NULL when
  * v_shares_k).  The memory must be page-locked and mapped into the device address space.  The
  * device reads one word of every 4 KiB page once (synchronously), so the translations of the
- * whole history exist before the first fetch.  Errors: KVS_ERR_HOST_MEM when the pointers are
- * not device-accessible. */
+ * whole history exist before the first fetch.  Errors: KVS_ERR_HOST_MEM when a pointer is not
+ * page-locked host memory mapped into the device address space (pageable memory is refused even
+ * where the device could reach it). */
 kvs_status kvs_bind_host_kv(kvs_ctx* ctx, void* h_k, void* h_v);
 
 /* Build the block-mean index keys of one layer from the host history (setup after prefill):
@@ -165,6 +166,11 @@ kvs_status kvs_sparse_decode_attn(kvs_ctx* ctx, int layer, const void* d_q, cons
  *   lookahead mode: [append] -> attention over the previous selection, and score(drafts) ->
  *                   select -> update with that selection pinned -> fetch on copy_stream.
  * The first lookahead step of a layer has no previous selection and runs the sync part first.
+ * Lookahead with a separate copy_stream overlaps the two halves [SPEC 1, OASIS module 2]: the
+ * selection chain (score, select, update) runs on a stream the context owns, starting once the
+ * work enqueued on `stream` before this call (the layer below's attention) has finished, beside
+ * this layer's attention on `stream`; the fetch on copy_stream waits for both.  All layers'
+ * selection chains run on that one stream, in call order.
  * k_new / v_new NULL: no append (else as kvs_append, after kvs_advance_ctx).  d_score_q NULL
  * scores with d_q (nq = 1).  copy_stream NULL or == stream: the fetch runs on stream.  With a
  * separate copy_stream the caller calls kvs_join before reusing the layer or ending a capture.

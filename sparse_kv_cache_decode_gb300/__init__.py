@@ -242,6 +242,51 @@ class Context:
         return st.value
 
 
+_MBIND_NR = {"aarch64": 235, "x86_64": 237}
+
+
+def bind_local_node(addr: int, length: int):
+    """Give [addr, addr + length) an explicit memory policy of this process: preferred node = the
+    NUMA node of the CPU the caller runs on (mbind, MPOL_PREFERRED).  A range with an explicit
+    policy is left alone by automatic NUMA balancing, which otherwise samples it with hinting
+    faults.  Only this process's mapping changes.  Returns the node, or None when the call is not
+    available."""
+    import os
+    import platform
+    nr = _MBIND_NR.get(platform.machine())
+    if nr is None:
+        return None
+    try:
+        cpu = min(os.sched_getaffinity(0))
+        nodes = [d for d in os.listdir(f"/sys/devices/system/cpu/cpu{cpu}") if d.startswith("node") and d[4:].isdigit()]
+        node = int(nodes[0][4:]) if nodes else 0
+    except OSError:
+        return None
+    mask = (ctypes.c_ulong * 16)()
+    mask[node // 64] = 1 << (node % 64)
+    libc = ctypes.CDLL(None, use_errno=True)
+    libc.syscall.restype = ctypes.c_long
+    rc = libc.syscall(ctypes.c_long(nr), ctypes.c_void_p(addr), ctypes.c_ulong(length), ctypes.c_int(1),  # MPOL_PREFERRED
+                      mask, ctypes.c_ulong(16 * 64), ctypes.c_uint(0))
+    return node if rc == 0 else None
+
+
+def numa_vmstat() -> dict:
+    """Counters of /proc/vmstat about huge-page splits and NUMA balancing (diagnostics)."""
+    keys = ("thp_split_pmd", "thp_split_page", "numa_hint_faults", "numa_pages_migrated", "numa_pte_updates",
+            "thp_migration_success", "thp_migration_fail", "thp_migration_split", "pgmigrate_fail")
+    out = {}
+    try:
+        with open("/proc/vmstat") as f:
+            for ln in f:
+                k, v = ln.split()
+                if k in keys:
+                    out[k] = int(v)
+    except OSError:
+        pass
+    return out
+
+
 class HostArray:
     """Page-locked, device-mapped host memory for the KV history, backed by transparent huge
     pages: an anonymous mmap aligned to 512 MiB and advised MADV_HUGEPAGE, then registered with
@@ -250,7 +295,7 @@ class HostArray:
 
     HUGE_ALIGN = 1 << 29
 
-    def __init__(self, shape, dtype=None, huge: bool = True):
+    def __init__(self, shape, dtype=None, huge: bool = True, local_node: bool = False):
         import mmap
         import torch
         dtype = dtype or torch.int16
@@ -259,8 +304,10 @@ class HostArray:
         self._mm = mmap.mmap(-1, self.nbytes + align, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
         base = ctypes.addressof(ctypes.c_char.from_buffer(self._mm))
         off = (-base) % align
+        length = (self.nbytes + mmap.PAGESIZE - 1) // mmap.PAGESIZE * mmap.PAGESIZE
         if huge and hasattr(mmap, "MADV_HUGEPAGE"):
-            self._mm.madvise(mmap.MADV_HUGEPAGE, off, (self.nbytes + mmap.PAGESIZE - 1) // mmap.PAGESIZE * mmap.PAGESIZE)
+            self._mm.madvise(mmap.MADV_HUGEPAGE, off, length)
+        self.node = bind_local_node(base + off, length) if local_node else None
         self.tensor = torch.frombuffer(self._mm, dtype=torch.uint8, count=self.nbytes, offset=off).view(dtype).view(
             *shape)
         self._registered = False
@@ -327,14 +374,14 @@ class HostArray:
             pass
 
 
-def pinned_host_history(shape, fill, min_huge: float = 0.95):
+def pinned_host_history(shape, fill, min_huge: float = 0.95, local_node: bool = False):
     """Host history of the given shape, filled by fill(tensor) and page-locked for the device.
 
     Prefers a HostArray on transparent huge pages (fewest GPU translation misses on scattered
     block fetches); when the kernel could not back it with huge pages, falls back to
     cudaHostAlloc memory (torch pin_memory).  Returns (tensor, keepalive, description)."""
     import torch
-    arr = HostArray(shape)
+    arr = HostArray(shape, local_node=local_node)
     fill(arr.tensor)
     frac = arr.huge_fraction()
     if frac >= min_huge:

@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(AttnCfg<DK, MT, VSHARE>::NW * 32)
     attn_kernel(Dims d, Layer L, const __nv_bfloat16* __restrict__ q, const int* __restrict__ sel,
                 const int* __restrict__ slot_of_sel, const int* __restrict__ nsel, const int* __restrict__ ctx_len,
                 float* __restrict__ out, int n_split, int blocks_per_split) {
+  kvs_pdl_entry();
   using Cfg = AttnCfg<DK, MT, VSHARE>;
   constexpr int NW = Cfg::NW, KRS = Cfg::KRS, VRS = Cfg::VRS;
   constexpr int KSTEPS = DK / 16;
@@ -360,6 +361,7 @@ __global__ void __launch_bounds__(mla::NW * 32, 2)
     attn_mla_kernel(Dims d, Layer L, const __nv_bfloat16* __restrict__ q, const int* __restrict__ sel,
                     const int* __restrict__ slot_of_sel, const int* __restrict__ nsel,
                     const int* __restrict__ ctx_len, float* __restrict__ out, int n_split, int blocks_per_split) {
+  kvs_pdl_entry();
   using namespace mla;
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned char* qs = smem;
@@ -567,6 +569,7 @@ __global__ void __launch_bounds__(mla::NW * 32, 2)
 
 // out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s over the splits of a (unit, q head).
 __global__ void __launch_bounds__(128) attn_combine_kernel(Dims d, Layer L, float* __restrict__ out, int n_split) {
+  kvs_pdl_entry();
   const int u = blockIdx.x, g = blockIdx.y;
   const int r = u / d.Hkv, h = u % d.Hkv;
   const float* pml = L.attn_ml + ((size_t)u * n_split * d.G) * 2;
@@ -604,10 +607,10 @@ cudaError_t launch_attn_t(const Dims& d, const Layer& L, const __nv_bfloat16* q,
   int n_split, bps;
   if (!attention_split(d, &n_split, &bps)) return cudaErrorInvalidValue;
   dim3 grid(n_split, d.U, nz);
-  kern<<<grid, Cfg::NW * 32, Cfg::SMEM, s>>>(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, n_split, bps);
+  launch_pdl(kern, dim3(grid), dim3(Cfg::NW * 32), Cfg::SMEM, s, d, L, q, sel, slot_of_sel, nsel, ctx_len, out, n_split, bps);
   e = cudaGetLastError();
   if (e != cudaSuccess || n_split == 1) return e;
-  attn_combine_kernel<<<dim3(d.U, d.G), 128, 0, s>>>(d, L, out, n_split);
+  launch_pdl(attn_combine_kernel, dim3(dim3(d.U, d.G)), dim3(128), 0, s, d, L, out, n_split);
   return cudaGetLastError();
 }
 
@@ -620,10 +623,10 @@ cudaError_t launch_attn_mla(const Dims& d, const Layer& L, const __nv_bfloat16* 
   int n_split, bps;
   if (!attention_split(d, &n_split, &bps)) return cudaErrorInvalidValue;
   dim3 grid(n_split, d.U, d.G / mla::HEADS);
-  attn_mla_kernel<<<grid, mla::NW * 32, mla::SMEM, s>>>(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, n_split, bps);
+  launch_pdl(attn_mla_kernel, dim3(grid), dim3(mla::NW * 32), mla::SMEM, s, d, L, q, sel, slot_of_sel, nsel, ctx_len, out, n_split, bps);
   e = cudaGetLastError();
   if (e != cudaSuccess || n_split == 1) return e;
-  attn_combine_kernel<<<dim3(d.U, d.G), 128, 0, s>>>(d, L, out, n_split);
+  launch_pdl(attn_combine_kernel, dim3(dim3(d.U, d.G)), dim3(128), 0, s, d, L, out, n_split);
   return cudaGetLastError();
 }
 

@@ -2,14 +2,15 @@
 // head dim 128, block size a multiple of 16).
 //
 // The (unit, selected block, 16-row sub-tile) sequence of a layer is cut into equal contiguous
-// ranges, one per CTA, with exactly 2 CTAs per SM (room for a fetch CTA beside them).  In each CTA one producer thread streams the
-// K and V tiles of its range into an 8-stage shared-memory ring with 2D tensor loads (128-byte
+// ranges, one per CTA, with exactly 2 CTAs per SM (room for a fetch CTA beside them).  In each
+// CTA one producer thread streams the K and V tiles of its range into an 8-stage shared-memory ring with 2D tensor loads (128-byte
 // swizzle, completion on an mbarrier per stage); 4 consumer warps take the tiles round-robin,
 // each keeping an online softmax per q head on tensor-core tiles:
 //   S  = Q (16 heads x 128) . K^T (128 x 16 tokens)
 //   O += P (16 x 16) . V (16 x 128), P split into bf16 high and low parts.
-// A warp writes its (unnormalised O, max, sum) for every unit its CTA touches; a second kernel
-// merges the partials of a unit: o = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p.
+// A warp writes its (unnormalised O, max, sum) for every unit its CTA touches; the last CTA of a
+// unit to finish (a per-unit counter) merges that unit's partials:
+// o = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p.
 // The CTA's block ids, slots and the units' lengths are staged in shared memory first, so the
 // producer issues tensor loads without waiting on global memory.
 // Every mbarrier wait is bounded by the context's wait timeout (KVS_ERR_TIMEOUT on expiry).
@@ -42,7 +43,7 @@ __host__ __device__ inline Plan make_plan(const Dims& d, int n_sm) {
   const long long positions = (long long)d.U * d.Kb;
   int ctas = n_sm * kCtasPerSm;
   p.per_cta = (int)((positions + ctas - 1) / ctas);
-  // the merge kernel takes at most 1024 partials (segments x warps) of a unit
+  // at most 1024 partials (segments x warps) per unit (bounds the workspace's partial slots)
   const int seg_cap = 1024 / kConsumers - 1;
   const int min_per = (d.Kb + seg_cap - 1) / seg_cap;
   if (p.per_cta < min_per) p.per_cta = min_per;
@@ -61,12 +62,14 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
     attn_tma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, Dims d,
                     Layer L, const __nv_bfloat16* __restrict__ q, const int* __restrict__ sel,
                     const int* __restrict__ slot_of_sel, const int* __restrict__ nsel,
-                    const int* __restrict__ ctx_len, Plan plan) {
+                    const int* __restrict__ ctx_len, float* __restrict__ out, Plan plan) {
+  kvs_pdl_entry();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStage);
   uint64_t* empty = full + kStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+  volatile int* last_flag = abort_flag + 1;   // this CTA finished a unit last (consumers)
   int* m_blk = reinterpret_cast<int*>(smem + kStages * kStage + 2 * kStages * 8 + 64);   // [kMaxPos], -1: none
   int* m_slot = m_blk + kMaxPos;                                                       // [kMaxPos]
   int* u_len = m_slot + kMaxPos;                                                       // [kMaxUnits]
@@ -187,18 +190,21 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
     for (int x = 0; x < D / 8; ++x) oacc[x][0] = oacc[x][1] = oacc[x][2] = oacc[x][3] = 0.f;
 
     const long long pu0 = max(p0, (long long)u * d.Kb), pu1 = min(p1, (long long)(u + 1) * d.Kb);
-    for (long long p = pu0; p < pu1 && ok; ++p) {
+    for (long long p = pu0; p < pu1; ++p) {
       const int blk = m_blk[p - p0];
       if (blk < 0) continue;
       const int rows = rows_present(len, blk, d.bs);
       for (int sub = 0; sub < subs; ++sub) {
         if (sub * 16 >= rows) break;
         const int kk = k++;
-        if ((kk % kConsumers) != warp) continue;
+        if ((kk % kConsumers) != warp || !ok) continue;
         const int s = kk % kStages;
         if (!mbar_wait(&full[s], (kk / kStages) & 1, timeout_ns)) {
+          // give up on the remaining tiles, but still write and count this unit's partials below,
+          // so that the per-unit completion counters stay consistent for later launches
           ok = false;
-          break;
+          *abort_flag = 1;
+          continue;
         }
         const unsigned char* kt = smem + s * kStage;
         const unsigned char* vt = kt + kTile;
@@ -284,10 +290,11 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
         if (lane == 0) mbar_arrive(&empty[s]);
       }
     }
-    if (!ok) break;
     // partial state of this warp for unit u
-    const int seg = c - (int)(((long long)u * d.Kb) / plan.per_cta);
-    const size_t pidx = ((size_t)u * plan.max_segs + seg) * kConsumers + warp;
+    const int c0 = (int)(((long long)u * d.Kb) / plan.per_cta);
+    const int c1 = min(plan.n_cta - 1, (int)(((long long)(u + 1) * d.Kb - 1) / plan.per_cta));
+    const size_t base = (size_t)u * plan.max_segs * kConsumers;
+    const size_t pidx = base + (size_t)(c - c0) * kConsumers + warp;
     const int row_lo = lane >> 2, row_hi = row_lo + 8;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -297,79 +304,56 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
 #pragma unroll
       for (int nd = 0; nd < D / 8; ++nd) {
         const int col = nd * 8 + (lane & 3) * 2;
-        dst[col] = oacc[nd][hh * 2];
-        dst[col + 1] = oacc[nd][hh * 2 + 1];
+        *reinterpret_cast<float2*>(dst + col) = make_float2(oacc[nd][hh * 2], oacc[nd][hh * 2 + 1]);
       }
-      if ((lane & 3) == 0) {
-        L.attn_ml[(pidx * G + row) * 2 + 0] = hh ? m_hi : m_lo;
-        L.attn_ml[(pidx * G + row) * 2 + 1] = hh ? l_hi : l_lo;
+      if ((lane & 3) == 0)
+        *reinterpret_cast<float2*>(L.attn_ml + (pidx * G + row) * 2) = make_float2(hh ? m_hi : m_lo, hh ? l_hi : l_lo);
+    }
+    // Count this CTA's partials of unit u; the last CTA of the unit to finish merges them:
+    // o = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p, partials in ascending order, one warp per
+    // q head, 4 columns per lane.  The counter goes back to 0 for the next launch.
+    __threadfence();
+    named_bar_sync(1, kConsumers * 32);
+    if (tid == 0) *last_flag = atomicAdd(&L.unit_done[u], 1u) == (unsigned)(c1 - c0);
+    named_bar_sync(1, kConsumers * 32);
+    if (*last_flag) {
+      __threadfence();
+      const int np = (c1 - c0 + 1) * kConsumers;
+      const int r_out = u / d.Hkv, h_out = u % d.Hkv;
+      for (int g = warp; g < G; g += kConsumers) {
+        float M = -INFINITY;
+        for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(L.attn_ml + ((base + p) * G + g) * 2));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float lpart = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q0 = 0; q0 < np; q0 += 32) {
+          float wgt = 0.f;
+          if (q0 + lane < np) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(L.attn_ml + ((base + q0 + lane) * G + g) * 2));
+            wgt = (M == -INFINITY || ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+            lpart += wgt * ml.y;
+          }
+          const int nj = min(32, np - q0);
+          for (int j = 0; j < nj; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, wgt, j);
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(L.attn_part + ((base + q0 + j) * G + g) * D) + lane);
+            acc.x += wj * x.x;
+            acc.y += wj * x.y;
+            acc.z += wj * x.z;
+            acc.w += wj * x.w;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) lpart += __shfl_xor_sync(0xffffffffu, lpart, o);
+        const float inv = lpart > 0.f ? 1.f / lpart : 0.f;
+        float4 res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        reinterpret_cast<float4*>(out + ((size_t)r_out * d.Hq + h_out * G + g) * d.dv)[lane] = res;
       }
+      if (tid == 0) L.unit_done[u] = 0u;
     }
   }
-  if (!ok) {
-    set_error(L.err, KVS_ERR_TIMEOUT);
-    *abort_flag = 1;
-  }
-}
-
-// Merge the partials of one (unit, q head): load every partial's (max, sum) at once, then
-// o = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p with one thread per column.
-constexpr int kMergeThreads = 128;
-constexpr int kMergeMaxParts = 1024;
-
-__global__ void __launch_bounds__(kMergeThreads) attn_tma_merge(Dims d, Layer L, float* __restrict__ out, Plan plan) {
-  __shared__ float s_w[kMergeMaxParts];
-  __shared__ float s_red[kMergeThreads / 32];
-  __shared__ float s_M, s_L;
-  const int u = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
-  const int r = u / d.Hkv, h = u % d.Hkv;
-  const int c0 = (int)(((long long)u * d.Kb) / plan.per_cta);
-  const int c1 = min(plan.n_cta - 1, (int)(((long long)(u + 1) * d.Kb - 1) / plan.per_cta));
-  const int np = min(kMergeMaxParts, (c1 - c0 + 1) * kConsumers);
-  const size_t base = (size_t)u * plan.max_segs * kConsumers;
-  float mx = -INFINITY;
-  for (int p = tid; p < np; p += kMergeThreads) {
-    const float m = L.attn_ml[((base + p) * d.G + g) * 2];
-    s_w[p] = m;
-    mx = fmaxf(mx, m);
-  }
-  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if ((tid & 31) == 0) s_red[tid >> 5] = mx;
-  __syncthreads();
-  if (tid == 0) {
-    float M = -INFINITY;
-    for (int i = 0; i < kMergeThreads / 32; ++i) M = fmaxf(M, s_red[i]);
-    s_M = M;
-  }
-  __syncthreads();
-  const float M = s_M;
-  float ls = 0.f;
-  for (int p = tid; p < np; p += kMergeThreads) {
-    const float w = (M == -INFINITY || s_w[p] == -INFINITY) ? 0.f : exp2f(s_w[p] - M);
-    s_w[p] = w;
-    ls += w * L.attn_ml[((base + p) * d.G + g) * 2 + 1];
-  }
-  for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-  __syncthreads();
-  if ((tid & 31) == 0) s_red[tid >> 5] = ls;
-  __syncthreads();
-  if (tid == 0) {
-    float t = 0.f;
-    for (int i = 0; i < kMergeThreads / 32; ++i) t += s_red[i];
-    s_L = t;
-  }
-  __syncthreads();
-  const float lsum = s_L;
-  for (int col = tid; col < D; col += kMergeThreads) {
-    float o = 0.f;
-#pragma unroll 8
-    for (int p = 0; p < np; ++p) {
-      const float w = s_w[p];
-      const float x = L.attn_part[((base + p) * d.G + g) * D + col];
-      o += w * x;
-    }
-    out[((size_t)r * d.Hq + h * d.G + g) * d.dv + col] = lsum > 0.f ? o / lsum : 0.f;
-  }
+  if (!ok) set_error(L.err, KVS_ERR_TIMEOUT);
 }
 
 int sm_count() { return device_sm_count(); }
@@ -393,14 +377,11 @@ cudaError_t launch_attention_tma(const Dims& d, const Layer& L, const CUtensorMa
   }
   Plan plan = make_plan(d, sm_count());
   if (d.G <= 8)
-    attn_tma_kernel<true><<<plan.n_cta, (kConsumers + 1) * 32, kSmem, s>>>(*tmK, *tmV, d, L, q, sel, slot_of_sel,
-                                                                         nsel, ctx_len, plan);
+    launch_pdl(attn_tma_kernel<true>, dim3(plan.n_cta), dim3((kConsumers + 1) * 32), kSmem, s, *tmK, *tmV, d, L, q, sel,
+               slot_of_sel, nsel, ctx_len, out, plan);
   else
-    attn_tma_kernel<false><<<plan.n_cta, (kConsumers + 1) * 32, kSmem, s>>>(*tmK, *tmV, d, L, q, sel, slot_of_sel,
-                                                                          nsel, ctx_len, plan);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  attn_tma_merge<<<dim3(d.U, d.G), kMergeThreads, 0, s>>>(d, L, out, plan);
+    launch_pdl(attn_tma_kernel<false>, dim3(plan.n_cta), dim3((kConsumers + 1) * 32), kSmem, s, *tmK, *tmV, d, L, q, sel,
+               slot_of_sel, nsel, ctx_len, out, plan);
   return cudaGetLastError();
 }
 

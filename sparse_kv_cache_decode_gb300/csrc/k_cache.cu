@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
                                                                      const int* __restrict__ nsel,
                                                                      const int* __restrict__ ctx_len,
                                                                      int* __restrict__ slot_of_sel, kvs_stats* stats) {
+  kvs_pdl_entry();
   extern __shared__ __align__(16) unsigned char smraw[];
   __shared__ int hist[256];
   __shared__ int ws[33];
@@ -132,6 +133,7 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
     if (tid == 0) {
       set_error(L.err, KVS_ERR_BAD_INDEX);
       L.n_fetch[u] = 0;
+      L.next_commit[u] = 0;
     }
     return;
   }
@@ -172,6 +174,7 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
     if (tid == 0) {
       set_error(L.err, KVS_ERR_BAD_INDEX);
       L.n_fetch[u] = 0;
+      L.next_commit[u] = 0;
     }
     return;
   }
@@ -206,6 +209,7 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
     if (tid == 0) {
       set_error(L.err, KVS_ERR_CAPACITY);
       L.n_fetch[u] = 0;
+      L.next_commit[u] = 0;
     }
     return;
   }
@@ -235,14 +239,17 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
     int s = sm.sos[i];
     st[s] = now;
     slot_of_sel[(size_t)u * d.Kb + i] = s;
-    if (d.lookahead) {
-      L.pend_sel[(size_t)u * d.Kb + i] = su[i];
-      L.pend_slot[(size_t)u * d.Kb + i] = s;
+    if (d.lookahead) {   // staged; the fetch that follows commits it to pend_*
+      L.next_sel[(size_t)u * d.Kb + i] = su[i];
+      L.next_slot[(size_t)u * d.Kb + i] = s;
     }
   }
   if (tid == 0) {
     L.n_fetch[u] = m;
-    if (d.lookahead) L.pend_n[u] = n;
+    if (d.lookahead) {
+      L.next_n[u] = n;
+      L.next_commit[u] = 1;
+    }
     if (stats) {
       kvs_stats* sl = stats + L.layer;
       atomicAdd(&sl->hits, (unsigned long long)(n - m));
@@ -258,6 +265,7 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
 __global__ void __launch_bounds__(kCacheThreads) prefetch_kernel(Dims d, Layer L, const int* __restrict__ hint,
                                                                  const int* __restrict__ hint_n,
                                                                  const int* __restrict__ ctx_len, kvs_stats* stats) {
+  kvs_pdl_entry();
   extern __shared__ __align__(16) unsigned char smraw[];
   __shared__ int hist[256];
   __shared__ int ws[33];
@@ -355,9 +363,27 @@ constexpr int kFetchMaxUnits = 1024;
 constexpr int kFetchUnroll = 16;
 
 __global__ void __launch_bounds__(kFetchThreads) fetch_kernel(Dims d, Layer L, const int* __restrict__ ctx_len) {
+  kvs_pdl_entry();
   __shared__ int s_off[kFetchMaxUnits + 1];
   __shared__ int ws[33];
   const int tid = threadIdx.x, lane = tid & 31;
+  // lookahead: commit the selections the update staged (this kernel runs after the layer's
+  // attention over the previous pending selection); unit u is handled by CTA u % grid
+  if (d.lookahead) {
+    for (int u = blockIdx.x; u < d.U; u += gridDim.x) {
+      if (!L.next_commit[u]) continue;
+      const int n = L.next_n[u];
+      for (int i = tid; i < n; i += blockDim.x) {
+        L.pend_sel[(size_t)u * d.Kb + i] = L.next_sel[(size_t)u * d.Kb + i];
+        L.pend_slot[(size_t)u * d.Kb + i] = L.next_slot[(size_t)u * d.Kb + i];
+      }
+      __syncthreads();
+      if (tid == 0) {
+        L.pend_n[u] = n;
+        L.next_commit[u] = 0;
+      }
+    }
+  }
   // prefix sum of the per-unit item counts
   const int per = (d.U + blockDim.x - 1) / blockDim.x;
   const int u0 = min(d.U, tid * per), u1 = min(d.U, u0 + per);
@@ -442,7 +468,7 @@ cudaError_t launch_cache_update(const Dims& d, const Layer& L, const int* sel, c
     cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(cache_update_kernel), (int)smem);
     if (e != cudaSuccess) return e;
   }
-  cache_update_kernel<<<d.U, kCacheThreads, smem, s>>>(d, L, sel, nsel, ctx_len, slot_of_sel, stats);
+  launch_pdl(cache_update_kernel, dim3(d.U), dim3(kCacheThreads), smem, s, d, L, sel, nsel, ctx_len, slot_of_sel, stats);
   return cudaGetLastError();
 }
 
@@ -453,13 +479,13 @@ cudaError_t launch_prefetch(const Dims& d, const Layer& L, const int* hint, cons
     cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(prefetch_kernel), (int)smem);
     if (e != cudaSuccess) return e;
   }
-  prefetch_kernel<<<d.U, kCacheThreads, smem, s>>>(d, L, hint, hint_n, ctx_len, stats);
+  launch_pdl(prefetch_kernel, dim3(d.U), dim3(kCacheThreads), smem, s, d, L, hint, hint_n, ctx_len, stats);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fetch(const Dims& d, const Layer& L, const int* ctx_len, cudaStream_t s) {
   if (d.U > kFetchMaxUnits) return cudaErrorInvalidValue;
-  fetch_kernel<<<kFetchCTAs, kFetchThreads, 0, s>>>(d, L, ctx_len);
+  launch_pdl(fetch_kernel, dim3(kFetchCTAs), dim3(kFetchThreads), 0, s, d, L, ctx_len);
   return cudaGetLastError();
 }
 

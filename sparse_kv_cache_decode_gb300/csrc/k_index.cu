@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(128) append_kernel(Dims d, Layer L, const __nv
                                                      const __nv_bfloat16* __restrict__ v_new,
                                                      __nv_bfloat16* __restrict__ index,
                                                      const int* __restrict__ ctx_len) {
+  kvs_pdl_entry();
   const int u = blockIdx.x;
   const int r = u / d.Hkv;
   const int len = ctx_len[r];
@@ -132,7 +133,7 @@ __global__ void __launch_bounds__(128) append_kernel(Dims d, Layer L, const __nv
 
 cudaError_t launch_append(const Dims& d, const Layer& L, const __nv_bfloat16* k_new, const __nv_bfloat16* v_new,
                           __nv_bfloat16* index, const int* ctx_len, cudaStream_t s) {
-  append_kernel<<<d.U, 128, 0, s>>>(d, L, k_new, v_new, index, ctx_len);
+  launch_pdl(append_kernel, dim3(d.U), dim3(128), 0, s, d, L, k_new, v_new, index, ctx_len);
   return cudaGetLastError();
 }
 
@@ -158,12 +159,13 @@ cudaError_t launch_touch_pages(const void* base, size_t bytes, unsigned* sink, c
 }
 
 __global__ void advance_kernel(int B, int* ctx_len) {
+  kvs_pdl_entry();
   int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r < B) ctx_len[r] += 1;
 }
 
 cudaError_t launch_advance(int B, int* ctx_len, cudaStream_t s) {
-  advance_kernel<<<(B + 127) / 128, 128, 0, s>>>(B, ctx_len);
+  launch_pdl(advance_kernel, dim3((B + 127) / 128), dim3(128), 0, s, B, ctx_len);
   return cudaGetLastError();
 }
 

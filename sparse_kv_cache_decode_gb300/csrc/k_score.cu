@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(128) score_kernel(Dims d, const __nv_bfloat16*
                                                     const __nv_bfloat16* __restrict__ q, int nq,
                                                     const int* __restrict__ ctx_len, float* __restrict__ scores,
                                                     int tiles_per_cta, unsigned* err) {
+  kvs_pdl_entry();
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int RS = DK * 2 + 16;  // row stride in bytes
   constexpr int KSTEPS = DK / 16;
@@ -158,7 +159,7 @@ cudaError_t launch_score_t(const Dims& d, const __nv_bfloat16* index, const __nv
   int ctas_per_unit = max(1, min((max_tiles + 4 * nwarps - 1) / (4 * nwarps), (2 * device_sm_count() + d.U - 1) / d.U));
   int tiles_per_cta = (max_tiles + ctas_per_unit - 1) / ctas_per_unit;
   dim3 grid(ctas_per_unit, d.U);
-  kern<<<grid, 32 * nwarps, bytes, s>>>(d, index, q, nq, ctx_len, scores, tiles_per_cta, err);
+  launch_pdl(kern, dim3(grid), dim3(32 * nwarps), bytes, s, d, index, q, nq, ctx_len, scores, tiles_per_cta, err);
   return cudaGetLastError();
 }
 

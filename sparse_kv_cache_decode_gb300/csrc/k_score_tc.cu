@@ -63,6 +63,7 @@ TcPlan make_tc_plan(const Dims& d, int nq, int n_sm) {
 __global__ void __launch_bounds__(kThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap tm_idx, Dims d, const __nv_bfloat16* __restrict__ q, int nq,
                     const int* __restrict__ ctx_len, float* __restrict__ scores, TcPlan plan, unsigned* err) {
+  kvs_pdl_entry();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* a_st = smem;                                   // stages x 16 KiB
@@ -249,7 +250,7 @@ cudaError_t launch_score_tc(const Dims& d, const __nv_bfloat16* index, const __n
   if (!make_tmap_2d(&tm, const_cast<__nv_bfloat16*>(index), (uint64_t)d.dk, (uint64_t)d.U * d.nb_max, kChunk, kTileM))
     return cudaErrorInvalidValue;
   TcPlan plan = make_tc_plan(d, nq, sm_count_tc());
-  score_tc_kernel<<<plan.n_cta, kThreads, plan.smem, s>>>(tm, d, q, nq, ctx_len, scores, plan, err);
+  launch_pdl(score_tc_kernel, dim3(plan.n_cta), dim3(kThreads), plan.smem, s, tm, d, q, nq, ctx_len, scores, plan, err);
   return cudaGetLastError();
 }
 

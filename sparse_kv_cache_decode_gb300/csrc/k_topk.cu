@@ -113,6 +113,7 @@ __device__ void select_ordered(const uint32_t* keys, int n, int k, int* hist, in
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(Dims d, const float* __restrict__ scores,
                                                             const int* __restrict__ ctx_len, int* __restrict__ sel,
                                                             int* __restrict__ nsel, unsigned* err) {
+  kvs_pdl_entry();
   extern __shared__ uint32_t skeys[];
   __shared__ int hist[256];
   __shared__ int ws[33];
@@ -227,6 +228,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(Dims d, const 
                                                                   const int* __restrict__ ctx_len, int P,
                                                                   uint32_t* __restrict__ ckey, int* __restrict__ cidx,
                                                                   int* __restrict__ ccnt) {
+  kvs_pdl_entry();
   extern __shared__ uint32_t skeys[];
   __shared__ int hist[256];
   __shared__ int ws[33];
@@ -266,6 +268,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(Dims d, const 
                                                                   const int* __restrict__ cidx,
                                                                   const int* __restrict__ ccnt, int* __restrict__ sel,
                                                                   int* __restrict__ nsel, unsigned* err) {
+  kvs_pdl_entry();
   extern __shared__ uint32_t smem[];
   __shared__ int hist[256];
   __shared__ int ws[33];
@@ -345,11 +348,11 @@ cudaError_t launch_topk(const Dims& d, const float* scores, const int* ctx_len, 
       if (e == cudaSuccess) e = set_max_dynamic_smem(reinterpret_cast<const void*>(topk_merge_kernel), (int)kTopkMergeSmemMax);
       if (e != cudaSuccess) return e;
     }
-    topk_chunk_kernel<<<dim3(P, d.U), kTopkThreads, kChunk * sizeof(uint32_t), s>>>(d, scores, ctx_len, P, scratch->key,
+    launch_pdl(topk_chunk_kernel, dim3(dim3(P, d.U)), dim3(kTopkThreads), kChunk * sizeof(uint32_t), s, d, scores, ctx_len, P, scratch->key,
                                                                                   scratch->idx, scratch->cnt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    topk_merge_kernel<<<d.U, kTopkThreads, (size_t)P * d.Kb * 8, s>>>(d, ctx_len, P, scratch->key, scratch->idx,
+    launch_pdl(topk_merge_kernel, dim3(d.U), dim3(kTopkThreads), (size_t)P * d.Kb * 8, s, d, ctx_len, P, scratch->key, scratch->idx,
                                                                      scratch->cnt, sel, nsel, err);
     return cudaGetLastError();
   }
@@ -358,7 +361,7 @@ cudaError_t launch_topk(const Dims& d, const float* scores, const int* ctx_len, 
     cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(topk_kernel), (int)smem);
     if (e != cudaSuccess) return e;
   }
-  topk_kernel<<<d.U, kTopkThreads, smem, s>>>(d, scores, ctx_len, sel, nsel, err);
+  launch_pdl(topk_kernel, dim3(d.U), dim3(kTopkThreads), smem, s, d, scores, ctx_len, sel, nsel, err);
   return cudaGetLastError();
 }
 

@@ -35,7 +35,10 @@ struct kvs_ctx {
   std::vector<int> sel_pending, pf_pending;
   std::vector<CUtensorMap> tmaps;   // per layer: K pool, V pool (TMA attention path)
   kvs::TopkScratch tk{};            // two-phase top-K candidates (long contexts), shared by layers
-  cudaEvent_t fork;
+  // overlapped lookahead steps: the selection chain's stream, and per layer the events that order
+  // it (start after the layer below's attention; update done; attention done)
+  cudaStream_t sel_stream = nullptr;
+  std::vector<cudaEvent_t> layer_start, upd_done, attn_done;
   // diagnostics
   unsigned long long launches = 0;
   struct Timer {
@@ -100,6 +103,7 @@ bool fill_dims(const kvs_config* c, Dims* d) {
 // Byte sizes of the per-layer and shared workspace regions.
 struct Plan {
   size_t kpool, vpool, b2s, s2b, stamp, clock, pend_sel, pend_slot, pend_n, sel, nsel, sos, fblk, fslot, nfetch;
+  size_t next_sel, next_slot, next_n, next_commit;
   size_t per_layer;
   size_t err, scores, part, ml, done, tk_key, tk_idx, tk_cnt;
   size_t total;
@@ -123,8 +127,12 @@ Plan plan_of(const Dims& d) {
   p.fblk = align_up(U * d.C * 4);
   p.fslot = align_up(U * d.C * 4);
   p.nfetch = align_up(U * 4);
+  p.next_sel = align_up(U * d.Kb * 4);
+  p.next_slot = align_up(U * d.Kb * 4);
+  p.next_n = align_up(U * 4);
+  p.next_commit = align_up(U * 4);
   p.per_layer = p.kpool + p.vpool + p.b2s + p.s2b + p.stamp + p.clock + p.pend_sel + p.pend_slot + p.pend_n + p.sel +
-                p.nsel + p.sos + p.fblk + p.fslot + p.nfetch;
+                p.nsel + p.sos + p.fblk + p.fslot + p.nfetch + p.next_sel + p.next_slot + p.next_n + p.next_commit;
   p.err = align_up(16);
   p.scores = align_up(U * d.nb_max * 4);
   size_t parts = kAttnSplitMax;
@@ -208,8 +216,9 @@ cudaError_t timed(kvs_ctx* c, int kernel, cudaStream_t s, int n_kernels, F&& lau
 }
 
 int attn_kernels(const Dims& d) {
-  // attention kernel, plus the split combine when the selection is split across CTAs
-  if (attention_tma_supported(d)) return 2;
+  // attention kernel (the TMA path merges its partials in-kernel), plus the split combine of the
+  // cp.async paths when the selection is split across CTAs
+  if (attention_tma_supported(d)) return 1;
   int n_split = 1, bps = 0;
   if (!attention_split(d, &n_split, &bps)) return 1;
   return n_split > 1 ? 2 : 1;
@@ -315,6 +324,10 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
     L.fetch_blk = reinterpret_cast<int*>(b); b += p.fblk;
     L.fetch_slot = reinterpret_cast<int*>(b); b += p.fslot;
     L.n_fetch = reinterpret_cast<int*>(b); b += p.nfetch;
+    L.next_sel = reinterpret_cast<int*>(b); b += p.next_sel;
+    L.next_slot = reinterpret_cast<int*>(b); b += p.next_slot;
+    L.next_n = reinterpret_cast<int*>(b); b += p.next_n;
+    L.next_commit = reinterpret_cast<int*>(b); b += p.next_commit;
     L.scores = scores;
     L.attn_part = part;
     L.attn_ml = ml;
@@ -331,6 +344,7 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
     if (e == cudaSuccess) e = cudaMemset(L.clock, 0, p.clock);
     if (e == cudaSuccess) e = cudaMemset(L.pend_n, 0xff, p.pend_n);
     if (e == cudaSuccess) e = cudaMemset(L.n_fetch, 0, p.nfetch);
+    if (e == cudaSuccess) e = cudaMemset(L.next_commit, 0, p.next_commit);
     if (e != cudaSuccess) {
       delete c;
       return KVS_ERR_CUDA;
@@ -363,19 +377,22 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   c->pf_done.assign(d.NL, nullptr);
   c->sel_pending.assign(d.NL, 0);
   c->pf_pending.assign(d.NL, 0);
-  for (int l = 0; l < d.NL; ++l)
-    if (cudaEventCreateWithFlags(&c->sel_ready[l], cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&c->pf_done[l], cudaEventDisableTiming) != cudaSuccess) {
-      delete c;
-      return KVS_ERR_CUDA;
-    }
-  for (int l = 0; l < d.NL; ++l)
-    if (cudaEventCreateWithFlags(&c->fetch_done[l], cudaEventDisableTiming) != cudaSuccess) {
-      delete c;
-      return KVS_ERR_CUDA;
-    }
-  if (cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming) != cudaSuccess) {
-    delete c;
+  c->layer_start.assign(d.NL, nullptr);
+  c->upd_done.assign(d.NL, nullptr);
+  c->attn_done.assign(d.NL, nullptr);
+  for (auto* v : {&c->sel_ready, &c->pf_done, &c->fetch_done, &c->layer_start, &c->upd_done, &c->attn_done})
+    for (cudaEvent_t& ev : *v)
+      if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+        ev = nullptr;
+        kvs_destroy(c);
+        return KVS_ERR_CUDA;
+      }
+  // the selection chain of overlapped lookahead steps is the step's critical path: highest priority
+  int lo = 0, hi = 0;
+  if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&c->sel_stream, cudaStreamNonBlocking, hi) != cudaSuccess) {
+    c->sel_stream = nullptr;
+    kvs_destroy(c);
     return KVS_ERR_CUDA;
   }
   *out = c;
@@ -423,13 +440,10 @@ kvs_status kvs_destroy(kvs_ctx* c) {
     for (cudaEvent_t e : t.start) cudaEventDestroy(e);
     for (cudaEvent_t e : t.stop) cudaEventDestroy(e);
   }
-  for (cudaEvent_t e : c->fetch_done)
-    if (e) cudaEventDestroy(e);
-  for (cudaEvent_t e : c->sel_ready)
-    if (e) cudaEventDestroy(e);
-  for (cudaEvent_t e : c->pf_done)
-    if (e) cudaEventDestroy(e);
-  if (c->fork) cudaEventDestroy(c->fork);
+  for (auto* v : {&c->sel_ready, &c->pf_done, &c->fetch_done, &c->layer_start, &c->upd_done, &c->attn_done})
+    for (cudaEvent_t e : *v)
+      if (e) cudaEventDestroy(e);
+  if (c->sel_stream) cudaStreamDestroy(c->sel_stream);
   delete c;
   return KVS_OK;
 }
@@ -439,6 +453,16 @@ kvs_status kvs_bind_host_kv(kvs_ctx* c, void* h_k, void* h_v) {
   if (c->d.v_shares_k ? h_v != nullptr : h_v == nullptr) return KVS_ERR_INVALID_ARG;
   void* dk = nullptr;
   void* dv = nullptr;
+  // page-locked host memory only: where the device can also reach pageable memory (address
+  // translation services), cudaHostGetDevicePointer alone would accept it
+  for (void* h : {h_k, h_v}) {
+    if (!h) continue;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, h) != cudaSuccess || a.type != cudaMemoryTypeHost) {
+      cudaGetLastError();
+      return KVS_ERR_HOST_MEM;
+    }
+  }
   if (cudaHostGetDevicePointer(&dk, h_k, 0) != cudaSuccess) {
     cudaGetLastError();
     return KVS_ERR_HOST_MEM;
@@ -576,24 +600,27 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
   cudaError_t e = cudaSuccess;
   const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(d_k_new);
   const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(d_v_new);
+  // the selection chain (score, top-K, update) runs on `ss`: `s`, or in lookahead mode with a copy
+  // stream the context's own selection stream, beside the attention on `s`
+  cudaStream_t ss = s;
   auto score = [&](const __nv_bfloat16* rows, int n) {
-    return timed(c, KVS_K_SCORE, s, 1, [&] { return launch_score(d, idx, rows, n, d_ctx_len, L.scores, c->err, s); });
+    return timed(c, KVS_K_SCORE, ss, 1, [&] { return launch_score(d, idx, rows, n, d_ctx_len, L.scores, c->err, ss); });
   };
   auto topk = [&](int* so, int* no) {
-    cudaError_t r = timed(c, KVS_K_TOPK, s, 1, [&] { return launch_topk(d, L.scores, d_ctx_len, so, no, c->err, s, c->tk.key ? &c->tk : nullptr); });
-    if (r == cudaSuccess) r = cudaEventRecord(c->sel_ready[layer], s);   // hint for a prefetch into layer + 1
+    cudaError_t r = timed(c, KVS_K_TOPK, ss, 1, [&] { return launch_topk(d, L.scores, d_ctx_len, so, no, c->err, ss, c->tk.key ? &c->tk : nullptr); });
+    if (r == cudaSuccess) r = cudaEventRecord(c->sel_ready[layer], ss);   // hint for a prefetch into layer + 1
     if (r == cudaSuccess) c->sel_pending[layer] = 1;
     return r;
   };
   auto update = [&](const int* so, const int* no) {
     cudaError_t r = cudaSuccess;
     if (c->pf_pending[layer]) {       // a prefetch into this layer ran on another stream
-      r = cudaStreamWaitEvent(s, c->pf_done[layer], 0);
+      r = cudaStreamWaitEvent(ss, c->pf_done[layer], 0);
       c->pf_pending[layer] = 0;
     }
     if (r != cudaSuccess) return r;
-    return timed(c, KVS_K_UPDATE, s, 1,
-                 [&] { return launch_cache_update(d, L, so, no, d_ctx_len, L.slot_of_sel, d_stats, s); });
+    return timed(c, KVS_K_UPDATE, ss, 1,
+                 [&] { return launch_cache_update(d, L, so, no, d_ctx_len, L.slot_of_sel, d_stats, ss); });
   };
   auto fetch = [&](cudaStream_t fs) {
     return timed(c, KVS_K_FETCH, fs, 1, [&] { return launch_fetch(d, L, d_ctx_len, fs); });
@@ -611,28 +638,51 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
     if (e == cudaSuccess) e = attn(sel, L.slot_of_sel, nsel);
     return cuda_status(e);
   }
-  if (!c->booted[layer]) {
-    // no selection yet: pick S_t from the current query and make it resident (sync part)
-    if (e == cudaSuccess) e = score(q, 1);
-    if (e == cudaSuccess) e = topk(L.sel, L.nsel);
-    if (e == cudaSuccess) e = update(L.sel, L.nsel);
+  // no selection yet (the layer's first lookahead step): pick S_t from the current query and make
+  // it resident, on the stream that runs the selection chain, before the attention reads it
+  auto bootstrap = [&](cudaStream_t fs) {
+    cudaError_t r = score(q, 1);
+    if (r == cudaSuccess) r = topk(L.sel, L.nsel);
+    if (r == cudaSuccess) r = update(L.sel, L.nsel);
+    if (r == cudaSuccess) r = fetch(fs);
+    if (r == cudaSuccess) c->booted[layer] = 1;
+    return r;
+  };
+  if (cs == s) {
+    // one stream: attention over S_t, then the selection of S_{t+1} and its fetch
+    if (e == cudaSuccess && !c->booted[layer]) e = bootstrap(s);
+    if (e == cudaSuccess) e = attn(L.pend_sel, L.pend_slot, L.pend_n);
+    if (e == cudaSuccess) e = score(sq, nq);
+    if (e == cudaSuccess) e = topk(sel, nsel);
+    if (e == cudaSuccess) e = update(sel, nsel);
     if (e == cudaSuccess) e = fetch(s);
-    if (e == cudaSuccess) c->booted[layer] = 1;
+    return cuda_status(e);
   }
-  if (e == cudaSuccess) e = attn(L.pend_sel, L.pend_slot, L.pend_n);
+  // Overlapped: the selection of S_{t+1} (score with the drafts, top-K, update with S_t pinned,
+  // which stages the new pending selection) starts on the selection stream as soon as the layer
+  // below has finished its attention, and runs beside this layer's attention over S_t on `s`.  The
+  // fetch waits for both: it writes only slots the update freed, and it commits the staged
+  // selection, which the attention must no longer be reading.  The selection chains of all layers
+  // share the block-score and top-K scratch, so they all run on the one selection stream.
+  ss = c->sel_stream;
+  if (e == cudaSuccess) e = cudaEventRecord(c->layer_start[layer], s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss, c->layer_start[layer], 0);
+  if (e == cudaSuccess && !c->booted[layer]) {
+    e = bootstrap(ss);
+    if (e == cudaSuccess) e = cudaEventRecord(c->upd_done[layer], ss);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->upd_done[layer], 0);
+  }
   if (e == cudaSuccess) e = score(sq, nq);
   if (e == cudaSuccess) e = topk(sel, nsel);
   if (e == cudaSuccess) e = update(sel, nsel);
-  if (e != cudaSuccess) return cuda_status(e);
-  if (cs != s) {
-    e = cudaEventRecord(c->fork, s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, c->fork, 0);
-    if (e == cudaSuccess) e = fetch(cs);
-    if (e == cudaSuccess) e = cudaEventRecord(c->fetch_done[layer], cs);
-    if (e == cudaSuccess) c->fetch_pending[layer] = 1;
-  } else {
-    e = fetch(s);
-  }
+  if (e == cudaSuccess) e = cudaEventRecord(c->upd_done[layer], ss);
+  if (e == cudaSuccess) e = attn(L.pend_sel, L.pend_slot, L.pend_n);
+  if (e == cudaSuccess) e = cudaEventRecord(c->attn_done[layer], s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, c->attn_done[layer], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, c->upd_done[layer], 0);
+  if (e == cudaSuccess) e = fetch(cs);
+  if (e == cudaSuccess) e = cudaEventRecord(c->fetch_done[layer], cs);
+  if (e == cudaSuccess) c->fetch_pending[layer] = 1;
   return cuda_status(e);
 }
 

@@ -34,6 +34,13 @@ struct Layer {
   int* pend_sel;         // [U][Kb]  selection the next lookahead attention reads
   int* pend_slot;        // [U][Kb]
   int* pend_n;           // [U]      -1: none yet
+  // A lookahead update stages the selection it made here and marks the unit; the fetch that
+  // follows it (which runs after the layer's attention over the current pending selection has
+  // finished) commits the staged copy to pend_*, so attention and update may run concurrently.
+  int* next_sel;         // [U][Kb]
+  int* next_slot;        // [U][Kb]
+  int* next_n;           // [U]
+  int* next_commit;      // [U]      1: next_* awaits its commit
   float* scores;         // [U][nb_max]   scratch
   int* sel;              // [U][Kb]       scratch (fused step)
   int* nsel;             // [U]
@@ -52,6 +59,33 @@ struct Layer {
 };
 
 constexpr int kAttnSplitMax = 32;
+
+// Programmatic dependent launch.  The step's kernels are launched with programmatic stream
+// serialisation (launch_pdl), so a kernel's CTAs may be scheduled while the kernel before it in
+// the stream is still running; each such kernel therefore begins with kvs_pdl_entry(): wait until
+// the preceding grid has completed and its writes are visible (before any global memory access),
+// then allow the next kernel's CTAs to be scheduled.  Without the launch attribute both
+// instructions are no-ops.
+__device__ __forceinline__ void kvs_pdl_entry() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 __device__ __forceinline__ void set_error(unsigned* err, unsigned code) {
   atomicCAS(err, 0u, code);

@@ -18,6 +18,8 @@ INT_CASES = [
     (W.TINY.with_(name="tiny_int", n_req=2, int_scale=2.0), [4096, 3001], False),
     (W.TINY_LOOKAHEAD.with_(name="tiny_la_int", n_req=2, int_scale=2.0), [4096, 3001], False),
     (W.TINY_LOOKAHEAD.with_(name="tiny_la_int_cs", n_req=2, int_scale=2.0), [4096, 2050], True),
+    # three layers: each layer's selection chain overlaps the attention of the layers around it
+    (W.TINY_LOOKAHEAD.with_(name="tiny_la3_int_cs", n_req=2, n_layer=3, int_scale=2.0), [4096, 1777], True),
     (W.TINY_APPEND.with_(name="tiny_app_int", n_req=2, int_scale=2.0), [4096, 1000], False),
     (W.TINY_PREFETCH.with_(name="tiny_pf_int", n_req=2, int_scale=2.0), [4096, 4095], False),
     (W.TINY_PREFETCH.with_(name="tiny_pf_int_cs", n_req=2, n_layer=3, int_scale=2.0), [4096, 3333], True),
@@ -36,6 +38,56 @@ def test_decode_step_integer_inputs_bit_exact(w, lens, copy_stream):
     for t in range(min(w.steps, 16)):
         q, d, nk, nv = g.step_inputs(t)
         g.gpu_step(q, d, nk, nv)
+        out_ref, recs = o.step(q, d, nk, nv)
+        _compare_step(g, o, out_ref, recs, cum, exact=True)
+    assert g.ctx.poll_error() == 0
+
+
+GRAPH_CASES = [
+    (W.TINY_LOOKAHEAD.with_(name="tiny_la3_graph", n_req=2, n_layer=3, int_scale=2.0), [4096, 2050]),
+    (W.TINY_APPEND.with_(name="tiny_app2_graph", n_req=2, n_layer=2, int_scale=2.0), [4096, 1000]),
+]
+
+
+@pytest.mark.parametrize("w,lens", GRAPH_CASES, ids=[c[0].name for c in GRAPH_CASES])
+def test_captured_step_replays_bit_exact(w, lens):
+    """The whole step captured once as a CUDA graph over fixed input buffers (as a serving loop
+    runs it, with the fetch and the selection chain on their own streams) and replayed step after
+    step: selections, cache state, counters and outputs follow the oracle exactly."""
+    g = GpuCase(w, lens, copy_stream=True)
+    o = g.oracle()
+    cum = {l: {k: 0 for k in STAT_KEYS} for l in range(w.n_layer)}
+    q, d, nk, nv = g.step_inputs(0)
+    g.gpu_step(q, d, nk, nv)
+    out_ref, recs = o.step(q, d, nk, nv)
+    _compare_step(g, o, out_ref, recs, cum, exact=True)
+    B, NL = w.n_req, w.n_layer
+    qf = torch.empty((NL, B, w.n_q_head, w.d_k), dtype=torch.int16, device="cuda")
+    df = torch.empty((NL, B, w.n_draft, w.n_q_head, w.d_k), dtype=torch.int16, device="cuda") if w.lookahead else None
+    kf = torch.empty((NL, B, w.n_kv_head, w.d_k), dtype=torch.int16, device="cuda") if w.append else None
+    vf = torch.empty((NL, B, w.n_kv_head, w.d_v), dtype=torch.int16, device="cuda") if w.append else None
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        if w.append:
+            g.ctx.advance_ctx(g.ctx_len, stream=s)
+        for l in range(NL):
+            g.ctx.decode_step(l, qf[l], None if df is None else df[l], w.n_score_q if df is not None else 1, g.index,
+                              g.ctx_len, g.out[l], g.stats, None if kf is None else kf[l],
+                              None if vf is None else vf[l], g.sel[l], g.nsel[l], stream=s,
+                              copy_stream=g.copy_stream)
+        g.ctx.join(s)
+    for t in range(1, 8):
+        q, d, nk, nv = g.step_inputs(t)
+        qf.copy_(torch.from_numpy(q.view(np.int16)))
+        if df is not None:
+            df.copy_(torch.from_numpy(d.view(np.int16)))
+        if kf is not None:
+            kf.copy_(torch.from_numpy(nk.view(np.int16)))
+            vf.copy_(torch.from_numpy(nv.view(np.int16)))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
         out_ref, recs = o.step(q, d, nk, nv)
         _compare_step(g, o, out_ref, recs, cum, exact=True)
     assert g.ctx.poll_error() == 0
