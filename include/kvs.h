@@ -87,7 +87,14 @@ typedef struct {
   int max_prefetch;    /* per-unit cap of kvs_layer_prefetch; 0 -> C - K_b */
   float softmax_scale; /* 0 -> 1/sqrt(d_k) rounded to fp32 */
   unsigned wait_timeout_us; /* bound on device waits (0 -> 2000000 us) */
+  int evict_policy;    /* KVS_EVICT_LRU (0) or KVS_EVICT_IMPORTANCE (1) [OASIS module 3, HISP insight 2] */
 } kvs_config;
+
+/* Victim order of the cache update.  LRU: least recently used first, by (stamp, slot).
+ * IMPORTANCE: least important first: the block's score in the scoring that made the selection
+ * (NaN lowest, -0.0 == +0.0), ties by slot.  Both take empty slots first; the cross-layer
+ * prefetch always picks its victims by LRU (no scores of the destination layer exist yet). */
+enum { KVS_EVICT_LRU = 0, KVS_EVICT_IMPORTANCE = 1 };
 
 /* Per-layer counters, accumulated with atomics into a caller buffer kvs_stats[N_l]. */
 typedef struct {
@@ -142,14 +149,33 @@ kvs_status kvs_topk_select(kvs_ctx* ctx, const float* d_scores, const int* d_ctx
 /* Cache update of one layer [SPEC 2.1, OASIS module 3, HISP insight 2], then the fetch of the
  * misses from host memory into their slots (rows < L of each block), on `stream`:
  *   clock += 1; hits = selected blocks already resident; misses = the delta (ascending);
- *   victims = slots that are empty or hold a block neither selected nor pinned, least recently
- *   used first by (stamp, slot); miss i takes victim i; every selected block is stamped 2*clock.
+ *   victims = slots that are empty or hold a block neither selected nor pinned, in the order of
+ *   cfg.evict_policy (least recently used by (stamp, slot), or least important by d_scores);
+ *   miss i takes victim i; every selected block is stamped 2*clock.
  * In lookahead mode the blocks of the layer's previous selection are pinned (they are what the
  * pending attention reads); with too few victims the pins are dropped (pin_fallbacks).  Writes
- * slot_of_sel; adds to d_stats[layer] when d_stats is not NULL.  Device error
- * KVS_ERR_CAPACITY when even without pins the victims are fewer than the misses. */
+ * slot_of_sel; adds to d_stats[layer] when d_stats is not NULL.  d_scores [B][H_kv][n_b(max_ctx)]
+ * fp32: the block scores behind d_sel, required under KVS_EVICT_IMPORTANCE (else unused, may be
+ * NULL).  Device errors: KVS_ERR_CAPACITY when even without pins the victims are fewer than the
+ * misses; KVS_ERR_BAD_INDEX for a block id out of range or a selection that is not strictly
+ * ascending (the unit's state is then left unchanged). */
 kvs_status kvs_cache_update(kvs_ctx* ctx, int layer, const int* d_sel, const int* d_nsel, const int* d_ctx_len,
-                            int* d_slot_of_sel, kvs_stats* d_stats, kvs_stream_t stream);
+                            int* d_slot_of_sel, const float* d_scores, kvs_stats* d_stats, kvs_stream_t stream);
+
+/* Speculative rollback of a layer's cache state [KVC 6.1: save the block table before the drafts,
+ * copy it back when they are rejected].  The snapshot holds the maps, stamps, clocks and the
+ * pending lookahead selection of every unit of the layer, in a caller device buffer of
+ * kvs_snapshot_bytes(cfg) bytes (256-byte aligned).  kvs_cache_snapshot copies them there with
+ * device-to-device copies on `stream`.  kvs_cache_restore copies them back and, because evicted
+ * slots of this cache are overwritten, fetches again from the host history every slot whose block
+ * differs from the snapshot's (when the snapshot's slot held a block; rows < ctx_len), so that
+ * state and slot contents are exactly as at the snapshot.  Both are asynchronous and capturable;
+ * the caller orders them after the layer's pending fetches (kvs_join) and restores ctx_len itself.
+ * Restores do not add to the counters. */
+size_t kvs_snapshot_bytes(const kvs_config* cfg);
+kvs_status kvs_cache_snapshot(kvs_ctx* ctx, int layer, void* d_snapshot, kvs_stream_t stream);
+kvs_status kvs_cache_restore(kvs_ctx* ctx, int layer, const void* d_snapshot, const int* d_ctx_len,
+                             kvs_stream_t stream);
 
 /* Exact decode attention over the selected slots [OASIS module 1, HISP insight 1]:
  * out[r][g] = sum_t softmax_t(scale * q[r][g] . k_t) v_t over the tokens t < ctx_len[r] of the

@@ -18,10 +18,11 @@ What it computes, written plainly (numpy, fp64 where the arithmetic is floating 
                OasisKV page, key module 2: lookahead drafts score KV blocks).
   select       sink + recent + top-K by (score desc, block asc) (tuntang.top survey, section
                2.3 SparseSpec-L; section 3 step 1 "topk(k=kv_budget)").
-  cache        hit detection, delta to_load = S_now - resident, LRU victims under a capacity
-               cap, slot assignment, stamps (tuntang.top survey, section 2.1 elastic loading;
-               OasisKV page, key module 3; HiSparse page, insights 1 and 2), and the
-               cross-layer prefetch (HiSparse page, insight 3).
+  cache        hit detection, delta to_load = S_now - resident, LRU (or least-important)
+               victims under a capacity cap, slot assignment, stamps (tuntang.top survey,
+               section 2.1 elastic loading; OasisKV page, key module 3; HiSparse page, insights
+               1 and 2), the cross-layer prefetch (HiSparse page, insight 3), and snapshot /
+               restore for speculative rollback (KV-cache overview, section 6.1).
   attention    exact softmax attention over the selected tokens (OasisKV page, key module 1;
                HiSparse page, insight 1: outputs identical to full KV in HBM).
   step         one decode step over all layers: append, score, select, update, prefetch,
@@ -35,13 +36,14 @@ from .kv_size import kv_cache_bytes, kv_cache_bytes_variant
 from .index_keys import index_keys, index_key_block
 from .scores import block_scores
 from .select import forced_blocks, select_blocks
-from .cache import UnitCache, UpdateResult, PrefetchResult, cache_update, layer_prefetch
+from .cache import (UnitCache, UpdateResult, PrefetchResult, cache_restore, cache_update, importance_key,
+                    layer_prefetch)
 from .attention import attend
 from .step import OracleDecoder, UnitRecord
 
 __all__ = [
     "bf16_to_f32", "bf16_to_f64", "f32_to_bf16_rne", "kv_cache_bytes", "kv_cache_bytes_variant",
     "index_keys", "index_key_block", "block_scores", "forced_blocks", "select_blocks", "UnitCache",
-    "UpdateResult", "PrefetchResult", "cache_update", "layer_prefetch", "attend", "OracleDecoder",
+    "UpdateResult", "PrefetchResult", "cache_update", "cache_restore", "importance_key", "layer_prefetch", "attend", "OracleDecoder",
     "UnitRecord",
 ]

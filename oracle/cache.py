@@ -29,9 +29,23 @@ unit's own update in the same step (HiSparse page, insight 3), with tag = 2 * cl
   and stamp it tag.  A later hit on such a slot (stamp == now - 1 at update) is a
   prefetch hit.
 
+Importance eviction (a policy switch; OasisKV page, key module 3: "evict the least important
+blocks", where the HiSparse page, insight 2, says LRU): step 3 orders the candidates by the
+importance of the block each holds -- the block's score in the scoring that made S (the same
+scores the selection ranked) -- least important first: empty slots first, then NaN scores, then
+ascending score (-0.0 equal to +0.0), ties by slot.  Everything else is unchanged (stamps are
+still assigned, pins and fallback likewise).
+
+Snapshot and restore (speculative rollback; KV-cache overview, section 6.1: the block table is
+saved before the drafts and copied back when they are rejected): a snapshot is a copy of the
+unit's state.  Restoring puts the state back; because this cache overwrites evicted slots, a slot
+whose block differs now from the snapshot's must get the snapshot's block again from the host
+history (when the snapshot's slot was not empty).  The restore returns those (slot, block)
+pairs in slot order.
+
 Pinned by tests/test_oracle_cache.py: hand-worked sequences (tests/golden/cache_*.json), an
 independent second simulator that picks victims by repeated linear min-scan over an
-explicit recency map, and the invariants |R| <= cap, hits + misses = |S|,
+explicit recency (or importance) map, and the invariants |R| <= cap, hits + misses = |S|,
 misses = S - R_before, S within R_after, evicted disjoint from S.
 """
 from dataclasses import dataclass, field
@@ -97,7 +111,24 @@ def _lru_order(c: UnitCache, eligible) -> list:
     return sorted(slots, key=lambda s: (0 if c.slot2block[s] < 0 else int(c.stamp[s]), s))
 
 
-def cache_update(c: UnitCache, sel: np.ndarray, pinned=None) -> UpdateResult:
+def importance_key(score) -> tuple:
+    """Sort key of a block's importance, least important first: NaN below every number, and
+    -0.0 equal to +0.0 (the selection's order, reversed)."""
+    x = float(score)
+    if x != x:
+        return (0, 0.0)
+    return (1, x + 0.0)
+
+
+def _importance_order(c: UnitCache, eligible, scores) -> list:
+    slots = [s for s in range(c.cap) if eligible(s)]
+    return sorted(slots, key=lambda s: ((0, (0, 0.0)) if c.slot2block[s] < 0
+                                        else (1, importance_key(scores[c.slot2block[s]])), s))
+
+
+def cache_update(c: UnitCache, sel: np.ndarray, pinned=None, importance=None) -> UpdateResult:
+    """importance: None for LRU victims, else the fp32 block scores (indexed by block) behind sel:
+    victims are then the least important blocks."""
     sel = np.asarray(sel, np.int64)
     c.clock += 1
     now = 2 * c.clock
@@ -111,10 +142,13 @@ def cache_update(c: UnitCache, sel: np.ndarray, pinned=None) -> UpdateResult:
     def eligible_with(p):
         return lambda s: c.slot2block[s] < 0 or (int(c.slot2block[s]) not in in_sel and int(c.slot2block[s]) not in p)
 
-    cand = _lru_order(c, eligible_with(pins))
+    def order(elig):
+        return _lru_order(c, elig) if importance is None else _importance_order(c, elig, importance)
+
+    cand = order(eligible_with(pins))
     fallback = False
     if len(cand) < len(misses) and pins:
-        cand = _lru_order(c, eligible_with(set()))
+        cand = order(eligible_with(set()))
         fallback = True
     if len(cand) < len(misses):
         raise CapacityError(f"{len(misses)} misses but {len(cand)} victim slots")
@@ -157,3 +191,15 @@ def layer_prefetch(c: UnitCache, hint: np.ndarray, max_prefetch: int) -> Prefetc
         c.stamp[s] = tag
         blocks.append(int(b)); slots.append(int(s)); evicted.append(int(old))
     return PrefetchResult(np.array(blocks, np.int64), np.array(slots, np.int64), np.array(evicted, np.int64))
+
+
+def cache_restore(c: UnitCache, snapshot: UnitCache):
+    """Put c back to the snapshot; returns (slots, blocks) to fetch again from the host history:
+    the slots whose block now differs from the snapshot's, where the snapshot's slot held one."""
+    slots = [s for s in range(c.cap) if c.slot2block[s] != snapshot.slot2block[s] and snapshot.slot2block[s] >= 0]
+    blocks = [int(snapshot.slot2block[s]) for s in slots]
+    c.block2slot[:] = snapshot.block2slot
+    c.slot2block[:] = snapshot.slot2block
+    c.stamp[:] = snapshot.stamp
+    c.clock = snapshot.clock
+    return np.array(slots, np.int64), np.array(blocks, np.int64)

@@ -14,7 +14,10 @@ Per step, layers in order; per (request, kv-head) unit of a layer:
       score with the draft queries' group rows, select S_{t+1}, update with S_t pinned.  The
       first step has no S_t yet and bootstraps it in sync mode from the current query.
 Lookahead mode is defined without append and without prefetch (those combinations are not
-part of this build's workloads).
+part of this build's workloads).  With w.evict_policy == "importance" every update evicts the
+least important blocks by the scores that made its selection (see oracle.cache).  snapshot() and
+restore() save and put back every unit's cache state and pending selection (speculative
+rollback, KV-cache overview, section 6.1).
 
 Parity-relevant outputs are recorded per unit (UnitRecord) and per layer (stats()).
 """
@@ -23,7 +26,7 @@ from dataclasses import dataclass
 import numpy as np
 
 from .attention import attend
-from .cache import PrefetchResult, UnitCache, UpdateResult, cache_update, layer_prefetch
+from .cache import PrefetchResult, UnitCache, UpdateResult, cache_restore, cache_update, layer_prefetch
 from .index_keys import index_key_block, index_keys
 from .scores import block_scores
 from .select import select_blocks
@@ -124,26 +127,40 @@ class OracleDecoder:
                     heads = slice(h * g, (h + 1) * g)
                     qh = q[l, r, heads]
                     boot = None
+                    imp = getattr(w, "evict_policy", "lru") == "importance"
                     if not w.lookahead:
                         s32, a, sel = self._score_select(u, qh)
-                        upd = cache_update(self.cache[u], sel)
+                        upd = cache_update(self.cache[u], sel, importance=s32 if imp else None)
                         attn_sel = sel
                     else:
                         attn_sel = self.pending[u]
                         if attn_sel is None:
                             b32, ba, bsel = self._score_select(u, qh)
-                            bupd = cache_update(self.cache[u], bsel)
+                            bupd = cache_update(self.cache[u], bsel, importance=b32 if imp else None)
                             boot = (b32, ba, bsel, bupd)
                             attn_sel = bsel
                         rows = score_q[l, r, :, heads].reshape(-1, w.d_k)
                         s32, a, sel = self._score_select(u, rows)
-                        upd = cache_update(self.cache[u], sel, pinned=attn_sel)
+                        upd = cache_update(self.cache[u], sel, pinned=attn_sel, importance=s32 if imp else None)
                         self.pending[u] = sel
                     kt, vt = self.tokens(u, attn_sel)
                     out[l, ri, heads] = attend(qh, kt, vt, w.softmax_scale)
                     recs[u] = UnitRecord(attn_sel, sel, s32, a, upd, boot, pf, self.L[r])
         self.records = recs
         return out, recs
+
+    def snapshot(self, layer=None):
+        """Copies of the cache state and pending selection of every unit (of one layer)."""
+        return {u: (c.copy(), None if self.pending[u] is None else self.pending[u].copy())
+                for u, c in self.cache.items() if layer is None or u[0] == layer}
+
+    def restore(self, snap):
+        """Put the units of a snapshot back; returns {unit: (slots, blocks)} to fetch again."""
+        out = {}
+        for u, (c, pend) in snap.items():
+            out[u] = cache_restore(self.cache[u], c)
+            self.pending[u] = None if pend is None else pend.copy()
+        return out
 
     def fetched_rows(self, r: int, blocks) -> int:
         bs, L = self.w.block_size, self.L[r]

@@ -32,7 +32,9 @@ class KvsConfig(ctypes.Structure):
                 ("budget_blocks", ctypes.c_int), ("n_sink", ctypes.c_int), ("n_recent", ctypes.c_int),
                 ("cap_blocks", ctypes.c_int), ("max_score_q", ctypes.c_int), ("lookahead", ctypes.c_int),
                 ("max_prefetch", ctypes.c_int), ("softmax_scale", ctypes.c_float),
-                ("wait_timeout_us", ctypes.c_uint)]
+                ("wait_timeout_us", ctypes.c_uint), ("evict_policy", ctypes.c_int)]
+
+EVICT_POLICY = {"lru": 0, "importance": 1}
 
 
 class KvsStats(ctypes.Structure):
@@ -55,7 +57,10 @@ _SIGS = {
     "kvs_index_build": (_I, [_P, _I, _P, _P, _P]),
     "kvs_score_blocks": (_I, [_P, _I, _P, _I, _P, _P, _P, _P]),
     "kvs_topk_select": (_I, [_P, _P, _P, _P, _P, _P]),
-    "kvs_cache_update": (_I, [_P, _I, _P, _P, _P, _P, _P, _P]),
+    "kvs_cache_update": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "kvs_snapshot_bytes": (ctypes.c_size_t, [ctypes.POINTER(KvsConfig)]),
+    "kvs_cache_snapshot": (_I, [_P, _I, _P, _P]),
+    "kvs_cache_restore": (_I, [_P, _I, _P, _P, _P]),
     "kvs_sparse_decode_attn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P]),
     "kvs_decode_step": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "kvs_join": (_I, [_P, _P]),
@@ -114,7 +119,7 @@ def make_config(w, max_score_q: int | None = None, max_prefetch: int = 0, wait_t
     return KvsConfig(w.n_req, w.n_layer, w.n_q_head, w.n_kv_head, w.d_k, w.d_v, int(w.v_shares_k), w.block_size,
                      w.max_ctx, w.budget_blocks, w.n_sink, w.n_recent, w.cap_blocks,
                      max_score_q if max_score_q is not None else max(1, w.n_score_q), int(w.lookahead), max_prefetch,
-                     float(w.softmax_scale), wait_timeout_us)
+                     float(w.softmax_scale), wait_timeout_us, EVICT_POLICY[getattr(w, "evict_policy", "lru")])
 
 
 class Context:
@@ -164,9 +169,19 @@ class Context:
         _check(self.L.kvs_topk_select(self.h, _ptr(scores), _ptr(ctx_len), _ptr(sel), _ptr(nsel), _stream(stream)),
                "kvs_topk_select")
 
-    def cache_update(self, layer, sel, nsel, ctx_len, slot_of_sel, stats=None, stream=None):
+    def cache_update(self, layer, sel, nsel, ctx_len, slot_of_sel, stats=None, stream=None, scores=None):
         _check(self.L.kvs_cache_update(self.h, layer, _ptr(sel), _ptr(nsel), _ptr(ctx_len), _ptr(slot_of_sel),
-                                       _ptr(stats), _stream(stream)), "kvs_cache_update")
+                                       _ptr(scores), _ptr(stats), _stream(stream)), "kvs_cache_update")
+
+    def snapshot_bytes(self) -> int:
+        return int(self.L.kvs_snapshot_bytes(ctypes.byref(self.cfg)))
+
+    def cache_snapshot(self, layer, snap, stream=None):
+        _check(self.L.kvs_cache_snapshot(self.h, layer, _ptr(snap), _stream(stream)), "kvs_cache_snapshot")
+
+    def cache_restore(self, layer, snap, ctx_len, stream=None):
+        _check(self.L.kvs_cache_restore(self.h, layer, _ptr(snap), _ptr(ctx_len), _stream(stream)),
+               "kvs_cache_restore")
 
     def sparse_decode_attn(self, layer, q, sel, slot_of_sel, nsel, ctx_len, out, stream=None):
         _check(self.L.kvs_sparse_decode_attn(self.h, layer, _ptr(q), _ptr(sel), _ptr(slot_of_sel), _ptr(nsel),

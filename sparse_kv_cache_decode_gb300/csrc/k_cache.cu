@@ -114,7 +114,8 @@ __device__ __forceinline__ unsigned long long fetch_rows(const Dims& d, int len,
 __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Layer L, const int* __restrict__ sel,
                                                                      const int* __restrict__ nsel,
                                                                      const int* __restrict__ ctx_len,
-                                                                     int* __restrict__ slot_of_sel, kvs_stats* stats) {
+                                                                     int* __restrict__ slot_of_sel,
+                                                                     const float* __restrict__ imp, kvs_stats* stats) {
   kvs_pdl_entry();
   extern __shared__ __align__(16) unsigned char smraw[];
   __shared__ int hist[256];
@@ -216,9 +217,17 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
   // accepted: a refused update (bad index, capacity) leaves the unit's state as it was
   if (tid == 0) L.clock[u] = now / 2u;
   const uint8_t emask = fallback ? 1 : 3;
+  // victim keys, smallest first: empty slots 0; LRU: the stamp (>= 2); importance: 1 + the
+  // orderable key of the held block's score (NaN lowest), so the least important go first
+  const float* imp_u = imp ? imp + (size_t)u * d.nb_max : nullptr;
   select_victims(
       d.C, m, [&](int s) { return (sm.flags[s] & emask) == 0; },
-      [&](int s) { return s2b[s] < 0 ? 0u : st[s]; }, hist, ws, pick, sm);
+      [&](int s) {
+        const int b = s2b[s];
+        if (b < 0) return 0u;
+        return imp_u ? score_key(imp_u[b]) + 1u : st[s];
+      },
+      hist, ws, pick, sm);
 
   unsigned long long my_ev = 0, my_bytes = 0;
   for (int j = tid; j < m; j += NT) {
@@ -352,6 +361,66 @@ __global__ void __launch_bounds__(kCacheThreads) prefetch_kernel(Dims d, Layer L
   }
 }
 
+// Restore of one unit from a snapshot (one CTA per unit): the slots whose block differs from the
+// snapshot's (where the snapshot's slot held a block) go to the unit's fetch list in slot order,
+// then the snapshot's maps, stamps, clock and pending selection are copied back.  A snapshot
+// block id outside [-1, n_b(max_ctx)) is reported (KVS_ERR_BAD_INDEX) and not fetched.
+constexpr int kRestoreThreads = 256;
+
+__global__ void __launch_bounds__(kRestoreThreads) restore_kernel(Dims d, Layer L, const unsigned char* __restrict__ snap,
+                                                                  SnapshotPlan p) {
+  kvs_pdl_entry();
+  __shared__ int ws[33];
+  const int u = blockIdx.x, tid = threadIdx.x, NT = blockDim.x;
+  const int* sb2s = reinterpret_cast<const int*>(snap) + (size_t)u * d.nb_max;
+  const int* ss2b = reinterpret_cast<const int*>(snap + p.b2s) + (size_t)u * d.C;
+  const unsigned* sst = reinterpret_cast<const unsigned*>(snap + p.b2s + p.s2b) + (size_t)u * d.C;
+  const unsigned* sclk = reinterpret_cast<const unsigned*>(snap + p.b2s + p.s2b + p.stamp);
+  const int* spsel = reinterpret_cast<const int*>(snap + p.b2s + p.s2b + p.stamp + p.clock) + (size_t)u * d.Kb;
+  const int* spslot =
+      reinterpret_cast<const int*>(snap + p.b2s + p.s2b + p.stamp + p.clock + p.pend_sel) + (size_t)u * d.Kb;
+  const int* spn = reinterpret_cast<const int*>(snap + p.b2s + p.s2b + p.stamp + p.clock + p.pend_sel + p.pend_slot);
+  int* b2s = L.block2slot + (size_t)u * d.nb_max;
+  int* s2b = L.slot2block + (size_t)u * d.C;
+  unsigned* st = L.stamp + (size_t)u * d.C;
+  const int per = (d.C + NT - 1) / NT;
+  const int s0 = min(d.C, tid * per), s1 = min(d.C, s0 + per);
+  auto needs = [&](int s) {
+    const int want = ss2b[s];
+    if (want < -1 || want >= d.nb_max) {
+      set_error(L.err, KVS_ERR_BAD_INDEX);
+      return false;
+    }
+    return want >= 0 && s2b[s] != want;
+  };
+  int mine = 0;
+  for (int s = s0; s < s1; ++s) mine += needs(s);
+  int total;
+  int pos = block_excl_sum(mine, ws, &total);
+  for (int s = s0; s < s1; ++s) {
+    if (!needs(s)) continue;
+    L.fetch_blk[(size_t)u * d.C + pos] = ss2b[s];
+    L.fetch_slot[(size_t)u * d.C + pos] = s;
+    ++pos;
+  }
+  __syncthreads();   // every read of the live slot map is done before it is overwritten
+  for (int i = tid; i < d.nb_max; i += NT) b2s[i] = sb2s[i];
+  for (int s = tid; s < d.C; s += NT) {
+    s2b[s] = ss2b[s];
+    st[s] = sst[s];
+  }
+  for (int i = tid; i < d.Kb; i += NT) {
+    L.pend_sel[(size_t)u * d.Kb + i] = spsel[i];
+    L.pend_slot[(size_t)u * d.Kb + i] = spslot[i];
+  }
+  if (tid == 0) {
+    L.clock[u] = sclk[u];
+    L.pend_n[u] = spn[u];
+    L.next_commit[u] = 0;
+    L.n_fetch[u] = total;
+  }
+}
+
 // Zero-copy fetch with a small persistent grid, so that it leaves the SMs to the compute
 // kernels that run beside it: the CTAs flatten the (unit, item) lists with a prefix sum over
 // units; each warp copies batches of whole items (about 512 16-byte vectors per batch), 16 loads
@@ -462,13 +531,14 @@ __global__ void __launch_bounds__(kFetchThreads) fetch_kernel(Dims d, Layer L, c
 }  // namespace
 
 cudaError_t launch_cache_update(const Dims& d, const Layer& L, const int* sel, const int* nsel, const int* ctx_len,
-                                int* slot_of_sel, kvs_stats* stats, cudaStream_t s) {
+                                int* slot_of_sel, const float* scores, kvs_stats* stats, cudaStream_t s) {
   size_t smem = cache_smem_bytes(d);
   if (smem > 48 * 1024) {
     cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(cache_update_kernel), (int)smem);
     if (e != cudaSuccess) return e;
   }
-  launch_pdl(cache_update_kernel, dim3(d.U), dim3(kCacheThreads), smem, s, d, L, sel, nsel, ctx_len, slot_of_sel, stats);
+  launch_pdl(cache_update_kernel, dim3(d.U), dim3(kCacheThreads), smem, s, d, L, sel, nsel, ctx_len, slot_of_sel, scores,
+             stats);
   return cudaGetLastError();
 }
 
@@ -480,6 +550,26 @@ cudaError_t launch_prefetch(const Dims& d, const Layer& L, const int* hint, cons
     if (e != cudaSuccess) return e;
   }
   launch_pdl(prefetch_kernel, dim3(d.U), dim3(kCacheThreads), smem, s, d, L, hint, hint_n, ctx_len, stats);
+  return cudaGetLastError();
+}
+
+SnapshotPlan snapshot_plan(const Dims& d) {
+  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  SnapshotPlan p;
+  const size_t U = d.U;
+  p.b2s = al(U * d.nb_max * 4);
+  p.s2b = al(U * d.C * 4);
+  p.stamp = al(U * d.C * 4);
+  p.clock = al(U * 4);
+  p.pend_sel = al(U * d.Kb * 4);
+  p.pend_slot = al(U * d.Kb * 4);
+  p.pend_n = al(U * 4);
+  p.total = p.b2s + p.s2b + p.stamp + p.clock + p.pend_sel + p.pend_slot + p.pend_n;
+  return p;
+}
+
+cudaError_t launch_restore(const Dims& d, const Layer& L, const unsigned char* snap, cudaStream_t s) {
+  launch_pdl(restore_kernel, dim3(d.U), dim3(kRestoreThreads), 0, s, d, L, snap, snapshot_plan(d));
   return cudaGetLastError();
 }
 

@@ -75,6 +75,7 @@ bool fill_dims(const kvs_config* c, Dims* d) {
   if (c->lookahead != 0 && c->lookahead != 1) return false;
   if (c->max_prefetch < 0 || c->max_prefetch > c->cap_blocks - c->budget_blocks) return false;
   if (!(c->softmax_scale >= 0.f) || isinf(c->softmax_scale)) return false;
+  if (c->evict_policy != KVS_EVICT_LRU && c->evict_policy != KVS_EVICT_IMPORTANCE) return false;
   d->B = c->n_req;
   d->NL = c->n_layer;
   d->Hq = c->n_q_head;
@@ -97,6 +98,7 @@ bool fill_dims(const kvs_config* c, Dims* d) {
   d->scale = c->softmax_scale > 0.f ? c->softmax_scale : (float)(1.0 / sqrt((double)c->d_k));
   d->timeout_us = c->wait_timeout_us ? c->wait_timeout_us : 2000000u;
   d->row_bytes = 2 * (c->d_k + (c->v_shares_k ? 0 : c->d_v));
+  d->evict_importance = c->evict_policy == KVS_EVICT_IMPORTANCE;
   return true;
 }
 
@@ -515,12 +517,53 @@ kvs_status kvs_topk_select(kvs_ctx* c, const float* d_scores, const int* d_ctx_l
 }
 
 kvs_status kvs_cache_update(kvs_ctx* c, int layer, const int* d_sel, const int* d_nsel, const int* d_ctx_len,
-                            int* d_slot_of_sel, kvs_stats* d_stats, kvs_stream_t stream) {
+                            int* d_slot_of_sel, const float* d_scores, kvs_stats* d_stats, kvs_stream_t stream) {
   if (!layer_ok(c, layer) || !d_sel || !d_nsel || !d_ctx_len || !d_slot_of_sel) return KVS_ERR_INVALID_ARG;
+  if (c->d.evict_importance && !d_scores) return KVS_ERR_INVALID_ARG;
   if (!c->host_k_dev) return KVS_ERR_HOST_MEM;
   const Layer& L = c->layers[layer];
   cudaError_t e = timed(c, KVS_K_UPDATE, S(stream), 1, [&] {
-    return launch_cache_update(c->d, L, d_sel, d_nsel, d_ctx_len, d_slot_of_sel, d_stats, S(stream));
+    return launch_cache_update(c->d, L, d_sel, d_nsel, d_ctx_len, d_slot_of_sel,
+                               c->d.evict_importance ? d_scores : nullptr, d_stats, S(stream));
+  });
+  if (e == cudaSuccess) e = timed(c, KVS_K_FETCH, S(stream), 1, [&] { return launch_fetch(c->d, L, d_ctx_len, S(stream)); });
+  return cuda_status(e);
+}
+
+size_t kvs_snapshot_bytes(const kvs_config* cfg) {
+  Dims d;
+  if (!fill_dims(cfg, &d)) return 0;
+  return snapshot_plan(d).total;
+}
+
+kvs_status kvs_cache_snapshot(kvs_ctx* c, int layer, void* d_snapshot, kvs_stream_t stream) {
+  if (!layer_ok(c, layer) || !d_snapshot || (reinterpret_cast<uintptr_t>(d_snapshot) % kAlign)) return KVS_ERR_INVALID_ARG;
+  const Dims& d = c->d;
+  const Layer& L = c->layers[layer];
+  const SnapshotPlan p = snapshot_plan(d);
+  unsigned char* o = static_cast<unsigned char*>(d_snapshot);
+  const size_t U = d.U;
+  struct Part { void* dst; const void* src; size_t n; } parts[] = {
+      {o, L.block2slot, U * d.nb_max * 4},
+      {o + p.b2s, L.slot2block, U * d.C * 4},
+      {o + p.b2s + p.s2b, L.stamp, U * d.C * 4},
+      {o + p.b2s + p.s2b + p.stamp, L.clock, U * 4},
+      {o + p.b2s + p.s2b + p.stamp + p.clock, L.pend_sel, U * d.Kb * 4},
+      {o + p.b2s + p.s2b + p.stamp + p.clock + p.pend_sel, L.pend_slot, U * d.Kb * 4},
+      {o + p.b2s + p.s2b + p.stamp + p.clock + p.pend_sel + p.pend_slot, L.pend_n, U * 4}};
+  for (const Part& x : parts)
+    if (cudaMemcpyAsync(x.dst, x.src, x.n, cudaMemcpyDeviceToDevice, S(stream)) != cudaSuccess) return KVS_ERR_CUDA;
+  return KVS_OK;
+}
+
+kvs_status kvs_cache_restore(kvs_ctx* c, int layer, const void* d_snapshot, const int* d_ctx_len,
+                             kvs_stream_t stream) {
+  if (!layer_ok(c, layer) || !d_snapshot || !d_ctx_len || (reinterpret_cast<uintptr_t>(d_snapshot) % kAlign))
+    return KVS_ERR_INVALID_ARG;
+  if (!c->host_k_dev) return KVS_ERR_HOST_MEM;
+  const Layer& L = c->layers[layer];
+  cudaError_t e = timed(c, KVS_K_UPDATE, S(stream), 1, [&] {
+    return launch_restore(c->d, L, static_cast<const unsigned char*>(d_snapshot), S(stream));
   });
   if (e == cudaSuccess) e = timed(c, KVS_K_FETCH, S(stream), 1, [&] { return launch_fetch(c->d, L, d_ctx_len, S(stream)); });
   return cuda_status(e);
@@ -620,7 +663,8 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
     }
     if (r != cudaSuccess) return r;
     return timed(c, KVS_K_UPDATE, ss, 1,
-                 [&] { return launch_cache_update(d, L, so, no, d_ctx_len, L.slot_of_sel, d_stats, ss); });
+                 [&] { return launch_cache_update(d, L, so, no, d_ctx_len, L.slot_of_sel,
+                                                  d.evict_importance ? L.scores : nullptr, d_stats, ss); });
   };
   auto fetch = [&](cudaStream_t fs) {
     return timed(c, KVS_K_FETCH, fs, 1, [&] { return launch_fetch(d, L, d_ctx_len, fs); });

@@ -16,6 +16,7 @@ struct Dims {
   int dk, dv, v_shares_k;
   int bs, max_ctx, nb_max;
   int Kb, n_sink, n_recent, C, max_nq, lookahead, max_prefetch;
+  int evict_importance;  // victims least important first (else least recently used)
   int U;                 // units per layer = B * Hkv
   float scale;
   unsigned timeout_us;
@@ -121,7 +122,13 @@ int topk_chunks(const Dims& d);   // P, or 0 when one pass per unit is used
 cudaError_t launch_topk(const Dims& d, const float* scores, const int* ctx_len, int* sel, int* nsel,
                         unsigned* err, cudaStream_t s, const TopkScratch* scratch);
 cudaError_t launch_cache_update(const Dims& d, const Layer& L, const int* sel, const int* nsel, const int* ctx_len,
-                                int* slot_of_sel, kvs_stats* stats, cudaStream_t s);
+                                int* slot_of_sel, const float* scores, kvs_stats* stats, cudaStream_t s);
+// Restore a layer's cache state from a snapshot (per-unit refetch list, then the maps).
+struct SnapshotPlan {
+  size_t b2s, s2b, stamp, clock, pend_sel, pend_slot, pend_n, total;
+};
+SnapshotPlan snapshot_plan(const Dims& d);
+cudaError_t launch_restore(const Dims& d, const Layer& L, const unsigned char* snap, cudaStream_t s);
 cudaError_t launch_prefetch(const Dims& d, const Layer& L, const int* hint, const int* hint_n, const int* ctx_len,
                             kvs_stats* stats, cudaStream_t s);
 cudaError_t launch_fetch(const Dims& d, const Layer& L, const int* ctx_len, cudaStream_t s);

@@ -27,6 +27,10 @@ INT_CASES = [
                       steps=12), [4096], False),
     (W.TINY.with_(name="tiny_bs64_int", n_req=2, block_size=64, ctx0=4000, budget_blocks=8, cap_blocks=10,
                   int_scale=2.0), [4000, 3900], False),
+    # least-important-first eviction by the step's block scores
+    (W.TINY.with_(name="tiny_imp_int", n_req=2, int_scale=2.0, evict_policy="importance"), [4096, 3001], False),
+    (W.TINY_LOOKAHEAD.with_(name="tiny_la_imp_int_cs", n_req=2, int_scale=2.0, evict_policy="importance"),
+     [4096, 2050], True),
 ]
 
 

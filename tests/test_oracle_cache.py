@@ -1,12 +1,13 @@
 """Pins for oracle.cache: hand-worked sequences, an independent second simulator, invariants."""
 import json
+import math
 import os
 
 import numpy as np
 import pytest
 
 from conftest import GOLDEN
-from oracle import UnitCache, cache_update, layer_prefetch
+from oracle import UnitCache, cache_restore, cache_update, layer_prefetch
 
 
 def _golden():
@@ -48,6 +49,62 @@ def test_hand_worked_prefetch():
     assert c.stamp.tolist() == p["after_update_stamp"]
 
 
+def test_hand_worked_importance_eviction():
+    with open(os.path.join(GOLDEN, "cache_importance.json")) as f:
+        g = json.load(f)
+    c = UnitCache(g["cap"], g["n_blocks"])
+    for i, st in enumerate(g["steps"]):
+        scores = np.zeros(g["n_blocks"], np.float32)
+        for b, v in st["scores"].items():
+            scores[int(b)] = float(v)
+        r = cache_update(c, np.array(st["sel"]), importance=scores)
+        where = f"step {i + 1}: {st['note']}"
+        assert r.misses.tolist() == st["misses"], where
+        assert r.victim_slots.tolist() == st["victims"], where
+        assert r.evicted.tolist() == st["evicted"], where
+        assert c.slot2block.tolist() == st["slot2block"], where
+
+
+def test_hand_worked_restore():
+    with open(os.path.join(GOLDEN, "cache_restore.json")) as f:
+        g = json.load(f)
+    c = UnitCache(g["cap"], g["n_blocks"])
+    for sel in g["before"]:
+        cache_update(c, np.array(sel))
+    snap = c.copy()
+    assert snap.slot2block.tolist() == g["snapshot"]["slot2block"] and snap.clock == g["snapshot"]["clock"]
+    assert snap.stamp.tolist() == g["snapshot"]["stamp"]
+    for sel in g["after"]:
+        cache_update(c, np.array(sel))
+    st = g["state_before_restore"]
+    assert c.slot2block.tolist() == st["slot2block"] and c.stamp.tolist() == st["stamp"] and c.clock == st["clock"]
+    slots, blocks = cache_restore(c, snap)
+    assert slots.tolist() == g["refetch_slots"] and blocks.tolist() == g["refetch_blocks"]
+    assert c.slot2block.tolist() == snap.slot2block.tolist() and c.stamp.tolist() == snap.stamp.tolist()
+    assert c.block2slot.tolist() == snap.block2slot.tolist() and c.clock == snap.clock
+
+
+def test_restore_properties():
+    """After any sequence, restore returns the snapshot's state exactly, and the refetched slots
+    are exactly those whose block changed (a planted restore that skips moved blocks fails here)."""
+    rng = np.random.default_rng(7)
+    for trial in range(20):
+        nblk, budget = 40, int(rng.integers(2, 7))
+        cap = budget + int(rng.integers(0, 5))
+        c = UnitCache(cap, nblk)
+        for _ in range(int(rng.integers(1, 6))):
+            cache_update(c, np.sort(rng.choice(nblk, budget, replace=False)))
+        snap = c.copy()
+        for _ in range(int(rng.integers(0, 6))):
+            cache_update(c, np.sort(rng.choice(nblk, budget, replace=False)))
+        cur = c.slot2block.copy()
+        slots, blocks = cache_restore(c, snap)
+        assert sorted(slots.tolist()) == slots.tolist()
+        want = [s for s in range(cap) if cur[s] != snap.slot2block[s] and snap.slot2block[s] >= 0]
+        assert slots.tolist() == want and blocks.tolist() == [int(snap.slot2block[s]) for s in want]
+        assert c.slot2block.tolist() == snap.slot2block.tolist() and c.block2slot.tolist() == snap.block2slot.tolist()
+
+
 class SecondSim:
     """Independent formulation: each slot remembers its block and the time of its last use
     (decode step number; a prefetch made before step n+1 counts as time n + 0.5); victims
@@ -69,7 +126,21 @@ class SecondSim:
                 best = (key, s)
         return None if best is None else best[1]
 
-    def update(self, sel, pins):
+    def _least_important(self, eligible, taken, score):
+        best = None
+        for s in range(self.cap):
+            if s in taken or not eligible(s):
+                continue
+            if self.block[s] is None:
+                key = (-2, 0.0, s)
+            else:
+                v = float(score[self.block[s]])
+                key = (-1, 0.0, s) if math.isnan(v) else (0, v + 0.0, s)
+            if best is None or key < best[0]:
+                best = (key, s)
+        return None if best is None else best[1]
+
+    def update(self, sel, pins, importance=None):
         self.n += 1
         where = {b: s for s, b in enumerate(self.block) if b is not None}
         misses = [b for b in sel if b not in where]
@@ -78,7 +149,9 @@ class SecondSim:
         def run(pset):
             taken, out = set(), []
             for _ in misses:
-                s = self._oldest(lambda s: self.block[s] is None or (self.block[s] not in sset and self.block[s] not in pset), taken)
+                elig = (lambda s: self.block[s] is None or (self.block[s] not in sset and self.block[s] not in pset))
+                s = (self._oldest(elig, taken) if importance is None
+                     else self._least_important(elig, taken, importance))
                 if s is None:
                     return None
                 taken.add(s)
@@ -151,4 +224,29 @@ def test_against_second_simulator(seed, lookahead, prefetch):
             assert set(prev.tolist()) <= after
         assert all(c.block2slot[b] == s for s, b in enumerate(c.slot2block) if b >= 0)
         assert int((c.block2slot >= 0).sum()) == len(after)
+        prev = cur
+
+
+@pytest.mark.parametrize("seed,lookahead", [(s, la) for s in range(4) for la in (False, True)])
+def test_importance_against_second_simulator(seed, lookahead):
+    """Importance eviction against the linear-scan simulator, with scores that tie, include -0.0
+    and +0.0, and NaN."""
+    rng = np.random.default_rng(300 + seed)
+    nblk, budget = 50, int(rng.integers(3, 8))
+    cap = budget + int(rng.integers(1, 6))
+    c, sim = UnitCache(cap, nblk), SecondSim(cap)
+    prev = None
+    cur = np.sort(rng.choice(nblk, budget, replace=False))
+    for step in range(50):
+        keep = cur[rng.random(len(cur)) < 0.6]
+        fresh = rng.choice(np.setdiff1d(np.arange(nblk), keep), budget - len(keep), replace=False)
+        cur = np.sort(np.concatenate([keep, fresh]))
+        scores = rng.integers(-3, 4, nblk).astype(np.float32)
+        scores[rng.random(nblk) < 0.1] = np.nan
+        scores[rng.random(nblk) < 0.1] = -0.0
+        pins = prev if lookahead else None
+        r = cache_update(c, cur, pins, importance=scores)
+        misses, victims, fb = sim.update(cur.tolist(), None if pins is None else pins.tolist(), importance=scores)
+        assert r.misses.tolist() == misses and r.victim_slots.tolist() == victims and r.pin_fallback == fb
+        assert [b if b is not None else -1 for b in sim.block] == c.slot2block.tolist()
         prev = cur

@@ -134,6 +134,7 @@ class Workload:
     seed: int = 0
     int_scale: float = 0.0   # > 0: integer-valued inputs round(x * int_scale), clipped (exact fp32 scores)
     int_clip: float = 7.0
+    evict_policy: str = "lru"   # "lru" or "importance" (least important block first)
     notes: str = ""
 
     @property
