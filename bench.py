@@ -405,6 +405,42 @@ def dense_softmax_coverage(ws, dec, q):
             "sample": f"oracle, last step of the CPU-baseline sample, layer 0 of request 0, {len(shares)} q heads"}
 
 
+def coverage_study(w, q):
+    """Dense-softmax coverage of the selection each block-scoring rule makes, on request 0, layer 0,
+    every kv head, with the step's current query (oracle, fp64; outside any timed region): the share
+    of the exact attention mass over all present tokens that the selected tokens carry, mean and
+    minimum over the q heads.  Rules: the block-mean key ("mean"), the [max | min] upper bound
+    ("bound"), and two references that need every key: the block's largest token logit
+    ("token_max") and the block's exact softmax mass ("mass", the best any block selection can do)."""
+    from oracle import bf16_to_f64, block_scores, block_scores_bound, index_keys, index_minmax, select_blocks
+    ws = w.with_(n_req=1, n_layer=1)
+    k, _ = W.kv_numpy(ws)
+    g, bs, L = ws.group, ws.block_size, ws.ctx0
+    nb = (L + bs - 1) // bs
+    cov = {m: [] for m in ("mean", "bound", "token_max", "mass")}
+    for h in range(ws.n_kv_head):
+        kr = k[0, 0, h, :L]
+        rows = q[0, 0, h * g:(h + 1) * g]
+        logits = float(ws.softmax_scale) * (bf16_to_f64(rows) @ bf16_to_f64(kr).T)      # (G, L)
+        p = np.exp(logits - logits.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        pad = nb * bs - L
+        lp = np.pad(logits, ((0, 0), (0, pad)), constant_values=-np.inf).reshape(g, nb, bs)
+        mass = np.pad(p, ((0, 0), (0, pad))).reshape(g, nb, bs).sum(axis=2)
+        scores = {"mean": block_scores(rows, index_keys(kr, L, bs), ws.softmax_scale)[0],
+                  "bound": block_scores_bound(rows, index_minmax(kr, L, bs), ws.softmax_scale)[0],
+                  "token_max": lp.max(axis=2).max(axis=0),
+                  "mass": mass.max(axis=0)}
+        for m, sc in scores.items():
+            sel = select_blocks(sc.astype(np.float32), nb, ws.budget_blocks, ws.n_sink, ws.n_recent)
+            taken = np.zeros(nb, bool)
+            taken[sel] = True
+            cov[m] += list(mass[:, taken].sum(axis=1))
+    return {m: {"value": round(float(np.mean(v)), 4), "min": round(float(np.min(v)), 4)} for m, v in cov.items()} | {
+        "sample": f"oracle, request 0, layer 0, {ws.n_kv_head} kv heads x {g} q heads, the step's own query scoring, "
+                  f"budget {ws.budget_blocks} blocks of {bs}"}
+
+
 def run_reference(args, dist):
     if dist.rank != 0:
         return 0
@@ -592,7 +628,7 @@ def run_point(args, dist, w, hist, link, e2e: bool, cpu_baseline: bool):
     ctx.bind_host_kv(hist.k, hist.v)
     lens = [w.ctx0] * B
     ctx_len = torch.tensor(lens, dtype=torch.int32, device="cuda")
-    index = torch.zeros((NL, B, Hkv, w.max_blocks, w.d_k), dtype=torch.int16, device="cuda")
+    index = torch.zeros((NL, B, Hkv, w.max_blocks, w.d_idx), dtype=torch.int16, device="cuda")
     for l in range(NL):
         ctx.index_build(l, index, ctx_len)
     torch.cuda.synchronize()
@@ -814,6 +850,7 @@ def run_point(args, dist, w, hist, link, e2e: bool, cpu_baseline: bool):
         line["cpu_baseline"] = {"value": round(1.0 / full, 6), "unit": UNIT, "cores": cores, "cpu": cpu_model(),
                                 "kind": "oracle", "sample": desc}
         line["dense_softmax_coverage"] = coverage
+        line["coverage_study"] = coverage_study(w, q_all[0].numpy().view(np.uint16))
     ctx.close()
     del index, q_dev, d_dev, tok_dev
     torch.cuda.empty_cache()
@@ -884,6 +921,10 @@ def workload_of(args, name, dist):
     return w
 
 
+# Policy variants of the headline workload, measured on its history: the [max | min] upper-bound
+# block score, and least-important-first eviction.
+VARIANTS = {"score_mode=bound": {"score_mode": "bound"}, "evict_policy=importance": {"evict_policy": "importance"}}
+
 SUMMARY_KEYS = ("value", "ms_per_step", "effective_kv_gbs", "step_roofline", "dependency_bound", "achieved_overlap",
                 "miss_fraction", "prefetch", "roofline", "kernel_ms_per_step", "clocks", "gpu_launches", "host_memory")
 
@@ -938,6 +979,12 @@ def run_ours(args, dist):
     line = run_point(args, dist, w, hist, link, e2e=not args.no_e2e,
                      cpu_baseline=not args.no_cpu_baseline and not args.child)
     line["link_peak"] = link.get()
+    if dist.rank == 0 and dist.world == 1 and not args.child and not args.no_per_config:
+        line["variants"] = {}
+        for vname, kw in VARIANTS.items():
+            j = run_point(args, dist, w.with_(name=f"{w.name}_{vname.split('=')[1]}", **kw), hist, link, e2e=False,
+                          cpu_baseline=False)
+            line["variants"][vname] = {k: j[k] for k in SUMMARY_KEYS if k in j}
     line["host_vmstat_delta"] = hist.vmstat_delta()
     hist.close()
     del hist

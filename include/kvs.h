@@ -26,7 +26,8 @@
  * Layouts (row-major, bf16 = 16-bit patterns):
  *   host K      [N_l][B][H_kv][max_ctx][d_k]      pinned, device-mapped (see kvs_bind_host_kv)
  *   host V      [N_l][B][H_kv][max_ctx][d_v]      absent when v_shares_k (V = first d_v of K row)
- *   index       [N_l][B][H_kv][n_b(max_ctx)][d_k] device; block-mean keys (kvs_index_build)
+ *   index       [N_l][B][H_kv][n_b(max_ctx)][d_idx] device; block summaries (kvs_index_build):
+ *                                                 d_idx = d_k (mean key) or 2 d_k ([max | min])
  *   q           [B][H_q][d_k]                     one layer's attention queries
  *   score_q     [B][nq][H_q][d_k]                 one layer's scoring queries (drafts)
  *   scores      [B][H_kv][n_b(max_ctx)] fp32      one layer's block scores
@@ -88,7 +89,15 @@ typedef struct {
   float softmax_scale; /* 0 -> 1/sqrt(d_k) rounded to fp32 */
   unsigned wait_timeout_us; /* bound on device waits (0 -> 2000000 us) */
   int evict_policy;    /* KVS_EVICT_LRU (0) or KVS_EVICT_IMPORTANCE (1) [OASIS module 3, HISP insight 2] */
+  int score_mode;      /* KVS_SCORE_MEAN (0) or KVS_SCORE_BOUND (1): how blocks are summarised and scored */
 } kvs_config;
+
+/* Block summaries and scores.  MEAN: the index row of a block is its mean key (d_idx = d_k) and
+ * the score is the mean token logit q . ik.  BOUND: the index row is [max | min] of its present
+ * keys per dimension (d_idx = 2 d_k, exact bf16) and the score is the query-aware upper bound
+ * sum_d max(q_d max_d, q_d min_d) of the block's largest token logit (the Quest rule; the pages
+ * name Quest among the selector families the host-KV cache serves [HISP insight 1]). */
+enum { KVS_SCORE_MEAN = 0, KVS_SCORE_BOUND = 1 };
 
 /* Victim order of the cache update.  LRU: least recently used first, by (stamp, slot).
  * IMPORTANCE: least important first: the block's score in the scoring that made the selection
@@ -122,14 +131,16 @@ kvs_status kvs_destroy(kvs_ctx* ctx);
  * where the device could reach it). */
 kvs_status kvs_bind_host_kv(kvs_ctx* ctx, void* h_k, void* h_v);
 
-/* Build the block-mean index keys of one layer from the host history (setup after prefill):
- * ik[b] = bf16_rne( (sum over present tokens t of block b, ascending, of fp32 k_t) / n_b ).
- * Reading of [OASIS module 2] "per-block importance": by linearity q.ik[b] is the block's mean
- * token logit.  Blocks >= n_b(ctx_len[r]) are left untouched. */
+/* Build the block summaries of one layer from the host history (setup after prefill).  MEAN:
+ * ik[b] = bf16_rne( (sum over present tokens t of block b, ascending, of fp32 k_t) / n_b ); reading
+ * of [OASIS module 2] "per-block importance": by linearity q.ik[b] is the block's mean token logit.
+ * BOUND: ik[b] = [max_t k_t | min_t k_t] per dimension over the present tokens (ties keep the
+ * earliest token's value).  Blocks >= n_b(ctx_len[r]) are left untouched. */
 kvs_status kvs_index_build(kvs_ctx* ctx, int layer, void* d_index, const int* d_ctx_len, kvs_stream_t stream);
 
 /* Block scores of one layer [SPEC 3 step 3, OASIS module 2]:
- * s[r][h][b] = scale * max over j < nq and q heads g of group h of (score_q[r][j][g] . ik[b]),
+ * s[r][h][b] = scale * max over j < nq and q heads g of group h of (score_q[r][j][g] . ik[b])
+ * (BOUND: of sum_d max(q_d max_d, q_d min_d), evaluated as [max(q,0) | min(q,0)] . ik[b]),
  * fp32 with fp32 accumulation of exact bf16 products, for b < n_b(ctx_len[r]); other entries
  * are left untouched.  nq in [1, max_score_q].  Kernels: tcgen05 tensor cores for 64-256 scoring
  * rows per unit (nq * G) with d_k a multiple of 64; mma.sync tiles for up to 128 rows with d_k 128

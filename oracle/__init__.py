@@ -13,6 +13,8 @@ What it computes, written plainly (numpy, fp64 where the arithmetic is floating 
   bf16         bf16 round-to-nearest-even from the IEEE-754 definitions.
   index_keys   per-block mean key used to score blocks (a reading: the pages name "attention
                scoring -> per-block importance" without the block summary).
+  bound        per-block [max | min] key summaries and the query-aware upper-bound block score
+               (second scoring mode; the Quest rule the pages name among selector families).
   scores       block score = scale * max over GQA group heads and scoring queries of q.ik
                (tuntang.top survey, section 3 step 3: element-wise max within a GQA group;
                OasisKV page, key module 2: lookahead drafts score KV blocks).
@@ -34,6 +36,7 @@ fixtures (``tests/golden/``), brute force or a library routine; see each module'
 from .bf16 import bf16_to_f32, bf16_to_f64, f32_to_bf16_rne
 from .kv_size import kv_cache_bytes, kv_cache_bytes_variant
 from .index_keys import index_keys, index_key_block
+from .bound import block_scores_bound, index_minmax, index_minmax_block
 from .scores import block_scores
 from .select import forced_blocks, select_blocks
 from .cache import (UnitCache, UpdateResult, PrefetchResult, cache_restore, cache_update, importance_key,
@@ -43,7 +46,7 @@ from .step import OracleDecoder, UnitRecord
 
 __all__ = [
     "bf16_to_f32", "bf16_to_f64", "f32_to_bf16_rne", "kv_cache_bytes", "kv_cache_bytes_variant",
-    "index_keys", "index_key_block", "block_scores", "forced_blocks", "select_blocks", "UnitCache",
+    "index_keys", "index_key_block", "index_minmax", "index_minmax_block", "block_scores", "block_scores_bound", "forced_blocks", "select_blocks", "UnitCache",
     "UpdateResult", "PrefetchResult", "cache_update", "cache_restore", "importance_key", "layer_prefetch", "attend", "OracleDecoder",
     "UnitRecord",
 ]

@@ -17,7 +17,9 @@ Lookahead mode is defined without append and without prefetch (those combination
 part of this build's workloads).  With w.evict_policy == "importance" every update evicts the
 least important blocks by the scores that made its selection (see oracle.cache).  snapshot() and
 restore() save and put back every unit's cache state and pending selection (speculative
-rollback, KV-cache overview, section 6.1).
+rollback, KV-cache overview, section 6.1).  With w.score_mode == "bound" blocks are summarised by
+their per-dimension [max | min] keys and scored by the query-aware upper bound (oracle.bound)
+instead of the block-mean key.
 
 Parity-relevant outputs are recorded per unit (UnitRecord) and per layer (stats()).
 """
@@ -26,6 +28,7 @@ from dataclasses import dataclass
 import numpy as np
 
 from .attention import attend
+from .bound import block_scores_bound, index_minmax, index_minmax_block
 from .cache import PrefetchResult, UnitCache, UpdateResult, cache_restore, cache_update, layer_prefetch
 from .index_keys import index_key_block, index_keys
 from .scores import block_scores
@@ -51,6 +54,7 @@ class OracleDecoder:
         if w.lookahead and (w.append or w.layer_prefetch):
             raise ValueError("lookahead mode is defined without append and without prefetch")
         self.w = w
+        self.bound = getattr(w, "score_mode", "mean") == "bound"
         self.reqs = list(range(w.n_req)) if reqs is None else list(reqs)
         self.L = {r: int(ctx_len[r]) for r in self.reqs}
         self.k, self.v, self.ik, self.cache, self.pending = {}, {}, {}, {}, {}
@@ -60,9 +64,13 @@ class OracleDecoder:
                     u = (l, r, h)
                     self.k[u] = np.array(host_k[l, r, h][: w.max_ctx], copy=True)
                     self.v[u] = None if w.v_shares_k else np.array(host_v[l, r, h][: w.max_ctx], copy=True)
-                    ik = np.zeros((w.max_blocks, w.d_k), np.uint16)
                     nb = self.n_blocks(r)
-                    ik[:nb] = index_keys(self.k[u], self.L[r], w.block_size)
+                    if self.bound:
+                        ik = np.zeros((w.max_blocks, 2 * w.d_k), np.uint16)
+                        ik[:nb] = index_minmax(self.k[u], self.L[r], w.block_size)
+                    else:
+                        ik = np.zeros((w.max_blocks, w.d_k), np.uint16)
+                        ik[:nb] = index_keys(self.k[u], self.L[r], w.block_size)
                     self.ik[u] = ik
                     self.cache[u] = UnitCache(w.cap_blocks, w.max_blocks)
                     self.pending[u] = None
@@ -90,7 +98,8 @@ class OracleDecoder:
     def _score_select(self, u, rows):
         w, r = self.w, u[1]
         nb = self.n_blocks(r)
-        s64, a = block_scores(rows, self.ik[u][:nb], w.softmax_scale)
+        score = block_scores_bound if self.bound else block_scores
+        s64, a = score(rows, self.ik[u][:nb], w.softmax_scale)
         s32 = s64.astype(np.float32)
         sel = select_blocks(s32, nb, w.budget_blocks, w.n_sink, w.n_recent)
         return s32, a, sel
@@ -102,7 +111,8 @@ class OracleDecoder:
         if not w.v_shares_k:
             self.v[u][p] = v_new
         b = p // w.block_size
-        self.ik[u][b] = index_key_block(self.k[u][b * w.block_size: self.L[r]])
+        summarise = index_minmax_block if self.bound else index_key_block
+        self.ik[u][b] = summarise(self.k[u][b * w.block_size: self.L[r]])
 
     def step(self, q, score_q=None, new_k=None, new_v=None):
         """q: [N_l][B][H_q][D_k] bf16; score_q: [N_l][B][n_draft][H_q][D_k] drafts (lookahead);

@@ -32,9 +32,10 @@ class KvsConfig(ctypes.Structure):
                 ("budget_blocks", ctypes.c_int), ("n_sink", ctypes.c_int), ("n_recent", ctypes.c_int),
                 ("cap_blocks", ctypes.c_int), ("max_score_q", ctypes.c_int), ("lookahead", ctypes.c_int),
                 ("max_prefetch", ctypes.c_int), ("softmax_scale", ctypes.c_float),
-                ("wait_timeout_us", ctypes.c_uint), ("evict_policy", ctypes.c_int)]
+                ("wait_timeout_us", ctypes.c_uint), ("evict_policy", ctypes.c_int), ("score_mode", ctypes.c_int)]
 
 EVICT_POLICY = {"lru": 0, "importance": 1}
+SCORE_MODE = {"mean": 0, "bound": 1}
 
 
 class KvsStats(ctypes.Structure):
@@ -119,7 +120,8 @@ def make_config(w, max_score_q: int | None = None, max_prefetch: int = 0, wait_t
     return KvsConfig(w.n_req, w.n_layer, w.n_q_head, w.n_kv_head, w.d_k, w.d_v, int(w.v_shares_k), w.block_size,
                      w.max_ctx, w.budget_blocks, w.n_sink, w.n_recent, w.cap_blocks,
                      max_score_q if max_score_q is not None else max(1, w.n_score_q), int(w.lookahead), max_prefetch,
-                     float(w.softmax_scale), wait_timeout_us, EVICT_POLICY[getattr(w, "evict_policy", "lru")])
+                     float(w.softmax_scale), wait_timeout_us, EVICT_POLICY[getattr(w, "evict_policy", "lru")],
+                     SCORE_MODE[getattr(w, "score_mode", "mean")])
 
 
 class Context:

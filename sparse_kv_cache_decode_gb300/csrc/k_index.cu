@@ -1,4 +1,5 @@
-// Index keys (block means of the keys) and the per-step append of one token.
+// Block summaries (the mean key, or the per-dimension [max | min] of the keys) and the per-step
+// append of one token.
 #include "kvs_common.cuh"
 #include "kvs_ptx.cuh"
 
@@ -6,7 +7,8 @@ namespace kvs {
 
 // One warp per block: lanes own 4 consecutive dims at a time; tokens are summed in fp32 one at
 // a time in ascending position, divided by the present-token count (IEEE) and rounded to bf16
-// (round-to-nearest-even).
+// (round-to-nearest-even).  Bound mode keeps the running max and min instead (strict compares,
+// so among equal values the earliest token's is kept) and writes [max | min].
 template <int CHUNKS>  // 4-dim chunks per lane = ceil(dk / 128)
 __global__ void __launch_bounds__(256) index_build_kernel(Dims d, Layer L, __nv_bfloat16* __restrict__ index,
                                                           const int* __restrict__ ctx_len) {
@@ -24,7 +26,7 @@ __global__ void __launch_bounds__(256) index_build_kernel(Dims d, Layer L, __nv_
   const int t0 = b * d.bs, t1 = min(t0 + d.bs, len);
   const int nchunk = d.dk / 4;
   const __nv_bfloat16* rows = L.host_k + (size_t)u * d.max_ctx * d.dk;
-  float acc[CHUNKS][4];
+  float acc[CHUNKS][4], mx[CHUNKS][4], mn[CHUNKS][4];
 #pragma unroll
   for (int c = 0; c < CHUNKS; ++c)
 #pragma unroll
@@ -36,15 +38,33 @@ __global__ void __launch_bounds__(256) index_build_kernel(Dims d, Layer L, __nv_
       int ch = lane + 32 * c;
       if (ch < nchunk) {
         uint2 v = row[ch];
-        acc[c][0] = __fadd_rn(acc[c][0], bf16_lo(v.x));
-        acc[c][1] = __fadd_rn(acc[c][1], bf16_hi(v.x));
-        acc[c][2] = __fadd_rn(acc[c][2], bf16_lo(v.y));
-        acc[c][3] = __fadd_rn(acc[c][3], bf16_hi(v.y));
+        const float x[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
+        if (d.bound) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (t == t0 || x[e] > mx[c][e]) mx[c][e] = x[e];
+            if (t == t0 || x[e] < mn[c][e]) mn[c][e] = x[e];
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[c][e] = __fadd_rn(acc[c][e], x[e]);
+        }
       }
     }
   }
   const float n = (float)(t1 - t0);
-  uint2* out = reinterpret_cast<uint2*>(index + ((size_t)u * d.nb_max + b) * d.dk);
+  uint2* out = reinterpret_cast<uint2*>(index + ((size_t)u * d.nb_max + b) * d.didx);
+  if (d.bound) {   // the kept values are bf16 already: packing them is exact
+#pragma unroll
+    for (int c = 0; c < CHUNKS; ++c) {
+      int ch = lane + 32 * c;
+      if (ch < nchunk) {
+        out[ch] = make_uint2(pack_bf16x2(mx[c][0], mx[c][1]), pack_bf16x2(mx[c][2], mx[c][3]));
+        out[nchunk + ch] = make_uint2(pack_bf16x2(mn[c][0], mn[c][1]), pack_bf16x2(mn[c][2], mn[c][3]));
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int c = 0; c < CHUNKS; ++c) {
     int ch = lane + 32 * c;
@@ -110,11 +130,25 @@ __global__ void __launch_bounds__(128) append_kernel(Dims d, Layer L, const __nv
       if (sv) sv[i] = x;
     }
   }
-  // index key of block b over tokens [b*bs, len): earlier rows in token order, then the new one
+  // summary of block b over tokens [b*bs, len): earlier rows in token order, then the new one
   const __nv_bfloat16* rows = slot >= 0 ? L.kpool + ((size_t)u * d.C + slot) * d.bs * d.dk
                                         : L.host_k + ((size_t)u * d.max_ctx + (size_t)b * d.bs) * d.dk;
   const int nt = row_in_blk;                                // earlier rows of the block
   const float n = (float)(nt + 1);
+  if (d.bound) {
+    for (int i = threadIdx.x; i < d.dk; i += blockDim.x) {
+      float mx = 0.f, mn = 0.f;
+      for (int t = 0; t <= nt; ++t) {
+        const float x = __bfloat162float(t < nt ? rows[(size_t)t * d.dk + i] : k_new[(size_t)u * d.dk + i]);
+        if (t == 0 || x > mx) mx = x;
+        if (t == 0 || x < mn) mn = x;
+      }
+      __nv_bfloat16* o = index + ((size_t)u * d.nb_max + b) * d.didx;
+      o[i] = __float2bfloat16_rn(mx);
+      o[d.dk + i] = __float2bfloat16_rn(mn);
+    }
+    return;
+  }
   for (int i = threadIdx.x; i < d.dk; i += blockDim.x) {
     float acc = 0.f;
     int t = 0;
@@ -127,7 +161,7 @@ __global__ void __launch_bounds__(128) append_kernel(Dims d, Layer L, const __nv
     }
     for (; t < nt; ++t) acc = __fadd_rn(acc, __bfloat162float(rows[(size_t)t * d.dk + i]));
     acc = __fadd_rn(acc, __bfloat162float(k_new[(size_t)u * d.dk + i]));
-    index[((size_t)u * d.nb_max + b) * d.dk + i] = __float2bfloat16_rn(__fdiv_rn(acc, n));
+    index[((size_t)u * d.nb_max + b) * d.didx + i] = __float2bfloat16_rn(__fdiv_rn(acc, n));
   }
 }
 

@@ -23,7 +23,7 @@ struct ScoreSmem {
   size_t bytes() const { return (size_t)rows_pad * row_stride + (size_t)nwarps * 2 * 16 * row_stride; }
 };
 
-template <int DK, int NP>  // NP = number of n8 tiles of scoring rows (rows_pad / 8)
+template <int DK, int NP>  // DK = index row width d_idx; NP = number of n8 tiles of scoring rows (rows_pad / 8)
 __global__ void __launch_bounds__(128) score_kernel(Dims d, const __nv_bfloat16* __restrict__ index,
                                                     const __nv_bfloat16* __restrict__ q, int nq,
                                                     const int* __restrict__ ctx_len, float* __restrict__ scores,
@@ -56,8 +56,7 @@ __global__ void __launch_bounds__(128) score_kernel(Dims d, const __nv_bfloat16*
     uint4 v = make_uint4(0, 0, 0, 0);
     if (row < R) {
       int j = row / d.G, g = row % d.G;
-      const uint4* src = reinterpret_cast<const uint4*>(q + (((size_t)r * nq + j) * d.Hq + h * d.G + g) * DK);
-      v = src[ch];
+      v = score_row_chunk(q + (((size_t)r * nq + j) * d.Hq + h * d.G + g) * d.dk, ch, d);
     }
     *reinterpret_cast<uint4*>(qs + row * RS + ch * 16) = v;
   }
@@ -168,7 +167,7 @@ cudaError_t launch_score_t(const Dims& d, const __nv_bfloat16* index, const __nv
 int score_supported(const Dims& d) {
   // every call width 1..max_nq must have a kernel: tcgen05 for wide rows, mma.sync otherwise
   for (int nq = 1; nq <= d.max_nq; ++nq) {
-    const bool mma = (d.dk == 128 || d.dk == 576) && nq * d.G <= kScoreMaxRows;
+    const bool mma = (d.didx == 128 || d.didx == 256 || d.didx == 576) && nq * d.G <= kScoreMaxRows;
     if (!mma && !score_tc_supported(d, nq)) return 0;
   }
   return 1;
@@ -181,7 +180,7 @@ cudaError_t launch_score(const Dims& d, const __nv_bfloat16* index, const __nv_b
   int np = (R + 7) / 8;
   if (np > 16 || nq < 1) return cudaErrorInvalidValue;
   np = np <= 2 ? 2 : np <= 4 ? 4 : np <= 8 ? 8 : 16;  // padded rows are zero and masked out
-  if (d.dk == 128) {
+  if (d.didx == 128) {
     switch (np) {
       case 2: return launch_score_t<128, 2>(d, index, q, nq, ctx_len, scores, err, s);
       case 4: return launch_score_t<128, 4>(d, index, q, nq, ctx_len, scores, err, s);
@@ -189,7 +188,15 @@ cudaError_t launch_score(const Dims& d, const __nv_bfloat16* index, const __nv_b
       case 16: return launch_score_t<128, 16>(d, index, q, nq, ctx_len, scores, err, s);
       default: break;
     }
-  } else if (d.dk == 576) {
+  } else if (d.didx == 256) {
+    switch (np) {
+      case 2: return launch_score_t<256, 2>(d, index, q, nq, ctx_len, scores, err, s);
+      case 4: return launch_score_t<256, 4>(d, index, q, nq, ctx_len, scores, err, s);
+      case 8: return launch_score_t<256, 8>(d, index, q, nq, ctx_len, scores, err, s);
+      case 16: return launch_score_t<256, 16>(d, index, q, nq, ctx_len, scores, err, s);
+      default: break;
+    }
+  } else if (d.didx == 576) {
     switch (np) {
       case 2: return launch_score_t<576, 2>(d, index, q, nq, ctx_len, scores, err, s);
       case 4: return launch_score_t<576, 4>(d, index, q, nq, ctx_len, scores, err, s);

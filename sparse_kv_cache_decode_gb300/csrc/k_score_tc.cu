@@ -39,7 +39,7 @@ TcPlan make_tc_plan(const Dims& d, int nq, int n_sm) {
   TcPlan p;
   p.n_rows = nq * d.G;
   p.n_pad = ((p.n_rows + 15) / 16) * 16;
-  p.kc = d.dk / kChunk;
+  p.kc = d.didx / kChunk;
   p.q_bytes = p.kc * p.n_pad * 128;
   const int fixed = 1024 + p.q_bytes + 512;
   p.stages = (kMaxSmem - kSmemLeft - fixed) / kChunkBytes;
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the unit's scoring rows (rows >= n_rows zero), 8 loads in flight per thread
   {
     const int r = u / d.Hkv, h = u % d.Hkv;
-    const int ch = d.dk / 8;                           // 16-byte chunks per row
+    const int ch = d.didx / 8;                         // 16-byte chunks per (staged) row
     const int total = plan.n_pad * ch;
     for (int base = tid; base < total; base += kThreads * 8) {
       uint4 v[8];
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = i / ch;
         if (i < total && row < plan.n_rows) {
           const int j = row / d.G, g = row - j * d.G;
-          v[x] = reinterpret_cast<const uint4*>(q + (((size_t)r * nq + j) * d.Hq + h * d.G + g) * d.dk)[i - row * ch];
+          v[x] = score_row_chunk(q + (((size_t)r * nq + j) * d.Hq + h * d.G + g) * d.dk, i - row * ch, d);
         }
       }
 #pragma unroll
@@ -235,7 +235,7 @@ int sm_count_tc() { return device_sm_count(); }
 
 int score_tc_supported(const Dims& d, int nq) {
   // the tensor-memory path pays off for wide contractions (many scoring rows per index row)
-  if (d.dk % kChunk != 0 || nq * d.G > 256 || nq * d.G < 64) return 0;
+  if (d.didx % kChunk != 0 || nq * d.G > 256 || nq * d.G < 64) return 0;
   TcPlan p = make_tc_plan(d, nq, sm_count_tc());
   return p.stages >= 2;
 }
@@ -247,7 +247,7 @@ cudaError_t launch_score_tc(const Dims& d, const __nv_bfloat16* index, const __n
     if (e != cudaSuccess) return e;
   }
   CUtensorMap tm;
-  if (!make_tmap_2d(&tm, const_cast<__nv_bfloat16*>(index), (uint64_t)d.dk, (uint64_t)d.U * d.nb_max, kChunk, kTileM))
+  if (!make_tmap_2d(&tm, const_cast<__nv_bfloat16*>(index), (uint64_t)d.didx, (uint64_t)d.U * d.nb_max, kChunk, kTileM))
     return cudaErrorInvalidValue;
   TcPlan plan = make_tc_plan(d, nq, sm_count_tc());
   launch_pdl(score_tc_kernel, dim3(plan.n_cta), dim3(kThreads), plan.smem, s, tm, d, q, nq, ctx_len, scores, plan, err);

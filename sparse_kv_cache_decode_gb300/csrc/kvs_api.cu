@@ -76,6 +76,7 @@ bool fill_dims(const kvs_config* c, Dims* d) {
   if (c->max_prefetch < 0 || c->max_prefetch > c->cap_blocks - c->budget_blocks) return false;
   if (!(c->softmax_scale >= 0.f) || isinf(c->softmax_scale)) return false;
   if (c->evict_policy != KVS_EVICT_LRU && c->evict_policy != KVS_EVICT_IMPORTANCE) return false;
+  if (c->score_mode != KVS_SCORE_MEAN && c->score_mode != KVS_SCORE_BOUND) return false;
   d->B = c->n_req;
   d->NL = c->n_layer;
   d->Hq = c->n_q_head;
@@ -99,6 +100,8 @@ bool fill_dims(const kvs_config* c, Dims* d) {
   d->timeout_us = c->wait_timeout_us ? c->wait_timeout_us : 2000000u;
   d->row_bytes = 2 * (c->d_k + (c->v_shares_k ? 0 : c->d_v));
   d->evict_importance = c->evict_policy == KVS_EVICT_IMPORTANCE;
+  d->bound = c->score_mode == KVS_SCORE_BOUND;
+  d->didx = d->bound ? 2 * c->d_k : c->d_k;
   return true;
 }
 
@@ -494,7 +497,7 @@ kvs_status kvs_index_build(kvs_ctx* c, int layer, void* d_index, const int* d_ct
   if (!layer_ok(c, layer) || !d_index || !d_ctx_len) return KVS_ERR_INVALID_ARG;
   if (!c->host_k_dev) return KVS_ERR_HOST_MEM;
   const Dims& d = c->d;
-  __nv_bfloat16* idx = static_cast<__nv_bfloat16*>(d_index) + (size_t)layer * d.U * d.nb_max * d.dk;
+  __nv_bfloat16* idx = static_cast<__nv_bfloat16*>(d_index) + (size_t)layer * d.U * d.nb_max * d.didx;
   return cuda_status(timed(c, KVS_K_INDEX, S(stream), 1, [&] { return launch_index_build(d, c->layers[layer], idx, d_ctx_len, S(stream)); }));
 }
 
@@ -504,7 +507,7 @@ kvs_status kvs_score_blocks(kvs_ctx* c, int layer, const void* d_score_q, int nq
   const Dims& d = c->d;
   if (nq < 1 || nq > d.max_nq) return KVS_ERR_INVALID_ARG;
   if (!score_supported(d)) return KVS_ERR_NOT_SUPPORTED;
-  const __nv_bfloat16* idx = static_cast<const __nv_bfloat16*>(d_index) + (size_t)layer * d.U * d.nb_max * d.dk;
+  const __nv_bfloat16* idx = static_cast<const __nv_bfloat16*>(d_index) + (size_t)layer * d.U * d.nb_max * d.didx;
   return cuda_status(timed(c, KVS_K_SCORE, S(stream), 1, [&] {
     return launch_score(d, idx, static_cast<const __nv_bfloat16*>(d_score_q), nq, d_ctx_len, d_scores, c->err, S(stream));
   }));
@@ -613,7 +616,7 @@ kvs_status kvs_append(kvs_ctx* c, int layer, const void* d_k_new, const void* d_
   if (!aligned16(d_k_new) || !aligned16(d_v_new)) return KVS_ERR_INVALID_ARG;
   if (!c->host_k_dev) return KVS_ERR_HOST_MEM;
   const Dims& d = c->d;
-  __nv_bfloat16* idx = static_cast<__nv_bfloat16*>(d_index) + (size_t)layer * d.U * d.nb_max * d.dk;
+  __nv_bfloat16* idx = static_cast<__nv_bfloat16*>(d_index) + (size_t)layer * d.U * d.nb_max * d.didx;
   return cuda_status(timed(c, KVS_K_APPEND, S(stream), 1, [&] {
     return launch_append(d, c->layers[layer], static_cast<const __nv_bfloat16*>(d_k_new),
                          static_cast<const __nv_bfloat16*>(d_v_new), idx, d_ctx_len, S(stream));
@@ -637,7 +640,7 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
   Layer& L = c->layers[layer];
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(d_q);
   const __nv_bfloat16* sq = d_score_q ? static_cast<const __nv_bfloat16*>(d_score_q) : q;
-  __nv_bfloat16* idx = static_cast<__nv_bfloat16*>(d_index) + (size_t)layer * d.U * d.nb_max * d.dk;
+  __nv_bfloat16* idx = static_cast<__nv_bfloat16*>(d_index) + (size_t)layer * d.U * d.nb_max * d.didx;
   int* sel = d_sel_out ? d_sel_out : L.sel;
   int* nsel = d_nsel_out ? d_nsel_out : L.nsel;
   cudaError_t e = cudaSuccess;

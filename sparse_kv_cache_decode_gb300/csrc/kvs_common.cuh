@@ -17,6 +17,8 @@ struct Dims {
   int bs, max_ctx, nb_max;
   int Kb, n_sink, n_recent, C, max_nq, lookahead, max_prefetch;
   int evict_importance;  // victims least important first (else least recently used)
+  int bound;             // blocks summarised by [max | min] keys and scored by the upper bound
+  int didx;              // index row width: dk (block-mean key) or 2 * dk ([max | min] summary)
   int U;                 // units per layer = B * Hkv
   float scale;
   unsigned timeout_us;
@@ -101,6 +103,25 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   if ((u & 0x7fffffffu) > 0x7f800000u) return 0u;      // NaN
   if (u == 0x80000000u) u = 0u;                         // -0.0 -> +0.0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Chunk c (8 bf16 values) of one scoring row as the scoring kernels stage it: the query row
+// itself (block-mean index), or [max(q, 0) | min(q, 0)] for the [max | min] summaries, whose dot
+// product with the summary row is sum_d max(q_d mx_d, q_d mn_d) (exact: the kept values are q's).
+__device__ __forceinline__ uint4 score_row_chunk(const __nv_bfloat16* qrow, int c, const Dims& d) {
+  if (!d.bound) return reinterpret_cast<const uint4*>(qrow)[c];
+  const int nc = d.dk / 8;
+  const bool neg = c >= nc;
+  uint4 v = reinterpret_cast<const uint4*>(qrow)[neg ? c - nc : c];
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = w[i] & 0xffffu, hi = w[i] >> 16;
+    const float flo = __uint_as_float(lo << 16), fhi = __uint_as_float(hi << 16);
+    const bool klo = neg ? flo < 0.f : flo > 0.f, khi = neg ? fhi < 0.f : fhi > 0.f;
+    w[i] = (klo ? lo : 0u) | ((khi ? hi : 0u) << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // -------------------------------------------------------------- launchers (one per kernel TU)

@@ -51,7 +51,7 @@ class GpuCase:
         self.ctx = K.Context(self.cfg)
         self.ctx.bind_host_kv(self.k_host, self.v_host)
         self.nb_max = w.max_blocks
-        self.index = torch.zeros((NL, B, Hkv, self.nb_max, w.d_k), dtype=torch.int16, device="cuda")
+        self.index = torch.zeros((NL, B, Hkv, self.nb_max, w.d_idx), dtype=torch.int16, device="cuda")
         for l in range(NL):
             self.ctx.index_build(l, self.index, self.ctx_len)
         self.stats = torch.zeros((NL, 7), dtype=torch.int64, device="cuda")

@@ -10,8 +10,8 @@ import pytest
 
 import workload as W
 from kvs_harness import GpuCase, score_tolerance
-from oracle import (UnitCache, attend, bf16_to_f32, block_scores, cache_update, index_keys, layer_prefetch,
-                    select_blocks)
+from oracle import (UnitCache, attend, bf16_to_f32, block_scores, block_scores_bound, cache_update, index_keys,
+                    index_minmax, layer_prefetch, select_blocks)
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -23,6 +23,18 @@ TINY_G8 = W.TINY.with_(name="tiny_g8", n_req=2, n_q_head=16, n_kv_head=2)
 TINY_BS64 = W.TINY.with_(name="tiny_bs64", n_req=2, block_size=64, ctx0=3000, budget_blocks=8, cap_blocks=12)
 # 16 query heads per kv head x 5 scoring queries: 80 rows per unit (the tensor-memory scoring path)
 TINY_LA_G16 = W.TINY_LOOKAHEAD.with_(name="tiny_la_g16", n_req=3, n_q_head=32, n_kv_head=2)
+# [max | min] summaries with the upper-bound score: 8B-like rows on the mma.sync path, 80 rows per
+# unit on the tensor-memory path
+TINY3_BOUND = TINY3.with_(name="tiny3_bound", score_mode="bound")
+TINY_LA_G16_BOUND = TINY_LA_G16.with_(name="tiny_la_g16_bound", score_mode="bound")
+
+
+def _summaries(w, k_rows, L):
+    return index_minmax(k_rows, L, w.block_size) if w.score_mode == "bound" else index_keys(k_rows, L, w.block_size)
+
+
+def _scores(w, rows, summ):
+    return (block_scores_bound if w.score_mode == "bound" else block_scores)(rows, summ, w.softmax_scale)
 
 
 def _dev(a):
@@ -34,7 +46,8 @@ def _nb(L, bs):
 
 
 @pytest.mark.parametrize("w,lens", [(TINY3, [4096, 1000, 17]), (W.TINY_MLA, [4096]),
-                                    (TINY_BS64, [3000, 2999]), (MLA_G128, [2048, 333])])
+                                    (TINY_BS64, [3000, 2999]), (MLA_G128, [2048, 333]),
+                                    (TINY3_BOUND, [4096, 1000, 17]), (TINY_BS64.with_(score_mode="bound"), [3000, 7])])
 def test_index_build_bit_exact(w, lens):
     g = GpuCase(w, lens)
     idx = g.index.cpu().numpy().view(np.uint16)
@@ -42,7 +55,7 @@ def test_index_build_bit_exact(w, lens):
         for r, L in enumerate(lens):
             for h in range(w.n_kv_head):
                 nb = _nb(L, w.block_size)
-                ref = index_keys(g.k_np[l, r, h], L, w.block_size)
+                ref = _summaries(w, g.k_np[l, r, h], L)
                 np.testing.assert_array_equal(idx[l, r, h, :nb], ref, err_msg=f"unit {(l, r, h)}")
 
 
@@ -58,7 +71,10 @@ def _score_rows(w, q, d, l, r, h):
                                     (TINY3.with_(int_scale=2.0), [4096, 1000, 17]),
                                     (TINY_LA_G16, [4096, 1000, 17]),
                                     (TINY_LA_G16.with_(int_scale=2.0), [4096, 2049, 129]),
-                                    (MLA_G128.with_(int_scale=1.0), [2048, 1500])])
+                                    (MLA_G128.with_(int_scale=1.0), [2048, 1500]),
+                                    (TINY3_BOUND, [4096, 1000, 17]), (TINY3_BOUND.with_(int_scale=2.0), [4096, 1000, 17]),
+                                    (TINY_LA_G16_BOUND, [4096, 1000, 17]),
+                                    (TINY_LA_G16_BOUND.with_(int_scale=2.0), [4096, 2049, 129])])
 def test_score_blocks(w, lens):
     g = GpuCase(w, lens)
     scores = torch.full((w.n_req, w.n_kv_head, g.nb_max), float("nan"), dtype=torch.float32, device="cuda")
@@ -72,8 +88,8 @@ def test_score_blocks(w, lens):
             for r, L in enumerate(lens):
                 for h in range(w.n_kv_head):
                     nb = _nb(L, w.block_size)
-                    ik = index_keys(g.k_np[l, r, h], L, w.block_size)
-                    s, a = block_scores(_score_rows(w, q, d, l, r, h), ik, w.softmax_scale)
+                    ik = _summaries(w, g.k_np[l, r, h], L)
+                    s, a = _scores(w, _score_rows(w, q, d, l, r, h), ik)
                     gs = got[r, h, :nb].astype(np.float64)
                     if w.int_scale > 0:     # exact integer-valued dot products: bit-exact fp32
                         np.testing.assert_array_equal(got[r, h, :nb], s.astype(np.float32))

@@ -31,6 +31,11 @@ INT_CASES = [
     (W.TINY.with_(name="tiny_imp_int", n_req=2, int_scale=2.0, evict_policy="importance"), [4096, 3001], False),
     (W.TINY_LOOKAHEAD.with_(name="tiny_la_imp_int_cs", n_req=2, int_scale=2.0, evict_policy="importance"),
      [4096, 2050], True),
+    # [max | min] block summaries scored by the upper bound, with append (the last block's summary
+    # is kept up to date) and in lookahead mode
+    (W.TINY_APPEND.with_(name="tiny_app_bound_int", n_req=2, int_scale=2.0, score_mode="bound"), [4096, 1000], False),
+    (W.TINY_LOOKAHEAD.with_(name="tiny_la_bound_int_cs", n_req=2, int_scale=2.0, score_mode="bound"),
+     [4096, 2050], True),
 ]
 
 

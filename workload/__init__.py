@@ -135,6 +135,7 @@ class Workload:
     int_scale: float = 0.0   # > 0: integer-valued inputs round(x * int_scale), clipped (exact fp32 scores)
     int_clip: float = 7.0
     evict_policy: str = "lru"   # "lru" or "importance" (least important block first)
+    score_mode: str = "mean"    # "mean" (block-mean key) or "bound" ([max | min] summary, upper-bound score)
     notes: str = ""
 
     @property
@@ -144,6 +145,11 @@ class Workload:
     @property
     def max_ctx(self) -> int:
         return self.ctx0 + (self.steps if self.append else 0)
+
+    @property
+    def d_idx(self) -> int:
+        """Width of a block's index row: d_k for block-mean keys, 2 d_k for [max | min] summaries."""
+        return 2 * self.d_k if self.score_mode == "bound" else self.d_k
 
     @property
     def n_score_q(self) -> int:
