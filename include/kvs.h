@@ -23,7 +23,8 @@
  * per unit.  A unit is one (request, layer, kv-head); a layer's units are numbered
  * u = request * H_kv + kv_head.  ctx_len[r] = L_r tokens present for request r; n_b(L) = ceil(L/bs).
  *
- * Layouts (row-major, bf16 = 16-bit patterns):
+ * Layouts (row-major, bf16 = 16-bit patterns; history and slot pools in E4M3 bytes when
+ * kv_dtype is FP8):
  *   host K      [N_l][B][H_kv][max_ctx][d_k]      pinned, device-mapped (see kvs_bind_host_kv)
  *   host V      [N_l][B][H_kv][max_ctx][d_v]      absent when v_shares_k (V = first d_v of K row)
  *   index       [N_l][B][H_kv][n_b(max_ctx)][d_idx] device; block summaries (kvs_index_build):
@@ -90,7 +91,19 @@ typedef struct {
   unsigned wait_timeout_us; /* bound on device waits (0 -> 2000000 us) */
   int evict_policy;    /* KVS_EVICT_LRU (0) or KVS_EVICT_IMPORTANCE (1) [OASIS module 3, HISP insight 2] */
   int score_mode;      /* KVS_SCORE_MEAN (0) or KVS_SCORE_BOUND (1): how blocks are summarised and scored */
+  int kv_dtype;        /* KVS_KV_BF16 (0) or KVS_KV_FP8_E4M3 (1): the history's and the slot pools' format */
+  float k_scale, v_scale; /* E4M3: a stored key is decode(code) * k_scale, a value decode(code) * v_scale (0 -> 1) */
 } kvs_config;
+
+/* KV storage format [KVC 3.2: FP8 E4M3 keeps accuracy at half the bytes].  BF16: host history and
+ * slot pools hold bf16.  FP8_E4M3: they hold E4M3 codes (bias 7, 3 mantissa bits, largest finite
+ * 448, no infinity) of value / scale; host K/V rows are d_k / d_v bytes.  Index keys (bf16) are
+ * built from the fp32 values fp32(decode(code) * k_scale); attention computes the logits as
+ * (softmax_scale * k_scale) * (q . decode(code_k)) and the output as v_scale * sum p decode(code_v)
+ * / sum p, with every code widened exactly to bf16 for the tensor-core tiles; appended bf16 tokens
+ * are quantised on arrival (round to nearest even, saturating to +-448).  Supported with block-mean
+ * scoring, separate K and V of head dim 128 and block sizes that are multiples of 16. */
+enum { KVS_KV_BF16 = 0, KVS_KV_FP8_E4M3 = 1 };
 
 /* Block summaries and scores.  MEAN: the index row of a block is its mean key (d_idx = d_k) and
  * the score is the mean token logit q . ik.  BOUND: the index row is [max | min] of its present
@@ -305,6 +318,12 @@ kvs_status kvs_probe_host_read(const void* h_base, size_t region_bytes, const lo
 kvs_status kvs_select_blocks_noalloc(const kvs_config* cfg, const void* d_score_q, int nq,
                                      const void* d_index_layer, const int* d_ctx_len, int* d_sel, int* d_nsel,
                                      unsigned* d_status, kvs_stream_t stream);
+
+/* E4M3 codes of n bf16 values (device buffers): code[i] = encode(fp32(src[i]) / scale), rounding to
+ * nearest even and saturating to +-448 (no counterpart in the pages beyond the format: the
+ * quantiser of an FP8 history, the rule the append applies to new tokens).  scale > 0.
+ * Errors: KVS_ERR_INVALID_ARG. */
+kvs_status kvs_quantize_e4m3(const void* d_src_bf16, void* d_dst, size_t n, float scale, kvs_stream_t stream);
 
 /* Library version string. */
 const char* kvs_version(void);

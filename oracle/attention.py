@@ -19,11 +19,16 @@ from .bf16 import bf16_to_f64
 
 
 def attend(q_rows: np.ndarray, k_tok: np.ndarray, v_tok: np.ndarray, scale: float) -> np.ndarray:
-    """q_rows (G, D_k), k_tok (T, D_k), v_tok (T, D_v): bf16 patterns -> (G, D_v) fp32."""
+    """q_rows (G, D_k) bf16 patterns; k_tok (T, D_k), v_tok (T, D_v): bf16 patterns or float64
+    values (dequantized FP8 rows) -> (G, D_v) fp32."""
     g, dv = q_rows.shape[0], v_tok.shape[1]
     if k_tok.shape[0] == 0:
         return np.zeros((g, dv), np.float32)
-    q, k, v = bf16_to_f64(q_rows), bf16_to_f64(k_tok), bf16_to_f64(v_tok)
+
+    def f64(a):
+        return a if a.dtype == np.float64 else bf16_to_f64(a)
+
+    q, k, v = bf16_to_f64(q_rows), f64(k_tok), f64(v_tok)
     logits = float(scale) * (q @ k.T)
     p = np.exp(logits - logits.max(axis=1, keepdims=True))
     o = (p @ v) / p.sum(axis=1, keepdims=True)

@@ -20,14 +20,20 @@ import numpy as np
 from .bf16 import bf16_to_f32, f32_to_bf16_rne
 
 
+def _f32(rows: np.ndarray) -> np.ndarray:
+    """Key rows as fp32 values: bf16 bit patterns (uint16) are widened; fp32 values (dequantized
+    FP8 keys) are taken as they are."""
+    return rows if rows.dtype == np.float32 else bf16_to_f32(rows)
+
+
 def index_key_block(k_rows: np.ndarray) -> np.ndarray:
-    """Index key of one block from its present key rows (n_b, D) as bf16 bit patterns."""
+    """Index key of one block from its present key rows (n_b, D): bf16 bit patterns or fp32 values."""
     n = k_rows.shape[0]
     if n == 0:
         raise ValueError("a block with no present token has no index key")
     acc = np.zeros(k_rows.shape[1], np.float32)
     for t in range(n):                       # ascending token order, fp32 adds
-        acc = acc + bf16_to_f32(k_rows[t])
+        acc = acc + _f32(k_rows[t])
     mean = acc / np.float32(n)               # IEEE fp32 division
     return f32_to_bf16_rne(mean)
 
@@ -42,7 +48,7 @@ def index_keys(k_rows: np.ndarray, ctx_len: int, block_size: int) -> np.ndarray:
     out = np.empty((nb, d), np.uint16)
     n_full = ctx_len // block_size
     if n_full:
-        blocks = bf16_to_f32(k_rows[: n_full * block_size]).reshape(n_full, block_size, d)
+        blocks = _f32(k_rows[: n_full * block_size]).reshape(n_full, block_size, d)
         acc = np.zeros((n_full, d), np.float32)
         for t in range(block_size):
             acc = acc + blocks[:, t, :]

@@ -19,7 +19,9 @@ least important blocks by the scores that made its selection (see oracle.cache).
 restore() save and put back every unit's cache state and pending selection (speculative
 rollback, KV-cache overview, section 6.1).  With w.score_mode == "bound" blocks are summarised by
 their per-dimension [max | min] keys and scored by the query-aware upper bound (oracle.bound)
-instead of the block-mean key.
+instead of the block-mean key.  With w.kv_dtype == "fp8" the history holds E4M3 codes (oracle.fp8):
+keys and values are decode(code) * k_scale / v_scale, the index keys sum their fp32 values, and an
+appended token is quantised on arrival.
 
 Parity-relevant outputs are recorded per unit (UnitRecord) and per layer (stats()).
 """
@@ -29,6 +31,8 @@ import numpy as np
 
 from .attention import attend
 from .bound import block_scores_bound, index_minmax, index_minmax_block
+from .bf16 import bf16_to_f32
+from .fp8 import dequantize_f32, e4m3_decode, quantize
 from .cache import PrefetchResult, UnitCache, UpdateResult, cache_restore, cache_update, layer_prefetch
 from .index_keys import index_key_block, index_keys
 from .scores import block_scores
@@ -55,6 +59,9 @@ class OracleDecoder:
             raise ValueError("lookahead mode is defined without append and without prefetch")
         self.w = w
         self.bound = getattr(w, "score_mode", "mean") == "bound"
+        self.fp8 = getattr(w, "kv_dtype", "bf16") == "fp8"
+        if self.fp8 and (self.bound or w.v_shares_k):
+            raise ValueError("FP8 history is defined for block-mean scoring of separate K and V")
         self.reqs = list(range(w.n_req)) if reqs is None else list(reqs)
         self.L = {r: int(ctx_len[r]) for r in self.reqs}
         self.k, self.v, self.ik, self.cache, self.pending = {}, {}, {}, {}, {}
@@ -70,7 +77,7 @@ class OracleDecoder:
                         ik[:nb] = index_minmax(self.k[u], self.L[r], w.block_size)
                     else:
                         ik = np.zeros((w.max_blocks, w.d_k), np.uint16)
-                        ik[:nb] = index_keys(self.k[u], self.L[r], w.block_size)
+                        ik[:nb] = index_keys(self.key_values(u), self.L[r], w.block_size)
                     self.ik[u] = ik
                     self.cache[u] = UnitCache(w.cap_blocks, w.max_blocks)
                     self.pending[u] = None
@@ -82,7 +89,12 @@ class OracleDecoder:
 
     def row_bytes(self) -> int:
         w = self.w
-        return 2 * (w.d_k + (0 if w.v_shares_k else w.d_v))
+        return (1 if self.fp8 else 2) * (w.d_k + (0 if w.v_shares_k else w.d_v))
+
+    def key_values(self, u, rows=slice(None)):
+        """Key rows for the index: bf16 patterns, or fp32 values of FP8 codes."""
+        k = self.k[u][rows]
+        return dequantize_f32(k, self.w.k_scale) if self.fp8 else k
 
     def tokens(self, u, sel):
         w, (l, r, h) = self.w, u
@@ -93,6 +105,9 @@ class OracleDecoder:
             pos = np.concatenate([np.arange(b * bs, min((b + 1) * bs, L)) for b in sel])
         k = self.k[u][pos]
         v = k[:, : w.d_v] if w.v_shares_k else self.v[u][pos]
+        if self.fp8:
+            k = e4m3_decode(k) * float(w.k_scale)
+            v = e4m3_decode(v) * float(w.v_scale)
         return k, v
 
     def _score_select(self, u, rows):
@@ -107,12 +122,15 @@ class OracleDecoder:
     def _append(self, u, k_new, v_new):
         w, r = self.w, u[1]
         p = self.L[r] - 1
+        if self.fp8:
+            k_new = quantize(bf16_to_f32(k_new), w.k_scale)
+            v_new = quantize(bf16_to_f32(v_new), w.v_scale)
         self.k[u][p] = k_new
         if not w.v_shares_k:
             self.v[u][p] = v_new
         b = p // w.block_size
         summarise = index_minmax_block if self.bound else index_key_block
-        self.ik[u][b] = summarise(self.k[u][b * w.block_size: self.L[r]])
+        self.ik[u][b] = summarise(self.key_values(u, slice(b * w.block_size, self.L[r])))
 
     def step(self, q, score_q=None, new_k=None, new_v=None):
         """q: [N_l][B][H_q][D_k] bf16; score_q: [N_l][B][n_draft][H_q][D_k] drafts (lookahead);

@@ -32,10 +32,12 @@ class KvsConfig(ctypes.Structure):
                 ("budget_blocks", ctypes.c_int), ("n_sink", ctypes.c_int), ("n_recent", ctypes.c_int),
                 ("cap_blocks", ctypes.c_int), ("max_score_q", ctypes.c_int), ("lookahead", ctypes.c_int),
                 ("max_prefetch", ctypes.c_int), ("softmax_scale", ctypes.c_float),
-                ("wait_timeout_us", ctypes.c_uint), ("evict_policy", ctypes.c_int), ("score_mode", ctypes.c_int)]
+                ("wait_timeout_us", ctypes.c_uint), ("evict_policy", ctypes.c_int), ("score_mode", ctypes.c_int),
+                ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 EVICT_POLICY = {"lru": 0, "importance": 1}
 SCORE_MODE = {"mean": 0, "bound": 1}
+KV_DTYPE = {"bf16": 0, "fp8": 1}
 
 
 class KvsStats(ctypes.Structure):
@@ -76,6 +78,7 @@ _SIGS = {
     "kvs_launch_count": (ctypes.c_ulonglong, [_P]),
     "kvs_select_blocks_noalloc": (_I, [ctypes.POINTER(KvsConfig), _P, _I, _P, _P, _P, _P, _P, _P]),
     "kvs_probe_host_read": (_I, [_P, ctypes.c_size_t, _P, _I, _I, _I, _I, _P, _P]),
+    "kvs_quantize_e4m3": (_I, [_P, _P, ctypes.c_size_t, ctypes.c_float, _P]),
 }
 
 KERNEL_IDS = {"score": 1, "topk": 2, "update": 3, "fetch": 4, "attn": 5, "prefetch": 6, "append": 7, "index": 8}
@@ -121,7 +124,8 @@ def make_config(w, max_score_q: int | None = None, max_prefetch: int = 0, wait_t
                      w.max_ctx, w.budget_blocks, w.n_sink, w.n_recent, w.cap_blocks,
                      max_score_q if max_score_q is not None else max(1, w.n_score_q), int(w.lookahead), max_prefetch,
                      float(w.softmax_scale), wait_timeout_us, EVICT_POLICY[getattr(w, "evict_policy", "lru")],
-                     SCORE_MODE[getattr(w, "score_mode", "mean")])
+                     SCORE_MODE[getattr(w, "score_mode", "mean")], KV_DTYPE[getattr(w, "kv_dtype", "bf16")],
+                     float(getattr(w, "k_scale", 1.0)), float(getattr(w, "v_scale", 1.0)))
 
 
 class Context:
@@ -227,16 +231,19 @@ class Context:
         return k.value, v.value
 
     def slot_pool_tensors(self, layer):
-        """Views (int16 bf16 patterns) of one layer's slot pools inside the workspace tensor:
+        """Views (int16 bf16 patterns, or uint8 E4M3 codes) of one layer's slot pools inside the workspace tensor:
         K [units][C][bs][d_k] and V [units][C][bs][d_v] (None when V shares the K row)."""
         c = self.cfg
         kp, vp = self.slot_pools(layer)
         base = self.workspace.data_ptr()
 
+        torch = __import__("torch")
+        fp8 = c.kv_dtype == KV_DTYPE["fp8"]
+
         def view(ptr, d):
-            n = self.units * c.cap_blocks * c.block_size * d * 2
+            n = self.units * c.cap_blocks * c.block_size * d * (1 if fp8 else 2)
             off = ptr - base
-            return self.workspace[off: off + n].view(dtype=__import__("torch").int16).view(
+            return self.workspace[off: off + n].view(dtype=torch.uint8 if fp8 else torch.int16).view(
                 self.units, c.cap_blocks, c.block_size, d)
 
         return view(kp, c.d_k), (None if vp is None else view(vp, c.d_v))
@@ -425,6 +432,34 @@ def probe_host_read(h_base, region_bytes: int, offsets, item_bytes: int, n_ctas:
     from page-locked, device-mapped host memory (diagnostics for the host-link peak)."""
     _check(lib().kvs_probe_host_read(_ptr(h_base), region_bytes, _ptr(offsets), int(offsets.numel()), item_bytes,
                                      n_ctas, threads, _ptr(sink), _stream(stream)), "kvs_probe_host_read")
+
+
+def quantize_e4m3(src, dst, scale: float, stream=None) -> None:
+    """kvs_quantize_e4m3 on device tensors: dst (uint8, n) = E4M3 codes of src (bf16 patterns, n) / scale."""
+    n = src.numel()
+    if dst.numel() != n:
+        raise ValueError("quantize_e4m3: sizes differ")
+    _check(lib().kvs_quantize_e4m3(_ptr(src), _ptr(dst), n, float(scale), _stream(stream)), "kvs_quantize_e4m3")
+
+
+def quantize_history_e4m3(src_host, dst_host, scale: float, chunk: int = 1 << 28) -> None:
+    """E4M3 codes of a host bf16 history into a host uint8 array of the same shape, through the GPU
+    in chunks (each chunk copied in, quantised by kvs_quantize_e4m3, copied back)."""
+    import torch
+    s = src_host.view(-1)
+    d = dst_host.view(-1)
+    if s.numel() != d.numel():
+        raise ValueError("quantize_history_e4m3: sizes differ")
+    n = s.numel()
+    step = min(chunk, n)
+    bs = torch.empty(step, dtype=torch.int16, device="cuda")
+    bd = torch.empty(step, dtype=torch.uint8, device="cuda")
+    for i in range(0, n, step):
+        m = min(step, n - i)
+        bs[:m].copy_(s[i:i + m])
+        quantize_e4m3(bs[:m], bd[:m], scale)
+        d[i:i + m].copy_(bd[:m])
+    torch.cuda.synchronize()
 
 
 def version() -> str:

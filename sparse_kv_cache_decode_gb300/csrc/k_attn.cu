@@ -667,6 +667,7 @@ int attention_split(const Dims& d, int* n_split_out, int* bps_out) {
 }
 
 int attention_supported(const Dims& d) {
+  if (d.fp8) return attention_tma_supported(d);   // E4M3 tiles: the TMA kernel only
   if (d.dv % kDVC) return 0;
   if (d.v_shares_k) return d.dk == 576 && d.dv <= 512 && (d.G <= 16 || d.G == 128);
   return d.dk == 128 && d.dv == 128 && d.G <= 16;
@@ -678,6 +679,7 @@ cudaError_t launch_attention(const Dims& d, const Layer& L, const __nv_bfloat16*
   if (!attention_supported(d)) return cudaErrorInvalidValue;
   if (attention_tma_supported(d) && L.tmK && L.tmV)
     return launch_attention_tma(d, L, L.tmK, L.tmV, q, sel, slot_of_sel, nsel, ctx_len, out, s);
+  if (d.fp8) return cudaErrorInvalidValue;
   if (d.v_shares_k) {
     if (d.G <= 16) return launch_attn_t<576, 1, true>(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, s);
     if (mla_path(d)) return launch_attn_mla(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, s);

@@ -14,7 +14,12 @@
 // The CTA's block ids, slots and the units' lengths are staged in shared memory first, so the
 // producer issues tensor loads without waiting on global memory.
 // Every mbarrier wait is bounded by the context's wait timeout (KVS_ERR_TIMEOUT on expiry).
+// E4M3 slot pools: a stage holds 16 rows x 128 codes of K and of V (one 128-byte box each); the
+// consumer warp widens its tile into a bf16 copy of the same swizzled layout in its own staging
+// area (every E4M3 value is exact in bf16), releases the stage, and runs the same tiles; the K
+// scale joins the softmax scale and the V scale is applied at the merge.
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "kvs_common.cuh"
 #include "kvs_ptx.cuh"
@@ -31,7 +36,24 @@ constexpr int kTile = 16 * D * 2;           // bytes of a 16-row K or V tile (tw
 constexpr int kStage = 2 * kTile;
 constexpr int kMaxPos = 1024;               // positions (selected blocks) per CTA
 constexpr int kMaxUnits = 64;               // units one CTA's range may touch
-constexpr int kSmem = kStages * kStage + 1024 + 2 * kStages * 8 + 64 + kMaxPos * 8 + kMaxUnits * 8;
+// Shared memory of the kernel: the stage ring, per-warp bf16 staging (E4M3 pools only), barriers,
+// flags and the CTA's block and slot lists.
+template <bool FP8>
+struct Smem {
+  static constexpr int kStageBytes = FP8 ? 2 * 16 * D : kStage;
+  static constexpr int kRing = kStages * kStageBytes;
+  static constexpr int kStaging = FP8 ? kConsumers * kStage : 0;
+  static constexpr int kBars = kRing + kStaging;
+  static constexpr int kTotal = kBars + 1024 + 2 * kStages * 8 + 64 + kMaxPos * 8 + kMaxUnits * 8;
+};
+
+// Two E4M3 codes (bits 0-7, 8-15) -> bf16x2, exactly (through f16, which holds every E4M3 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  return pack_bf16x2(f.x, f.y);
+}
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Plan {
@@ -57,7 +79,7 @@ __host__ __device__ inline Plan make_plan(const Dims& d, int n_sm) {
 
 __device__ __forceinline__ int rows_present(int len, int blk, int bs) { return min(bs, len - blk * bs); }
 
-template <bool ROWS8>  // G <= 8: fragment rows 8..15 are zero at compile time
+template <bool ROWS8, bool FP8>  // ROWS8: G <= 8, fragment rows 8..15 are zero at compile time
 __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
     attn_tma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, Dims d,
                     Layer L, const __nv_bfloat16* __restrict__ q, const int* __restrict__ sel,
@@ -66,11 +88,12 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
   kvs_pdl_entry();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStage);
+  using Lay = Smem<FP8>;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBars);
   uint64_t* empty = full + kStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
   volatile int* last_flag = abort_flag + 1;   // this CTA finished a unit last (consumers)
-  int* m_blk = reinterpret_cast<int*>(smem + kStages * kStage + 2 * kStages * 8 + 64);   // [kMaxPos], -1: none
+  int* m_blk = reinterpret_cast<int*>(smem + Lay::kBars + 2 * kStages * 8 + 64);       // [kMaxPos], -1: none
   int* m_slot = m_blk + kMaxPos;                                                       // [kMaxPos]
   int* u_len = m_slot + kMaxPos;                                                       // [kMaxUnits]
   int* u_n = u_len + kMaxUnits;                                                        // [kMaxUnits]
@@ -143,12 +166,17 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
         }
         if (*abort_flag) { ok = false; break; }
         const int y = ((u * d.C + slot) * d.bs) + sub * 16;
-        unsigned char* st = smem + s * kStage;
-        mbar_arrive_expect_tx(&full[s], kStage);
-        tma_load_2d(st, &tmK, 0, y, &full[s]);
-        tma_load_2d(st + 16 * 128, &tmK, 64, y, &full[s]);
-        tma_load_2d(st + kTile, &tmV, 0, y, &full[s]);
-        tma_load_2d(st + kTile + 16 * 128, &tmV, 64, y, &full[s]);
+        unsigned char* st = smem + s * Lay::kStageBytes;
+        mbar_arrive_expect_tx(&full[s], Lay::kStageBytes);
+        if (FP8) {
+          tma_load_2d(st, &tmK, 0, y, &full[s]);
+          tma_load_2d(st + 16 * 128, &tmV, 0, y, &full[s]);
+        } else {
+          tma_load_2d(st, &tmK, 0, y, &full[s]);
+          tma_load_2d(st + 16 * 128, &tmK, 64, y, &full[s]);
+          tma_load_2d(st + kTile, &tmV, 0, y, &full[s]);
+          tma_load_2d(st + kTile + 16 * 128, &tmV, 64, y, &full[s]);
+        }
         ++k;
       }
     }
@@ -164,7 +192,7 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
 
   // -------------------------------------------------------------------- consumers
   const int G = d.G;
-  const float sl2 = d.scale * kLog2e;
+  const float sl2 = FP8 ? d.scale * d.k_scale * kLog2e : d.scale * kLog2e;
   int k = 0;          // position in the CTA's tile sequence
   bool ok = true;
   for (int u = u_first; u <= u_last; ++u) {
@@ -207,6 +235,31 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
           continue;
         }
         const unsigned char* kt = smem + s * kStage;
+        if (FP8) {
+          // widen the stage's K and V codes into this warp's bf16 staging (same swizzled layout as a
+          // bf16 stage), then release the stage
+          unsigned char* stg = smem + Lay::kRing + warp * kStage;
+          const unsigned char* src = smem + s * Lay::kStageBytes;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int qi = lane + 32 * j;
+            const int tile = qi >> 7, row = (qi >> 3) & 15, c16 = qi & 7;
+            const uint4 v = *reinterpret_cast<const uint4*>(src + tile * 2048 + row * 128 + ((c16 ^ (row & 7)) << 4));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              o[2 * e] = e4m3x2_to_bf16x2(w[e] & 0xffffu);
+              o[2 * e + 1] = e4m3x2_to_bf16x2(w[e] >> 16);
+            }
+            unsigned char* dst = stg + tile * kTile;
+            *reinterpret_cast<uint4*>(dst + sw128_offset(row, c16 * 16, 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + sw128_offset(row, c16 * 16 + 8, 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+          kt = stg;
+        }
         const unsigned char* vt = kt + kTile;
         const int valid_rows = rows - sub * 16;     // tokens of this tile before the context end
         // S = Q K^T
@@ -287,7 +340,7 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
           mma_bf16_16816(oacc[nd + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (!FP8 && lane == 0) mbar_arrive(&empty[s]);
       }
     }
     // partial state of this warp for unit u
@@ -346,7 +399,7 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
         }
 #pragma unroll
         for (int o = 16; o; o >>= 1) lpart += __shfl_xor_sync(0xffffffffu, lpart, o);
-        const float inv = lpart > 0.f ? 1.f / lpart : 0.f;
+        const float inv = lpart > 0.f ? (FP8 ? d.v_scale / lpart : 1.f / lpart) : 0.f;
         float4 res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         reinterpret_cast<float4*>(out + ((size_t)r_out * d.Hq + h_out * G + g) * d.dv)[lane] = res;
       }
@@ -370,18 +423,20 @@ int attention_tma_partials(const Dims& d) { return make_plan(d, sm_count()).max_
 cudaError_t launch_attention_tma(const Dims& d, const Layer& L, const CUtensorMap* tmK, const CUtensorMap* tmV,
                                  const __nv_bfloat16* q, const int* sel, const int* slot_of_sel, const int* nsel,
                                  const int* ctx_len, float* out, cudaStream_t s) {
-  {
-    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(attn_tma_kernel<true>), kSmem);
-    if (e == cudaSuccess) e = set_max_dynamic_smem(reinterpret_cast<const void*>(attn_tma_kernel<false>), kSmem);
-    if (e != cudaSuccess) return e;
-  }
   Plan plan = make_plan(d, sm_count());
-  if (d.G <= 8)
-    launch_pdl(attn_tma_kernel<true>, dim3(plan.n_cta), dim3((kConsumers + 1) * 32), kSmem, s, *tmK, *tmV, d, L, q, sel,
-               slot_of_sel, nsel, ctx_len, out, plan);
+  auto go = [&](auto kern, int smem) {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3(plan.n_cta), dim3((kConsumers + 1) * 32), (size_t)smem, s, *tmK, *tmV, d, L, q, sel,
+                      slot_of_sel, nsel, ctx_len, out, plan);
+  };
+  cudaError_t e;
+  if (d.fp8)
+    e = d.G <= 8 ? go(attn_tma_kernel<true, true>, Smem<true>::kTotal) : go(attn_tma_kernel<false, true>, Smem<true>::kTotal);
   else
-    launch_pdl(attn_tma_kernel<false>, dim3(plan.n_cta), dim3((kConsumers + 1) * 32), kSmem, s, *tmK, *tmV, d, L, q, sel,
-               slot_of_sel, nsel, ctx_len, out, plan);
+    e = d.G <= 8 ? go(attn_tma_kernel<true, false>, Smem<false>::kTotal)
+                 : go(attn_tma_kernel<false, false>, Smem<false>::kTotal);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

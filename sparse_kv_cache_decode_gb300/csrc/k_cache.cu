@@ -464,8 +464,9 @@ __global__ void __launch_bounds__(kFetchThreads) fetch_kernel(Dims d, Layer L, c
   if (tid == 0) s_off[d.U] = total;
   __syncthreads();
 
-  const int vk = d.bs * d.dk / 8;                         // 16-byte vectors of K in a full block
-  const int vv = d.v_shares_k ? 0 : d.bs * d.dv / 8;
+  const int kvec = d.dk * d.ebytes / 16, vvec = d.dv * d.ebytes / 16;   // 16-byte vectors of a K / V row
+  const int vk = d.bs * kvec;                             // of K in a full block
+  const int vv = d.v_shares_k ? 0 : d.bs * vvec;
   const int vpi = vk + vv;
   const int ipb = max(1, 512 / vpi);                      // items per warp batch
   const int n_batches = (total + ipb - 1) / ipb;
@@ -507,15 +508,15 @@ __global__ void __launch_bounds__(kFetchThreads) fetch_kernel(Dims d, Layer L, c
         dst[k] = nullptr;
         if (f < nv) {
           if (w < vk) {
-            if (w < rows * d.dk / 8) {
-              src[k] = reinterpret_cast<const uint4*>(L.host_k + sr * d.dk) + w;
-              dst[k] = reinterpret_cast<uint4*>(L.kpool + dr * d.dk) + w;
+            if (w < rows * kvec) {
+              src[k] = reinterpret_cast<const uint4*>(L.host_k) + sr * kvec + w;
+              dst[k] = reinterpret_cast<uint4*>(L.kpool) + dr * kvec + w;
             }
           } else {
             const int w2 = w - vk;
-            if (w2 < rows * d.dv / 8) {
-              src[k] = reinterpret_cast<const uint4*>(L.host_v + sr * d.dv) + w2;
-              dst[k] = reinterpret_cast<uint4*>(L.vpool + dr * d.dv) + w2;
+            if (w2 < rows * vvec) {
+              src[k] = reinterpret_cast<const uint4*>(L.host_v) + sr * vvec + w2;
+              dst[k] = reinterpret_cast<uint4*>(L.vpool) + dr * vvec + w2;
             }
           }
         }

@@ -1,5 +1,9 @@
 // Block summaries (the mean key, or the per-dimension [max | min] of the keys) and the per-step
 // append of one token.
+#include <math.h>
+
+#include <algorithm>
+
 #include "kvs_common.cuh"
 #include "kvs_ptx.cuh"
 
@@ -26,6 +30,8 @@ __global__ void __launch_bounds__(256) index_build_kernel(Dims d, Layer L, __nv_
   const int t0 = b * d.bs, t1 = min(t0 + d.bs, len);
   const int nchunk = d.dk / 4;
   const __nv_bfloat16* rows = L.host_k + (size_t)u * d.max_ctx * d.dk;
+  // E4M3 history: byte rows, each code widened to fp32(decode(code) * k_scale)
+  const unsigned char* rows8 = reinterpret_cast<const unsigned char*>(L.host_k) + (size_t)u * d.max_ctx * d.dk;
   float acc[CHUNKS][4], mx[CHUNKS][4], mn[CHUNKS][4];
 #pragma unroll
   for (int c = 0; c < CHUNKS; ++c)
@@ -37,8 +43,18 @@ __global__ void __launch_bounds__(256) index_build_kernel(Dims d, Layer L, __nv_
     for (int c = 0; c < CHUNKS; ++c) {
       int ch = lane + 32 * c;
       if (ch < nchunk) {
-        uint2 v = row[ch];
-        const float x[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
+        float x[4];
+        if (d.fp8) {
+          const uint32_t c4 = *reinterpret_cast<const uint32_t*>(rows8 + (size_t)t * d.dk + ch * 4);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[e] = __fmul_rn(e4m3_to_f32((c4 >> (8 * e)) & 255u), d.k_scale);
+        } else {
+          const uint2 v = row[ch];
+          x[0] = bf16_lo(v.x);
+          x[1] = bf16_hi(v.x);
+          x[2] = bf16_lo(v.y);
+          x[3] = bf16_hi(v.y);
+        }
         if (d.bound) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -108,6 +124,45 @@ __global__ void __launch_bounds__(128) append_kernel(Dims d, Layer L, const __nv
   const int p = len - 1;
   const int b = p / d.bs, row_in_blk = p - b * d.bs;
   const int slot = L.block2slot[(size_t)u * d.nb_max + b];
+  if (d.fp8) {
+    // quantise the token (round to nearest even, saturating), store the codes in the history and
+    // the resident slot, then rebuild the block's key from the stored values
+    uint16_t* hk = reinterpret_cast<uint16_t*>(const_cast<__nv_bfloat16*>(L.host_k)) +
+                   (((size_t)u * d.max_ctx + p) * d.dk) / 2;
+    uint16_t* sk = slot >= 0 ? reinterpret_cast<uint16_t*>(L.kpool) + ((((size_t)u * d.C + slot) * d.bs + row_in_blk) * d.dk) / 2
+                             : nullptr;
+    for (int i = threadIdx.x; i < d.dk / 2; i += blockDim.x) {
+      const float a = __bfloat162float(k_new[(size_t)u * d.dk + 2 * i]);
+      const float c = __bfloat162float(k_new[(size_t)u * d.dk + 2 * i + 1]);
+      const uint16_t code = (uint16_t)f32x2_to_e4m3x2(__fdiv_rn(a, d.k_scale), __fdiv_rn(c, d.k_scale));
+      hk[i] = code;
+      if (sk) sk[i] = code;
+    }
+    uint16_t* hv = reinterpret_cast<uint16_t*>(const_cast<__nv_bfloat16*>(L.host_v)) +
+                   (((size_t)u * d.max_ctx + p) * d.dv) / 2;
+    uint16_t* sv = slot >= 0 ? reinterpret_cast<uint16_t*>(L.vpool) + ((((size_t)u * d.C + slot) * d.bs + row_in_blk) * d.dv) / 2
+                             : nullptr;
+    for (int i = threadIdx.x; i < d.dv / 2; i += blockDim.x) {
+      const float a = __bfloat162float(v_new[(size_t)u * d.dv + 2 * i]);
+      const float c = __bfloat162float(v_new[(size_t)u * d.dv + 2 * i + 1]);
+      const uint16_t code = (uint16_t)f32x2_to_e4m3x2(__fdiv_rn(a, d.v_scale), __fdiv_rn(c, d.v_scale));
+      hv[i] = code;
+      if (sv) sv[i] = code;
+    }
+    const unsigned char* rows8 =
+        slot >= 0 ? reinterpret_cast<const unsigned char*>(L.kpool) + ((size_t)u * d.C + slot) * d.bs * d.dk
+                  : reinterpret_cast<const unsigned char*>(L.host_k) + ((size_t)u * d.max_ctx + (size_t)b * d.bs) * d.dk;
+    const float n = (float)(row_in_blk + 1);
+    for (int i = threadIdx.x; i < d.dk; i += blockDim.x) {
+      float acc = 0.f;
+      for (int t = 0; t < row_in_blk; ++t) acc = __fadd_rn(acc, __fmul_rn(e4m3_to_f32(rows8[(size_t)t * d.dk + i]), d.k_scale));
+      const float kn = __bfloat162float(k_new[(size_t)u * d.dk + i]);
+      const uint32_t code = f32x2_to_e4m3x2(__fdiv_rn(kn, d.k_scale), 0.f) & 255u;
+      acc = __fadd_rn(acc, __fmul_rn(e4m3_to_f32(code), d.k_scale));
+      index[((size_t)u * d.nb_max + b) * d.didx + i] = __float2bfloat16_rn(__fdiv_rn(acc, n));
+    }
+    return;
+  }
   {
     uint4* hk = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(L.host_k) + ((size_t)u * d.max_ctx + p) * d.dk);
     const uint4* kn = reinterpret_cast<const uint4*>(k_new + (size_t)u * d.dk);
@@ -198,9 +253,41 @@ __global__ void advance_kernel(int B, int* ctx_len) {
   if (r < B) ctx_len[r] += 1;
 }
 
+// E4M3 codes of bf16 values: 8 per thread (one 16-byte load, one 8-byte store), the tail one by one.
+__global__ void __launch_bounds__(256) quantize_e4m3_kernel(const __nv_bfloat16* __restrict__ src, uint8_t* __restrict__ dst,
+                                                            size_t n, float scale) {
+  const size_t n8 = n / 8;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const uint4 v = reinterpret_cast<const uint4*>(src)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[2 * h]), scale), __fdiv_rn(bf16_hi(w[2 * h]), scale));
+      const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[2 * h + 1]), scale), __fdiv_rn(bf16_hi(w[2 * h + 1]), scale));
+      out[h] = lo | (hi << 16);
+    }
+    reinterpret_cast<uint2*>(dst)[i] = make_uint2(out[0], out[1]);
+  }
+  for (size_t i = n8 * 8 + (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    dst[i] = (uint8_t)(f32x2_to_e4m3x2(__fdiv_rn(__bfloat162float(src[i]), scale), 0.f) & 255u);
+}
+
 cudaError_t launch_advance(int B, int* ctx_len, cudaStream_t s) {
   launch_pdl(advance_kernel, dim3((B + 127) / 128), dim3(128), 0, s, B, ctx_len);
   return cudaGetLastError();
 }
 
 }  // namespace kvs
+
+extern "C" kvs_status kvs_quantize_e4m3(const void* d_src_bf16, void* d_dst, size_t n, float scale, kvs_stream_t stream) {
+  if (!d_src_bf16 || !d_dst || !(scale > 0.f) || isinf(scale)) return KVS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(d_src_bf16) & 15u) || (reinterpret_cast<uintptr_t>(d_dst) & 7u)) return KVS_ERR_INVALID_ARG;
+  if (n == 0) return KVS_OK;
+  const size_t n8 = n / 8 + 1;
+  const int blocks = (int)std::min<size_t>((n8 + 255) / 256, 4096);
+  kvs::quantize_e4m3_kernel<<<blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(d_src_bf16), static_cast<uint8_t*>(d_dst), n, scale);
+  return cudaGetLastError() == cudaSuccess ? KVS_OK : KVS_ERR_CUDA;
+}

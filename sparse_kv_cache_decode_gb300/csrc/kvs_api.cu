@@ -77,6 +77,12 @@ bool fill_dims(const kvs_config* c, Dims* d) {
   if (!(c->softmax_scale >= 0.f) || isinf(c->softmax_scale)) return false;
   if (c->evict_policy != KVS_EVICT_LRU && c->evict_policy != KVS_EVICT_IMPORTANCE) return false;
   if (c->score_mode != KVS_SCORE_MEAN && c->score_mode != KVS_SCORE_BOUND) return false;
+  if (c->kv_dtype != KVS_KV_BF16 && c->kv_dtype != KVS_KV_FP8_E4M3) return false;
+  if (c->kv_dtype == KVS_KV_FP8_E4M3) {
+    // E4M3 history: block-mean scoring, separate K and V, rows of whole 16-byte vectors
+    if (c->score_mode != KVS_SCORE_MEAN || c->v_shares_k || c->d_k % 16 || c->d_v % 16) return false;
+    if (!(c->k_scale >= 0.f) || !(c->v_scale >= 0.f) || isinf(c->k_scale) || isinf(c->v_scale)) return false;
+  }
   d->B = c->n_req;
   d->NL = c->n_layer;
   d->Hq = c->n_q_head;
@@ -98,7 +104,11 @@ bool fill_dims(const kvs_config* c, Dims* d) {
   d->U = c->n_req * c->n_kv_head;
   d->scale = c->softmax_scale > 0.f ? c->softmax_scale : (float)(1.0 / sqrt((double)c->d_k));
   d->timeout_us = c->wait_timeout_us ? c->wait_timeout_us : 2000000u;
-  d->row_bytes = 2 * (c->d_k + (c->v_shares_k ? 0 : c->d_v));
+  d->fp8 = c->kv_dtype == KVS_KV_FP8_E4M3;
+  d->ebytes = d->fp8 ? 1 : 2;
+  d->k_scale = d->fp8 && c->k_scale > 0.f ? c->k_scale : 1.f;
+  d->v_scale = d->fp8 && c->v_scale > 0.f ? c->v_scale : 1.f;
+  d->row_bytes = d->ebytes * (c->d_k + (c->v_shares_k ? 0 : c->d_v));
   d->evict_importance = c->evict_policy == KVS_EVICT_IMPORTANCE;
   d->bound = c->score_mode == KVS_SCORE_BOUND;
   d->didx = d->bound ? 2 * c->d_k : c->d_k;
@@ -117,8 +127,8 @@ struct Plan {
 Plan plan_of(const Dims& d) {
   Plan p;
   size_t U = d.U;
-  p.kpool = align_up(U * d.C * d.bs * (size_t)d.dk * 2);
-  p.vpool = d.v_shares_k ? 0 : align_up(U * d.C * d.bs * (size_t)d.dv * 2);
+  p.kpool = align_up(U * d.C * d.bs * (size_t)d.dk * d.ebytes);
+  p.vpool = d.v_shares_k ? 0 : align_up(U * d.C * d.bs * (size_t)d.dv * d.ebytes);
   p.b2s = align_up(U * d.nb_max * 4);
   p.s2b = align_up(U * d.C * 4);
   p.stamp = align_up(U * d.C * 4);
@@ -234,9 +244,10 @@ inline cudaStream_t S(kvs_stream_t s) { return reinterpret_cast<cudaStream_t>(s)
 }  // namespace
 
 namespace kvs {
-// 2D tensor map over a row-major bf16 matrix [rows][inner], boxes of box_inner x box_rows with the
-// 128-byte swizzle (box_inner * 2 must be 128).
-bool make_tmap_2d(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+// 2D tensor map over a row-major matrix [rows][inner] of bf16 (elem_bytes 2) or bytes (1), boxes of
+// box_inner x box_rows with the 128-byte swizzle (box_inner * elem_bytes must be 128).
+bool make_tmap_2d(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+                  int elem_bytes) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -249,10 +260,11 @@ bool make_tmap_2d(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows, uin
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * elem_bytes};
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+  CUresult r = encode(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base,
+                      dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -261,9 +273,10 @@ bool make_tmap_2d(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows, uin
 
 namespace {
 
-// The slot pools as [U*C*bs][d] with 64 x 16 boxes (the TMA attention kernel's tiles).
-bool make_pool_map(CUtensorMap* m, void* base, size_t rows, int d) {
-  return kvs::make_tmap_2d(m, base, (uint64_t)d, (uint64_t)rows, 64, 16);
+// The slot pools as [U*C*bs][d] with 16-row boxes of 128 bytes: 64 bf16 or 128 E4M3 columns (the
+// TMA attention kernel's tiles).
+bool make_pool_map(CUtensorMap* m, void* base, size_t rows, int d, int elem_bytes) {
+  return kvs::make_tmap_2d(m, base, (uint64_t)d, (uint64_t)rows, 128 / elem_bytes, 16, elem_bytes);
 }
 
 }  // namespace
@@ -364,8 +377,8 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
     c->tmaps.resize(2 * (size_t)d.NL);
     const size_t rows = (size_t)d.U * d.C * d.bs;
     for (int l = 0; l < d.NL; ++l) {
-      if (!make_pool_map(&c->tmaps[2 * l], c->layers[l].kpool, rows, d.dk) ||
-          !make_pool_map(&c->tmaps[2 * l + 1], c->layers[l].vpool, rows, d.dv)) {
+      if (!make_pool_map(&c->tmaps[2 * l], c->layers[l].kpool, rows, d.dk, d.ebytes) ||
+          !make_pool_map(&c->tmaps[2 * l + 1], c->layers[l].vpool, rows, d.dv, d.ebytes)) {
         c->tmaps.clear();
         break;
       }
@@ -481,14 +494,18 @@ kvs_status kvs_bind_host_kv(kvs_ctx* c, void* h_k, void* h_v) {
   const Dims& d = c->d;
   // touch every page once from the device: the first fetches then do not pay for translations
   const size_t rows = (size_t)d.NL * d.U * d.max_ctx;
-  cudaError_t e = launch_touch_pages(dk, rows * d.dk * 2, c->err + 1, 0);
-  if (e == cudaSuccess && dv) e = launch_touch_pages(dv, rows * d.dv * 2, c->err + 1, 0);
+  cudaError_t e = launch_touch_pages(dk, rows * d.dk * d.ebytes, c->err + 1, 0);
+  if (e == cudaSuccess && dv) e = launch_touch_pages(dv, rows * d.dv * d.ebytes, c->err + 1, 0);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return KVS_ERR_CUDA;
   for (int l = 0; l < d.NL; ++l) {
     size_t unit_rows = (size_t)d.U * d.max_ctx;
-    c->layers[l].host_k = c->host_k_dev + (size_t)l * unit_rows * d.dk;
-    c->layers[l].host_v = dv ? c->host_v_dev + (size_t)l * unit_rows * d.dv : nullptr;
+    // element offsets of bf16 pointers; E4M3 rows are half as many bytes
+    c->layers[l].host_k = reinterpret_cast<const __nv_bfloat16*>(reinterpret_cast<const unsigned char*>(c->host_k_dev) +
+                                                                 (size_t)l * unit_rows * d.dk * d.ebytes);
+    c->layers[l].host_v = dv ? reinterpret_cast<const __nv_bfloat16*>(reinterpret_cast<const unsigned char*>(c->host_v_dev) +
+                                                                      (size_t)l * unit_rows * d.dv * d.ebytes)
+                             : nullptr;
   }
   return KVS_OK;
 }

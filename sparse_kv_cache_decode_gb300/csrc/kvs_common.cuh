@@ -19,10 +19,13 @@ struct Dims {
   int evict_importance;  // victims least important first (else least recently used)
   int bound;             // blocks summarised by [max | min] keys and scored by the upper bound
   int didx;              // index row width: dk (block-mean key) or 2 * dk ([max | min] summary)
+  int fp8;               // history and slot pools hold E4M3 codes (1 byte per element)
+  int ebytes;            // bytes per stored K/V element: 2 (bf16) or 1 (E4M3)
+  float k_scale, v_scale;
   int U;                 // units per layer = B * Hkv
   float scale;
   unsigned timeout_us;
-  int row_bytes;         // host bytes moved per token: 2 * (dk + (v_shares_k ? 0 : dv))
+  int row_bytes;         // host bytes moved per token: ebytes * (dk + (v_shares_k ? 0 : dv))
 };
 
 // Device pointers of one layer.
@@ -124,6 +127,24 @@ __device__ __forceinline__ uint4 score_row_chunk(const __nv_bfloat16* qrow, int 
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// E4M3 code -> fp32 value (exact): normals (1 + m/8) 2^(e-7), subnormals m 2^-9, S.1111.111 NaN.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u, s = (c & 0x80u) << 24;
+  if (e == 15u && m == 7u) return __uint_as_float(0x7fc00000u | s);
+  if (e == 0u) {
+    const float v = (float)m * 0.001953125f;                           // exact; m = 0 gives +-0
+    return s ? -v : v;
+  }
+  return __uint_as_float(s | ((e + 120u) << 23) | (m << 20));
+}
+
+// Two fp32 values -> two E4M3 codes (round to nearest even, saturating to +-448): lo in bits 0-7.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // -------------------------------------------------------------- launchers (one per kernel TU)
 cudaError_t launch_index_build(const Dims& d, const Layer& L, __nv_bfloat16* index, const int* ctx_len,
                                cudaStream_t s);
@@ -157,7 +178,8 @@ cudaError_t launch_attention(const Dims& d, const Layer& L, const __nv_bfloat16*
                              const int* slot_of_sel, const int* nsel, const int* ctx_len, float* out,
                              cudaStream_t s);
 int attention_supported(const Dims& d);
-bool make_tmap_2d(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows);
+bool make_tmap_2d(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+                  int elem_bytes = 2);
 int score_tc_supported(const Dims& d, int nq);
 cudaError_t launch_score_tc(const Dims& d, const __nv_bfloat16* index, const __nv_bfloat16* q, int nq,
                             const int* ctx_len, float* scores, unsigned* err, cudaStream_t s);

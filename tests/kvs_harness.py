@@ -28,7 +28,23 @@ class GpuCase:
         kshape = (NL, B, Hkv, w.max_ctx, w.d_k)
         vshape = None if w.v_shares_k else (NL, B, Hkv, w.max_ctx, w.d_v)
         self._arrays = []
-        if w.host_kv_bytes >= (1 << 30):
+        self.k_bf16 = self.v_bf16 = None
+        if getattr(w, "kv_dtype", "bf16") == "fp8":
+            # E4M3 history: the library quantises the generator's bf16 values on the GPU; the oracle
+            # quantises the same values with its own encoder (tests compare the two code arrays)
+            from oracle import bf16_to_f32
+            from oracle.fp8 import quantize
+            kb = torch.empty(kshape, dtype=torch.int16, pin_memory=True)
+            vb = torch.empty(vshape, dtype=torch.int16, pin_memory=True)
+            W.fill_kv(w, kb, vb, n_threads)
+            self.k_host = torch.empty(kshape, dtype=torch.uint8, pin_memory=True)
+            self.v_host = torch.empty(vshape, dtype=torch.uint8, pin_memory=True)
+            K.quantize_history_e4m3(kb, self.k_host, w.k_scale)
+            K.quantize_history_e4m3(vb, self.v_host, w.v_scale)
+            self.k_bf16, self.v_bf16 = kb.numpy().view(np.uint16), vb.numpy().view(np.uint16)
+            self.k_np = quantize(bf16_to_f32(self.k_bf16), w.k_scale)
+            self.v_np = quantize(bf16_to_f32(self.v_bf16), w.v_scale)
+        elif w.host_kv_bytes >= (1 << 30):
             # large histories: huge-page host arrays, released by close() (torch keeps freed
             # pinned blocks cached, which would exhaust host memory across full-size tests)
             ka = K.HostArray(kshape)
@@ -43,8 +59,9 @@ class GpuCase:
             self.k_host = torch.empty(kshape, dtype=torch.int16, pin_memory=True)
             self.v_host = None if vshape is None else torch.empty(vshape, dtype=torch.int16, pin_memory=True)
             W.fill_kv(w, self.k_host, self.v_host, n_threads)
-        self.k_np = self.k_host.numpy().view(np.uint16)
-        self.v_np = None if self.v_host is None else self.v_host.numpy().view(np.uint16)
+        if self.k_bf16 is None:
+            self.k_np = self.k_host.numpy().view(np.uint16)
+            self.v_np = None if self.v_host is None else self.v_host.numpy().view(np.uint16)
         self.ctx_lens = list(ctx_lens) if ctx_lens is not None else [w.ctx0] * B
         self.ctx_len = torch.tensor(self.ctx_lens, dtype=torch.int32, device="cuda")
         self.cfg = K.make_config(w)

@@ -11,7 +11,7 @@ def _declared():
     with open(os.path.join(ROOT, "include", "kvs.h")) as f:
         text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(kvs_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(kvs_[a-z0-9_]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")

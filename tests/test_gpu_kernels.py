@@ -45,8 +45,11 @@ def _nb(L, bs):
     return (L + bs - 1) // bs
 
 
+TINY3_FP8 = TINY3.with_(name="tiny3_fp8", kv_dtype="fp8", k_scale=0.5, v_scale=0.25)
+
+
 @pytest.mark.parametrize("w,lens", [(TINY3, [4096, 1000, 17]), (W.TINY_MLA, [4096]),
-                                    (TINY_BS64, [3000, 2999]), (MLA_G128, [2048, 333]),
+                                    (TINY_BS64, [3000, 2999]), (MLA_G128, [2048, 333]), (TINY3_FP8, [4096, 1000, 17]),
                                     (TINY3_BOUND, [4096, 1000, 17]), (TINY_BS64.with_(score_mode="bound"), [3000, 7])])
 def test_index_build_bit_exact(w, lens):
     g = GpuCase(w, lens)
@@ -55,7 +58,11 @@ def test_index_build_bit_exact(w, lens):
         for r, L in enumerate(lens):
             for h in range(w.n_kv_head):
                 nb = _nb(L, w.block_size)
-                ref = _summaries(w, g.k_np[l, r, h], L)
+                if w.kv_dtype == "fp8":
+                    from oracle.fp8 import dequantize_f32
+                    ref = index_keys(dequantize_f32(g.k_np[l, r, h], w.k_scale), L, w.block_size)
+                else:
+                    ref = _summaries(w, g.k_np[l, r, h], L)
                 np.testing.assert_array_equal(idx[l, r, h, :nb], ref, err_msg=f"unit {(l, r, h)}")
 
 
@@ -167,8 +174,8 @@ def _check_state(g, layer, caches, lens):
 def _check_slots(g, layer, caches, lens, blocks_by_unit):
     w = g.w
     kp, vp = g.ctx.slot_pool_tensors(layer)
-    kp = kp.cpu().numpy().view(np.uint16)
-    vp = None if vp is None else vp.cpu().numpy().view(np.uint16)
+    kp = kp.cpu().numpy().view(g.k_np.dtype)
+    vp = None if vp is None else vp.cpu().numpy().view(g.k_np.dtype)
     for u, blocks in blocks_by_unit.items():
         r, h = divmod(u, w.n_kv_head)
         L = lens[r]
@@ -265,7 +272,8 @@ def test_layer_prefetch_sequences_bit_exact():
 @pytest.mark.parametrize("w,lens", [(TINY3, [4096, 1000, 17]), (TINY_G8, [4096, 3001]), (TINY_BS64, [3000, 2999]),
                                     (W.TINY_MLA, [4096]), (MLA_G128, [2048, 1999]),
                                     (W.TINY.with_(name="tiny_bigbudget", n_req=2, budget_blocks=300, cap_blocks=300),
-                                     [4096, 4000])])
+                                     [4096, 4000]),
+                                    (TINY3_FP8, [4096, 1000, 17]), (TINY_G8.with_(kv_dtype="fp8", v_scale=2.0), [4096, 3001])])
 def test_sparse_decode_attention(w, lens):
     g = GpuCase(w, lens)
     U = g.ctx.units
@@ -296,6 +304,9 @@ def test_sparse_decode_attention(w, lens):
         pos = np.concatenate([np.arange(b * w.block_size, min((b + 1) * w.block_size, L)) for b in sels[u]])
         kt = g.k_np[0, r, h, pos]
         vt = kt[:, : w.d_v] if w.v_shares_k else g.v_np[0, r, h, pos]
+        if w.kv_dtype == "fp8":
+            from oracle.fp8 import e4m3_decode
+            kt, vt = e4m3_decode(kt) * float(w.k_scale), e4m3_decode(vt) * float(w.v_scale)
         heads = slice(h * w.group, (h + 1) * w.group)
         ref = attend(q[0, r, heads], kt, vt, w.softmax_scale)
         err = np.abs(got[r, heads] - ref).max()
@@ -320,3 +331,29 @@ def test_append_rejects_misaligned_token_rows():
         assert K.STATUS[e.value.status] == "KVS_ERR_INVALID_ARG"
     torch.cuda.synchronize()
     assert g.ctx.poll_error() == 0
+
+
+def test_quantize_e4m3_bit_exact():
+    """kvs_quantize_e4m3 against the oracle's E4M3 encoder (round to nearest even, saturating):
+    N(0, 1) and wide values, values near the subnormal range, exact ties, +-0 and beyond +-448."""
+    import sparse_kv_cache_decode_gb300 as K
+    from oracle import bf16_to_f32, f32_to_bf16_rne
+    from oracle.fp8 import e4m3_encode
+    rng = np.random.default_rng(21)
+    x = np.concatenate([rng.normal(size=50001), rng.normal(size=20000) * 200, rng.normal(size=20000) * 0.004,
+                        [0.0, -0.0, 448.0, 460.0, 470.0, -1e4, 17.0, 19.0, 248.0, 2.0 ** -10, 3 * 2.0 ** -10]])
+    xb = f32_to_bf16_rne(x.astype(np.float32))
+    for scale in (1.0, 0.5, 3.0):
+        src = torch.from_numpy(xb.view(np.int16)).cuda()
+        dst = torch.zeros(xb.size, dtype=torch.uint8, device="cuda")
+        K.quantize_e4m3(src, dst, scale)
+        torch.cuda.synchronize()
+        ref = e4m3_encode((bf16_to_f32(xb) / np.float32(scale)).astype(np.float32))
+        np.testing.assert_array_equal(dst.cpu().numpy(), ref, err_msg=f"scale {scale}")
+
+
+def test_fp8_history_quantised_like_the_oracle():
+    """The E4M3 history the library quantised equals the oracle's own encoding of the same values."""
+    g = GpuCase(TINY3_FP8, [4096, 1000, 17])
+    np.testing.assert_array_equal(g.k_host.numpy(), g.k_np)
+    np.testing.assert_array_equal(g.v_host.numpy(), g.v_np)

@@ -36,6 +36,12 @@ INT_CASES = [
     (W.TINY_APPEND.with_(name="tiny_app_bound_int", n_req=2, int_scale=2.0, score_mode="bound"), [4096, 1000], False),
     (W.TINY_LOOKAHEAD.with_(name="tiny_la_bound_int_cs", n_req=2, int_scale=2.0, score_mode="bound"),
      [4096, 2050], True),
+    # E4M3 history and slot pools (integer values up to 16 and power-of-two scales are exact in
+    # E4M3, so selections and state stay bit-exact), with append and in lookahead mode
+    (W.TINY_APPEND.with_(name="tiny_app_fp8_int", n_req=2, int_scale=2.0, int_clip=4.0, kv_dtype="fp8", k_scale=0.5,
+                         v_scale=2.0), [4096, 1000], False),
+    (W.TINY_LOOKAHEAD.with_(name="tiny_la_fp8_int_cs", n_req=2, int_scale=2.0, int_clip=4.0, kv_dtype="fp8"),
+     [4096, 2050], True),
 ]
 
 
@@ -103,7 +109,7 @@ def test_captured_step_replays_bit_exact(w, lens):
 
 
 GAUSS_CASES = [W.TINY.with_(n_req=2), W.TINY_LOOKAHEAD.with_(n_req=2), W.TINY_APPEND, W.TINY_PREFETCH,
-               W.TINY_MLA.with_(steps=8)]
+               W.TINY_MLA.with_(steps=8), W.TINY_APPEND.with_(name="tiny_append_fp8", kv_dtype="fp8", v_scale=0.5)]
 
 
 @pytest.mark.parametrize("w", GAUSS_CASES, ids=[c.name for c in GAUSS_CASES])

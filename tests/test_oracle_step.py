@@ -105,3 +105,40 @@ def test_lookahead_pins_attention_set():
                 assert set(rec.attn_sel.tolist()) <= dec.cache[u].resident()
             assert set(rec.sel.tolist()) <= dec.cache[u].resident()
         prev = {u: rec.sel for u, rec in recs.items()}
+
+
+def test_fp8_history_with_exact_values_matches_bf16():
+    """Integer-valued keys and values (|x| <= 16) and power-of-two scales are exact in E4M3, so the
+    FP8 decoder must reproduce the bf16 decoder exactly -- selections, cache state, outputs --
+    with half the fetched bytes; an appended token is quantised on arrival."""
+    from oracle import bf16_to_f32
+    from oracle.fp8 import quantize
+    w = SMALL.with_(int_scale=2.0, int_clip=4.0, append=True, steps=6)   # heavy keys up to 16: 2k <= 32, even
+    w8 = w.with_(kv_dtype="fp8", k_scale=0.5, v_scale=2.0)
+    k, v = W.kv_numpy(w)
+    a = OracleDecoder(w, k, v, [w.ctx0])
+    b = OracleDecoder(w8, quantize(bf16_to_f32(k), w8.k_scale), quantize(bf16_to_f32(v), w8.v_scale), [w.ctx0])
+    qa, qb = W.QueryStream(w), W.QueryStream(w8)
+    for t in range(6):
+        nk, nv = W.token(w, w.ctx0 + t)
+        oa, ra = a.step(qa.queries(t), new_k=nk, new_v=nv)
+        ob, rb = b.step(qb.queries(t), new_k=nk, new_v=nv)
+        np.testing.assert_array_equal(oa, ob)
+        for u in ra:
+            assert ra[u].sel.tolist() == rb[u].sel.tolist()
+            np.testing.assert_array_equal(a.ik[u], b.ik[u])
+        sa, sb = a.stats(), b.stats()
+        assert sa[0]["bytes_fetched"] == 2 * sb[0]["bytes_fetched"]
+        assert {k2: v2 for k2, v2 in sa[0].items() if k2 != "bytes_fetched"} == \
+               {k2: v2 for k2, v2 in sb[0].items() if k2 != "bytes_fetched"}
+
+
+def test_fp8_quantisation_error_is_bounded():
+    """With N(0,1) values the FP8 decoder's outputs stay within E4M3's relative step (2^-4 of each
+    value at most) of the bf16 decoder's: the dequantised rows differ by at most that much."""
+    from oracle import bf16_to_f32
+    from oracle.fp8 import dequantize_f32, quantize
+    k, _ = W.kv_numpy(SMALL)
+    x = bf16_to_f32(k)
+    err = np.abs(dequantize_f32(quantize(x, 1.0), 1.0) - x)
+    assert np.all(err <= np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10))

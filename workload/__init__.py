@@ -136,6 +136,9 @@ class Workload:
     int_clip: float = 7.0
     evict_policy: str = "lru"   # "lru" or "importance" (least important block first)
     score_mode: str = "mean"    # "mean" (block-mean key) or "bound" ([max | min] summary, upper-bound score)
+    kv_dtype: str = "bf16"      # "bf16" or "fp8" (E4M3 codes of value / scale in the history and the cache)
+    k_scale: float = 1.0
+    v_scale: float = 1.0
     notes: str = ""
 
     @property
@@ -165,9 +168,13 @@ class Workload:
         return float(np.float32(1.0 / math.sqrt(self.d_k)))
 
     @property
+    def elt_bytes(self) -> int:
+        return 1 if self.kv_dtype == "fp8" else 2
+
+    @property
     def host_kv_bytes(self) -> int:
         per_tok = self.d_k + (0 if self.v_shares_k else self.d_v)
-        return self.n_layer * self.n_req * self.n_kv_head * self.max_ctx * per_tok * 2
+        return self.n_layer * self.n_req * self.n_kv_head * self.max_ctx * per_tok * self.elt_bytes
 
     def kv_params(self, n_threads: int = 0) -> _KVParams:
         return _KVParams(self.seed, self.n_req, self.n_layer, self.n_kv_head, self.d_k,
