@@ -45,7 +45,7 @@ METRIC = "sparse decode steps/s (effective KV GB/s and HBM/host-link roofline al
 UNIT = "steps/s"
 
 # Workloads measured beside the headline by the default run (child processes).
-PER_CONFIG = ["llama8b_128k_append", "mla_128k_token_topk"]
+PER_CONFIG = ["llama8b_128k_append", "mla_128k_token_topk", "llama8b_32k_lookahead_fp8"]
 # Reduced budget/eviction sweep: block size x budget tokens x target step overlap (%).
 SWEEP_POINTS = [f"sweep_bs{bs}_b{b}_ov{ov}" for bs in (16, 64) for b in (512, 2048, 4096) for ov in (50, 80, 95)]
 
@@ -290,8 +290,8 @@ def algorithmic_bytes(w, lens, link_bytes_per_step):
         nb = (L + w.block_size - 1) // w.block_size
         k = min(w.budget_blocks, nb)
         rows_per_unit += [min(k * w.block_size, L)] * w.n_kv_head
-    row_b = 2 * (w.d_k + (0 if w.v_shares_k else w.d_v))
-    idx_b = sum(((L + w.block_size - 1) // w.block_size) * w.d_k * 2 for L in lens) * w.n_kv_head
+    row_b = w.elt_bytes * (w.d_k + (0 if w.v_shares_k else w.d_v))          # bf16 or E4M3 rows
+    idx_b = sum(((L + w.block_size - 1) // w.block_size) * w.d_idx * 2 for L in lens) * w.n_kv_head
     attn_b = sum(rows_per_unit) * row_b
     q_b = w.n_req * w.n_q_head * w.d_k * 2 * (1 + (w.n_draft if w.lookahead else 0))
     out_b = w.n_req * w.n_q_head * w.d_v * 4
@@ -480,7 +480,7 @@ def prefetch_report(w, dstat, steps: int):
     if not w.layer_prefetch or steps <= 0:
         return None
     prefetched, used = float(dstat[3]) / steps, float(dstat[4]) / steps
-    block_bytes = w.block_size * (w.d_k + (0 if w.v_shares_k else w.d_v)) * 2
+    block_bytes = w.block_size * (w.d_k + (0 if w.v_shares_k else w.d_v)) * w.elt_bytes
     return {"blocks_per_step": round(prefetched, 1), "used_per_step": round(used, 1),
             "used_fraction": round(used / prefetched, 4) if prefetched else None,
             "hidden_miss_bytes_per_step": int(used * block_bytes)}
@@ -526,7 +526,24 @@ class History:
         t0 = time.time()
         self.K = K
         self.vm0 = K.numa_vmstat()
-        if w.v_shares_k:
+        if w.kv_dtype == "fp8":
+            # generate bf16, quantise to E4M3 through the GPU into the history that is then bound
+            kb = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_k))
+            vb = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_v))
+            W.fill_kv(w, kb.tensor, vb.tensor, threads)
+            k8 = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_k), dtype=torch.uint8, local_node=numa_local)
+            v8 = K.HostArray((NL, B, Hkv, w.max_ctx, w.d_v), dtype=torch.uint8, local_node=numa_local)
+            K.quantize_history_e4m3(kb.tensor, k8.tensor, w.k_scale)
+            K.quantize_history_e4m3(vb.tensor, v8.tensor, w.v_scale)
+            kb.close()
+            vb.close()
+            del kb, vb
+            frac = min(k8.huge_fraction(), v8.huge_fraction())
+            k8.register()
+            v8.register()
+            self.k, self.v, self.k_keep, self.v_keep = k8.tensor, v8.tensor, k8, v8
+            self.desc = f"E4M3 codes (scales {w.k_scale:g} / {w.v_scale:g}); mmap + huge pages ({frac:.0%}) + cudaHostRegister"
+        elif w.v_shares_k:
             self.k, self.k_keep, self.desc = K.pinned_host_history((NL, B, Hkv, w.max_ctx, w.d_k),
                                                                    lambda t: W.fill_kv(w, t, None, threads),
                                                                    local_node=numa_local)
@@ -581,11 +598,11 @@ class History:
             ctx.bind_host_kv(self.k, self.v)
             self.desc += f" (huge pages split by the first step, {left:.0%} left, collapsed again)"
             return
-        k_new = torch.empty(self.k.shape, dtype=torch.int16, pin_memory=True)
+        k_new = torch.empty(self.k.shape, dtype=self.k.dtype, pin_memory=True)
         k_new.copy_(self.k)
         v_new = None
         if self.v is not None:
-            v_new = torch.empty(self.v.shape, dtype=torch.int16, pin_memory=True)
+            v_new = torch.empty(self.v.shape, dtype=self.v.dtype, pin_memory=True)
             v_new.copy_(self.v)
         ctx.bind_host_kv(k_new, v_new)
         for a in arrays:

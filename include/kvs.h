@@ -48,9 +48,11 @@
  * kvs_poll_error, kvs_destroy).  The return value reports argument and launch errors only.
  * Errors found on the device (capacity overflow, bad block id, a wait that ran out of time)
  * set a sticky status word that kvs_poll_error reads after the caller synchronises; no
- * kernel traps.  Calls on the same layer must not overlap on the GPU; nor may kvs_decode_step
- * and kvs_topk_select calls on different layers, which share the workspace's block-score and
- * top-K candidate scratch (issue them on one stream; kvs_layer_prefetch may run beside them).
+ * kernel traps.  Calls on the same layer must not overlap on the GPU.  The workspace holds two
+ * copies of the block-score and top-K candidate scratch, one per layer parity: kvs_decode_step
+ * calls on layers of the same parity must not overlap (kvs_decode_step orders its own selection
+ * chains so), and a kvs_topk_select call (which uses the even copy) must not overlap an even
+ * layer's step; kvs_layer_prefetch may run beside them.
  */
 #ifndef KVS_H_
 #define KVS_H_
@@ -217,10 +219,10 @@ kvs_status kvs_sparse_decode_attn(kvs_ctx* ctx, int layer, const void* d_q, cons
  *                   select -> update with that selection pinned -> fetch on copy_stream.
  * The first lookahead step of a layer has no previous selection and runs the sync part first.
  * Lookahead with a separate copy_stream overlaps the two halves [SPEC 1, OASIS module 2]: the
- * selection chain (score, select, update) runs on a stream the context owns, starting once the
- * work enqueued on `stream` before this call (the layer below's attention) has finished, beside
- * this layer's attention on `stream`; the fetch on copy_stream waits for both.  All layers'
- * selection chains run on that one stream, in call order.
+ * selection chain (score, select, update) runs on one of two streams the context owns (one per
+ * layer parity), starting once the work enqueued on `stream` before this call (the layer below's
+ * attention) has finished, beside this layer's attention on `stream` and the chain of the layer
+ * below; the fetch on copy_stream waits for the chain and the attention.
  * k_new / v_new NULL: no append (else as kvs_append, after kvs_advance_ctx).  d_score_q NULL
  * scores with d_q (nq = 1).  copy_stream NULL or == stream: the fetch runs on stream.  With a
  * separate copy_stream the caller calls kvs_join before reusing the layer or ending a capture.

@@ -3,8 +3,9 @@
 // Tensor-core tile (m16n8k16, bf16 in, fp32 accumulate): A = 16 index keys (blocks) x 16 dims,
 // B = 16 dims x 8 scoring rows.  The scoring rows of unit (request, kv-head h) are the q heads
 // of group h for every scoring query j (row = j * G + g).  Rows are kept in shared memory for the
-// whole CTA; index tiles stream through per-warp double buffers with cp.async.  The max over
-// rows is taken in registers and across the 4 lanes of a quad.
+// whole CTA; index tiles stream through a per-warp ring of cp.async stages (4 for rows of up to
+// 256 bytes, 2 for wider rows).  The max over rows is taken in registers and across the 4 lanes
+// of a quad.  The grid is one wave: the CTAs per unit are chosen from the resident CTAs per SM.
 #include <float.h>
 
 #include "kvs_common.cuh"
@@ -16,11 +17,15 @@ namespace {
 
 constexpr int kScoreMaxRows = 128;
 
+template <int DK>
+constexpr int score_stages() { return DK <= 128 ? 4 : 2; }
+
 struct ScoreSmem {
   int rows_pad;     // scoring rows rounded up to 16
   int row_stride;   // bytes per smem row (dk * 2 + 16 pad: conflict-free ldmatrix)
   int nwarps;
-  size_t bytes() const { return (size_t)rows_pad * row_stride + (size_t)nwarps * 2 * 16 * row_stride; }
+  int stages;
+  size_t bytes() const { return (size_t)rows_pad * row_stride + (size_t)nwarps * stages * 16 * row_stride; }
 };
 
 template <int DK, int NP>  // DK = index row width d_idx; NP = number of n8 tiles of scoring rows (rows_pad / 8)
@@ -62,7 +67,8 @@ __global__ void __launch_bounds__(128) score_kernel(Dims d, const __nv_bfloat16*
   }
   __syncthreads();
 
-  unsigned char* buf = smem + NP * 8 * RS + (size_t)warp * 2 * 16 * RS;
+  constexpr int ST = score_stages<DK>();
+  unsigned char* buf = smem + NP * 8 * RS + (size_t)warp * ST * 16 * RS;
   const __nv_bfloat16* ik = index + (size_t)u * d.nb_max * DK;
 
   auto load_tile = [&](int tile, int stage) {
@@ -76,17 +82,21 @@ __global__ void __launch_bounds__(128) score_kernel(Dims d, const __nv_bfloat16*
     cp_async_commit();
   };
 
-  int my = tile0 + warp;
-  if (my < tile1) load_tile(my, 0);
+  // ring of ST stages: tiles my, my + nwarps, ... ; ST - 1 loads stay in flight ahead of the one
+  // being computed (an empty group is committed past the end so the wait count stays fixed)
+  const int first = tile0 + warp;
+#pragma unroll
+  for (int i = 0; i < ST - 1; ++i) {
+    const int t = first + i * nwarps;
+    if (t < tile1) load_tile(t, i);
+    else cp_async_commit();
+  }
   int stage = 0;
-  for (; my < tile1; my += nwarps, stage ^= 1) {
-    int next = my + nwarps;
-    if (next < tile1) {
-      load_tile(next, stage ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+  for (int my = first; my < tile1; my += nwarps, stage = (stage + 1) % ST) {
+    const int ahead = my + (ST - 1) * nwarps;
+    if (ahead < tile1) load_tile(ahead, (stage + ST - 1) % ST);
+    else cp_async_commit();
+    cp_async_wait<ST - 1>();
     __syncwarp();
     const unsigned char* a_tile = buf + stage * 16 * RS;
     float acc[NP][4];
@@ -120,7 +130,7 @@ __global__ void __launch_bounds__(128) score_kernel(Dims d, const __nv_bfloat16*
         }
       }
     }
-    __syncwarp();
+    __syncwarp();   // the stage is refilled only after every lane has read it
     // max over valid scoring rows (columns)
     float m_lo = -FLT_MAX, m_hi = -FLT_MAX;
 #pragma unroll
@@ -145,17 +155,23 @@ __global__ void __launch_bounds__(128) score_kernel(Dims d, const __nv_bfloat16*
 template <int DK, int NP>
 cudaError_t launch_score_t(const Dims& d, const __nv_bfloat16* index, const __nv_bfloat16* q, int nq,
                            const int* ctx_len, float* scores, unsigned* err, cudaStream_t s) {
-  int nwarps = (DK * 2 + 16) * (NP * 8 + 4 * 32) <= 200 * 1024 ? 4 : 2;
-  ScoreSmem sm{NP * 8, DK * 2 + 16, nwarps};
+  constexpr int ST = score_stages<DK>();
+  int nwarps = (DK * 2 + 16) * (NP * 8 + 4 * ST * 16) <= 200 * 1024 ? 4 : 2;
+  ScoreSmem sm{NP * 8, DK * 2 + 16, nwarps, ST};
   size_t bytes = sm.bytes();
   auto kern = score_kernel<DK, NP>;
   {
     cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), (int)bytes);
     if (e != cudaSuccess) return e;
   }
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * nwarps, bytes) != cudaSuccess || per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
   int max_tiles = (d.nb_max + 15) / 16;
-  // about 2 waves of CTAs over 152 SMs, at least 4 tiles per warp
-  int ctas_per_unit = max(1, min((max_tiles + 4 * nwarps - 1) / (4 * nwarps), (2 * device_sm_count() + d.U - 1) / d.U));
+  // one wave of CTAs over the SMs, at least 4 tiles per warp
+  int ctas_per_unit = max(1, min((max_tiles + 4 * nwarps - 1) / (4 * nwarps), per_sm * device_sm_count() / d.U));
   int tiles_per_cta = (max_tiles + ctas_per_unit - 1) / ctas_per_unit;
   dim3 grid(ctas_per_unit, d.U);
   launch_pdl(kern, dim3(grid), dim3(32 * nwarps), bytes, s, d, index, q, nq, ctx_len, scores, tiles_per_cta, err);

@@ -34,10 +34,12 @@ struct kvs_ctx {
   std::vector<cudaEvent_t> sel_ready, pf_done;
   std::vector<int> sel_pending, pf_pending;
   std::vector<CUtensorMap> tmaps;   // per layer: K pool, V pool (TMA attention path)
-  kvs::TopkScratch tk{};            // two-phase top-K candidates (long contexts), shared by layers
-  // overlapped lookahead steps: the selection chain's stream, and per layer the events that order
-  // it (start after the layer below's attention; update done; attention done)
-  cudaStream_t sel_stream = nullptr;
+  // two-phase top-K candidates (long contexts), one copy per layer parity (like the block scores)
+  kvs::TopkScratch tk[2] = {};
+  // overlapped lookahead steps: two selection-chain streams (even and odd layers, so that a layer's
+  // chain need not wait for the chain of the layer below), and per layer the events that order
+  // them (start after the layer below's attention; update done; attention done)
+  cudaStream_t sel_stream[2] = {nullptr, nullptr};
   std::vector<cudaEvent_t> layer_start, upd_done, attn_done;
   // diagnostics
   unsigned long long launches = 0;
@@ -149,16 +151,16 @@ Plan plan_of(const Dims& d) {
   p.per_layer = p.kpool + p.vpool + p.b2s + p.s2b + p.stamp + p.clock + p.pend_sel + p.pend_slot + p.pend_n + p.sel +
                 p.nsel + p.sos + p.fblk + p.fslot + p.nfetch + p.next_sel + p.next_slot + p.next_n + p.next_commit;
   p.err = align_up(16);
-  p.scores = align_up(U * d.nb_max * 4);
+  p.scores = 2 * align_up(U * d.nb_max * 4);   // one copy per layer parity
   size_t parts = kAttnSplitMax;
   if (attention_tma_supported(d)) parts = std::max<size_t>(parts, (size_t)attention_tma_partials(d));
   p.part = align_up(U * parts * d.G * d.dv * 4);
   p.ml = align_up(U * parts * d.G * 2 * 4);
   p.done = align_up(U * 4);
   const size_t P = (size_t)topk_chunks(d);
-  p.tk_key = align_up(U * P * d.Kb * 4);
-  p.tk_idx = align_up(U * P * d.Kb * 4);
-  p.tk_cnt = align_up(U * P * 4);
+  p.tk_key = 2 * align_up(U * P * d.Kb * 4);   // one copy per layer parity
+  p.tk_idx = 2 * align_up(U * P * d.Kb * 4);
+  p.tk_cnt = 2 * align_up(U * P * 4);
   p.total = p.per_layer * d.NL + p.err + p.scores + p.part + p.ml + p.done + p.tk_key + p.tk_idx + p.tk_cnt;
   return p;
 }
@@ -320,9 +322,11 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   float* ml = reinterpret_cast<float*>(shared + p.err + p.scores + p.part);
   unsigned* done = reinterpret_cast<unsigned*>(shared + p.err + p.scores + p.part + p.ml);
   unsigned char* tk = shared + p.err + p.scores + p.part + p.ml + p.done;
-  c->tk.key = p.tk_key ? reinterpret_cast<uint32_t*>(tk) : nullptr;
-  c->tk.idx = p.tk_key ? reinterpret_cast<int*>(tk + p.tk_key) : nullptr;
-  c->tk.cnt = p.tk_key ? reinterpret_cast<int*>(tk + p.tk_key + p.tk_idx) : nullptr;
+  for (int par = 0; par < 2; ++par) {
+    c->tk[par].key = p.tk_key ? reinterpret_cast<uint32_t*>(tk + par * (p.tk_key / 2)) : nullptr;
+    c->tk[par].idx = p.tk_key ? reinterpret_cast<int*>(tk + p.tk_key + par * (p.tk_idx / 2)) : nullptr;
+    c->tk[par].cnt = p.tk_key ? reinterpret_cast<int*>(tk + p.tk_key + p.tk_idx + par * (p.tk_cnt / 2)) : nullptr;
+  }
   for (int l = 0; l < d.NL; ++l) {
     unsigned char* b = base + p.per_layer * l;
     Layer& L = c->layers[l];
@@ -346,7 +350,7 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
     L.next_slot = reinterpret_cast<int*>(b); b += p.next_slot;
     L.next_n = reinterpret_cast<int*>(b); b += p.next_n;
     L.next_commit = reinterpret_cast<int*>(b); b += p.next_commit;
-    L.scores = scores;
+    L.scores = scores + (size_t)(l & 1) * (p.scores / 2 / sizeof(float));   // this layer's parity copy
     L.attn_part = part;
     L.attn_ml = ml;
     L.unit_done = done;
@@ -407,12 +411,13 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
       }
   // the selection chain of overlapped lookahead steps is the step's critical path: highest priority
   int lo = 0, hi = 0;
-  if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess ||
-      cudaStreamCreateWithPriority(&c->sel_stream, cudaStreamNonBlocking, hi) != cudaSuccess) {
-    c->sel_stream = nullptr;
-    kvs_destroy(c);
-    return KVS_ERR_CUDA;
-  }
+  for (cudaStream_t& st : c->sel_stream)
+    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, hi) != cudaSuccess) {
+      st = nullptr;
+      kvs_destroy(c);
+      return KVS_ERR_CUDA;
+    }
   *out = c;
   return KVS_OK;
 }
@@ -461,7 +466,8 @@ kvs_status kvs_destroy(kvs_ctx* c) {
   for (auto* v : {&c->sel_ready, &c->pf_done, &c->fetch_done, &c->layer_start, &c->upd_done, &c->attn_done})
     for (cudaEvent_t e : *v)
       if (e) cudaEventDestroy(e);
-  if (c->sel_stream) cudaStreamDestroy(c->sel_stream);
+  for (cudaStream_t st : c->sel_stream)
+    if (st) cudaStreamDestroy(st);
   delete c;
   return KVS_OK;
 }
@@ -533,7 +539,7 @@ kvs_status kvs_score_blocks(kvs_ctx* c, int layer, const void* d_score_q, int nq
 kvs_status kvs_topk_select(kvs_ctx* c, const float* d_scores, const int* d_ctx_len, int* d_sel, int* d_nsel,
                            kvs_stream_t stream) {
   if (!c || !d_scores || !d_ctx_len || !d_sel || !d_nsel) return KVS_ERR_INVALID_ARG;
-  return cuda_status(timed(c, KVS_K_TOPK, S(stream), 1, [&] { return launch_topk(c->d, d_scores, d_ctx_len, d_sel, d_nsel, c->err, S(stream), c->tk.key ? &c->tk : nullptr); }));
+  return cuda_status(timed(c, KVS_K_TOPK, S(stream), 1, [&] { return launch_topk(c->d, d_scores, d_ctx_len, d_sel, d_nsel, c->err, S(stream), c->tk[0].key ? &c->tk[0] : nullptr); }));
 }
 
 kvs_status kvs_cache_update(kvs_ctx* c, int layer, const int* d_sel, const int* d_nsel, const int* d_ctx_len,
@@ -670,7 +676,8 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
     return timed(c, KVS_K_SCORE, ss, 1, [&] { return launch_score(d, idx, rows, n, d_ctx_len, L.scores, c->err, ss); });
   };
   auto topk = [&](int* so, int* no) {
-    cudaError_t r = timed(c, KVS_K_TOPK, ss, 1, [&] { return launch_topk(d, L.scores, d_ctx_len, so, no, c->err, ss, c->tk.key ? &c->tk : nullptr); });
+    const kvs::TopkScratch* tks = c->tk[layer & 1].key ? &c->tk[layer & 1] : nullptr;
+    cudaError_t r = timed(c, KVS_K_TOPK, ss, 1, [&] { return launch_topk(d, L.scores, d_ctx_len, so, no, c->err, ss, tks); });
     if (r == cudaSuccess) r = cudaEventRecord(c->sel_ready[layer], ss);   // hint for a prefetch into layer + 1
     if (r == cudaSuccess) c->sel_pending[layer] = 1;
     return r;
@@ -726,9 +733,9 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
   // which stages the new pending selection) starts on the selection stream as soon as the layer
   // below has finished its attention, and runs beside this layer's attention over S_t on `s`.  The
   // fetch waits for both: it writes only slots the update freed, and it commits the staged
-  // selection, which the attention must no longer be reading.  The selection chains of all layers
-  // share the block-score and top-K scratch, so they all run on the one selection stream.
-  ss = c->sel_stream;
+  // selection, which the attention must no longer be reading.  Layers of one parity share the
+  // block-score and top-K scratch, so their chains run on the same one of the two selection streams.
+  ss = c->sel_stream[layer & 1];
   if (e == cudaSuccess) e = cudaEventRecord(c->layer_start[layer], s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(ss, c->layer_start[layer], 0);
   if (e == cudaSuccess && !c->booted[layer]) {

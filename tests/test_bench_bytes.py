@@ -73,3 +73,16 @@ def test_prefetch_report():
     r = b.prefetch_report(w, dstat, 10)
     assert r["blocks_per_step"] == 500 and r["used_per_step"] == 250 and r["used_fraction"] == 0.5
     assert r["hidden_miss_bytes_per_step"] == 250 * 576 * 2                  # token blocks of the latent row
+
+
+def test_fp8_rows_and_bound_index_widths():
+    """E4M3 rows move one byte per element; [max | min] summaries make the index scan twice as wide."""
+    b = _bench()
+    w = W.LLAMA8B_32K
+    lens = [w.ctx0] * w.n_req
+    _, _, base = b.algorithmic_bytes(w, lens, 0)
+    _, _, f8 = b.algorithmic_bytes(w.with_(kv_dtype="fp8"), lens, 0)
+    _, _, bd = b.algorithmic_bytes(w.with_(score_mode="bound"), lens, 0)
+    rows = 8 * 8 * 128 * 16                        # units x selected tokens
+    assert base["attn"] - f8["attn"] == rows * 256  # 512 B of bf16 K + V per token vs 256 B of E4M3
+    assert bd["index"] == 2 * base["index"] and f8["index"] == base["index"]

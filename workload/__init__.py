@@ -276,8 +276,12 @@ TINY_MLA = Workload(name="tiny_mla", n_req=1, n_layer=1, n_q_head=16, n_kv_head=
 # the 128K shape without the per-step append (history fixed): isolates the append's effect
 LONG_128K_SYNC = LONG_128K.with_(name="llama8b_128k_sync", append=False)
 
+# the 8B lookahead workload with an E4M3 history and cache (unit scales: N(0,1) values sit well
+# inside E4M3's range)
+LLAMA8B_32K_FP8 = LLAMA8B_32K.with_(name="llama8b_32k_lookahead_fp8", kv_dtype="fp8")
+
 WORKLOADS = {w.name: w for w in (TINY, TINY_LOOKAHEAD, TINY_APPEND, TINY_PREFETCH, TINY_MLA, LLAMA8B_32K, LONG_128K, LONG_128K_SYNC,
-                                 MLA_128K)}
+                                 MLA_128K, LLAMA8B_32K_FP8)}
 
 
 def get(name: str) -> Workload:
