@@ -388,13 +388,23 @@ __global__ void __launch_bounds__((kConsumers + 1) * 32, kCtasPerSm)
             lpart += wgt * ml.y;
           }
           const int nj = min(32, np - q0);
-          for (int j = 0; j < nj; ++j) {
-            const float wj = __shfl_sync(0xffffffffu, wgt, j);
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(L.attn_part + ((base + q0 + j) * G + g) * D) + lane);
-            acc.x += wj * x.x;
-            acc.y += wj * x.y;
-            acc.z += wj * x.z;
-            acc.w += wj * x.w;
+          // eight partials' loads in flight at a time (they are independent; only the sums chain)
+          for (int j0 = 0; j0 < nj; j0 += 8) {
+            float4 x[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              x[k] = j0 + k < nj ? __ldcg(reinterpret_cast<const float4*>(L.attn_part + ((base + q0 + j0 + k) * G + g) * D) + lane)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float wj = __shfl_sync(0xffffffffu, wgt, (j0 + k) & 31);
+              if (j0 + k < nj) {
+                acc.x += wj * x[k].x;
+                acc.y += wj * x[k].y;
+                acc.z += wj * x[k].z;
+                acc.w += wj * x[k].w;
+              }
+            }
           }
         }
 #pragma unroll

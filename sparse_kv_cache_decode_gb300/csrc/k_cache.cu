@@ -25,13 +25,15 @@ struct CacheSmem {
   int* list_blk;      // [Kb] misses (update) or non-resident hint blocks (prefetch), ascending
   int* list_pos;      // [Kb] position of each miss in the selection
   int* sos;           // [Kb] slot of each selected block
+  int* s2b;           // [C]  the unit's slot -> block map, read once (update)
+  unsigned* st;       // [C]  the unit's stamps, read once (update)
 };
 
 __host__ __device__ inline int max_victims(const Dims& d) { return d.Kb > d.max_prefetch ? d.Kb : d.max_prefetch; }
 
 __host__ __device__ inline size_t cache_smem_bytes(const Dims& d) {
   size_t mv = (size_t)max_victims(d);
-  return ((size_t)d.C + 15) / 16 * 16 + mv * 12 + (size_t)d.Kb * 12;
+  return ((size_t)d.C + 15) / 16 * 16 + mv * 12 + (size_t)d.Kb * 12 + (size_t)d.C * 8;
 }
 
 __device__ CacheSmem carve(unsigned char* base, const Dims& d) {
@@ -44,7 +46,9 @@ __device__ CacheSmem carve(unsigned char* base, const Dims& d) {
   s.vict = reinterpret_cast<int*>(base); base += mv * 4;
   s.list_blk = reinterpret_cast<int*>(base); base += (size_t)d.Kb * 4;
   s.list_pos = reinterpret_cast<int*>(base); base += (size_t)d.Kb * 4;
-  s.sos = reinterpret_cast<int*>(base);
+  s.sos = reinterpret_cast<int*>(base); base += (size_t)d.Kb * 4;
+  s.s2b = reinterpret_cast<int*>(base); base += (size_t)d.C * 4;
+  s.st = reinterpret_cast<unsigned*>(base);
   return s;
 }
 
@@ -147,7 +151,12 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
     s_bad = 0;
   }
   if (tid < 4) s_cnt[tid] = 0;
-  for (int s = tid; s < d.C; s += NT) sm.flags[s] = 0;
+  // the unit's slot map and stamps, read from global memory once (every later step uses these)
+  for (int s = tid; s < d.C; s += NT) {
+    sm.flags[s] = 0;
+    sm.s2b[s] = s2b[s];
+    sm.st[s] = st[s];
+  }
   __syncthreads();
   const unsigned now = s_now;
 
@@ -165,7 +174,7 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
     if (s >= 0) {
       sm.flags[s] = 1;
       sm.sos[i] = s;
-      my_pfh += st[s] == now - 1u;
+      my_pfh += sm.st[s] == now - 1u;
     } else {
       ++my_miss;
     }
@@ -223,16 +232,16 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
   select_victims(
       d.C, m, [&](int s) { return (sm.flags[s] & emask) == 0; },
       [&](int s) {
-        const int b = s2b[s];
+        const int b = sm.s2b[s];
         if (b < 0) return 0u;
-        return imp_u ? score_key(imp_u[b]) + 1u : st[s];
+        return imp_u ? score_key(imp_u[b]) + 1u : sm.st[s];
       },
       hist, ws, pick, sm);
 
   unsigned long long my_ev = 0, my_bytes = 0;
   for (int j = tid; j < m; j += NT) {
     int b = sm.list_blk[j], s = sm.vict[j];
-    int old = s2b[s];
+    int old = sm.s2b[s];
     if (old >= 0 && old < d.nb_max) { b2s[old] = -1; ++my_ev; }
     s2b[s] = b;
     b2s[b] = s;
