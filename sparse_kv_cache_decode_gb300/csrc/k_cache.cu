@@ -430,38 +430,29 @@ __global__ void __launch_bounds__(kRestoreThreads) restore_kernel(Dims d, Layer 
   }
 }
 
-// Zero-copy fetch with a small persistent grid, so that it leaves the SMs to the compute
-// kernels that run beside it: the CTAs flatten the (unit, item) lists with a prefix sum over
-// units; each warp copies batches of whole items (about 512 16-byte vectors per batch), 16 loads
-// in flight per lane, from the mapped host history into the items' slots.  Only rows < L are
-// copied.
-constexpr int kFetchCTAs = 64;
-constexpr int kFetchThreads = 128;   // 10K registers per CTA: fits beside two attention CTAs
+// Zero-copy fetch with one small CTA per SM, so that it fits beside the compute kernels that run
+// with it, and a layer's misses are all in flight at once (the host link needs a few MB in flight
+// to reach its peak): the CTAs flatten the (unit, item) lists with a prefix sum over units; each
+// warp copies batches of whole items (about 512 16-byte vectors per batch), 16 loads in flight
+// per lane, from the mapped host history into the items' slots.  Only rows < L are copied.
+constexpr int kFetchThreads = 128;   // about 12K registers per CTA (one item per batch): fits beside two attention CTAs
 constexpr int kFetchMaxUnits = 1024;
 constexpr int kFetchUnroll = 16;
 
-__global__ void __launch_bounds__(kFetchThreads) fetch_kernel(Dims d, Layer L, const int* __restrict__ ctx_len) {
+// Items per warp batch: whole items of about 512 16-byte vectors.
+__host__ __device__ inline int fetch_items_per_batch(const Dims& d) {
+  const int vpi = d.bs * d.dk * d.ebytes / 16 + (d.v_shares_k ? 0 : d.bs * d.dv * d.ebytes / 16);
+  return vpi >= 512 ? 1 : 512 / vpi;
+}
+
+// SINGLE: one item per warp batch (items of 512 vectors or more); every lane locates the item
+// itself, so no per-vector item state is held (a small register footprint).
+template <bool SINGLE>
+__global__ void __launch_bounds__(kFetchThreads, SINGLE ? 5 : 1) fetch_kernel(Dims d, Layer L, const int* __restrict__ ctx_len) {
   kvs_pdl_entry();
   __shared__ int s_off[kFetchMaxUnits + 1];
   __shared__ int ws[33];
   const int tid = threadIdx.x, lane = tid & 31;
-  // lookahead: commit the selections the update staged (this kernel runs after the layer's
-  // attention over the previous pending selection); unit u is handled by CTA u % grid
-  if (d.lookahead) {
-    for (int u = blockIdx.x; u < d.U; u += gridDim.x) {
-      if (!L.next_commit[u]) continue;
-      const int n = L.next_n[u];
-      for (int i = tid; i < n; i += blockDim.x) {
-        L.pend_sel[(size_t)u * d.Kb + i] = L.next_sel[(size_t)u * d.Kb + i];
-        L.pend_slot[(size_t)u * d.Kb + i] = L.next_slot[(size_t)u * d.Kb + i];
-      }
-      __syncthreads();
-      if (tid == 0) {
-        L.pend_n[u] = n;
-        L.next_commit[u] = 0;
-      }
-    }
-  }
   // prefix sum of the per-unit item counts
   const int per = (d.U + blockDim.x - 1) / blockDim.x;
   const int u0 = min(d.U, tid * per), u1 = min(d.U, u0 + per);
@@ -477,11 +468,44 @@ __global__ void __launch_bounds__(kFetchThreads) fetch_kernel(Dims d, Layer L, c
   const int vk = d.bs * kvec;                             // of K in a full block
   const int vv = d.v_shares_k ? 0 : d.bs * vvec;
   const int vpi = vk + vv;
-  const int ipb = max(1, 512 / vpi);                      // items per warp batch
+  const int ipb = fetch_items_per_batch(d);
   const int n_batches = (total + ipb - 1) / ipb;
   const int gwarp = blockIdx.x * (blockDim.x >> 5) + (tid >> 5);
   const int nwarps = gridDim.x * (blockDim.x >> 5);
-  for (int batch = gwarp; batch < n_batches; batch += nwarps) {
+  if (SINGLE) {
+    for (int item = gwarp; item < total; item += nwarps) {
+      int lo = 0, hi = d.U;                               // s_off[lo] <= item < s_off[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_off[mid] <= item) lo = mid; else hi = mid;
+      }
+      const int j = item - s_off[lo];
+      const int b = L.fetch_blk[(size_t)lo * d.C + j], sl = L.fetch_slot[(size_t)lo * d.C + j];
+      const int rows = max(0, min(d.bs, ctx_len[lo / d.Hkv] - b * d.bs));
+      const size_t src_row = (size_t)lo * d.max_ctx + (size_t)b * d.bs, dst_row = ((size_t)lo * d.C + sl) * d.bs;
+      const uint4* ks = reinterpret_cast<const uint4*>(L.host_k) + src_row * kvec;
+      const uint4* vs = reinterpret_cast<const uint4*>(L.host_v) + src_row * vvec;
+      uint4* kd = reinterpret_cast<uint4*>(L.kpool) + dst_row * kvec;
+      uint4* vd = reinterpret_cast<uint4*>(L.vpool) + dst_row * vvec;
+      const int nk = rows * kvec, nvv = d.v_shares_k ? 0 : rows * vvec;
+      for (int base = 0; base < vpi; base += 32 * kFetchUnroll) {
+        uint4 val[kFetchUnroll];
+#pragma unroll
+        for (int k = 0; k < kFetchUnroll; ++k) {
+          const int w = base + k * 32 + lane;
+          if (w < vk ? w < nk : w - vk < nvv) val[k] = w < vk ? ks[w] : vs[w - vk];
+        }
+#pragma unroll
+        for (int k = 0; k < kFetchUnroll; ++k) {
+          const int w = base + k * 32 + lane;
+          if (w < vk ? w < nk : w - vk < nvv) {
+            if (w < vk) kd[w] = val[k]; else vd[w - vk] = val[k];
+          }
+        }
+      }
+    }
+  }
+  for (int batch = gwarp; !SINGLE && batch < n_batches; batch += nwarps) {
     const int i0 = batch * ipb, ni = min(ipb, total - i0);
     // lane k < ni locates item i0 + k: unit by binary search over s_off, then its block and slot
     int my_u = 0, my_rows = 0;
@@ -536,6 +560,25 @@ __global__ void __launch_bounds__(kFetchThreads) fetch_kernel(Dims d, Layer L, c
         if (dst[k]) *dst[k] = val[k];
     }
   }
+  // lookahead: commit the selections the update staged (this kernel runs after the layer's
+  // attention over the previous pending selection; done after the copies, which do not depend on
+  // it, so that the host reads start at once); unit u is handled by CTA u % grid
+  if (d.lookahead) {
+    for (int u = blockIdx.x; u < d.U; u += gridDim.x) {
+      const int commit = L.next_commit[u];
+      __syncthreads();   // every thread has read the flag before thread 0 clears it
+      if (!commit) continue;
+      const int n = L.next_n[u];
+      for (int i = tid; i < n; i += blockDim.x) {
+        L.pend_sel[(size_t)u * d.Kb + i] = L.next_sel[(size_t)u * d.Kb + i];
+        L.pend_slot[(size_t)u * d.Kb + i] = L.next_slot[(size_t)u * d.Kb + i];
+      }
+      if (tid == 0) {
+        L.pend_n[u] = n;
+        L.next_commit[u] = 0;
+      }
+    }
+  }
 }
 
 }  // namespace
@@ -585,7 +628,10 @@ cudaError_t launch_restore(const Dims& d, const Layer& L, const unsigned char* s
 
 cudaError_t launch_fetch(const Dims& d, const Layer& L, const int* ctx_len, cudaStream_t s) {
   if (d.U > kFetchMaxUnits) return cudaErrorInvalidValue;
-  launch_pdl(fetch_kernel, dim3(kFetchCTAs), dim3(kFetchThreads), 0, s, d, L, ctx_len);
+  if (fetch_items_per_batch(d) == 1)
+    launch_pdl(fetch_kernel<true>, dim3(device_sm_count()), dim3(kFetchThreads), 0, s, d, L, ctx_len);
+  else
+    launch_pdl(fetch_kernel<false>, dim3(device_sm_count()), dim3(kFetchThreads), 0, s, d, L, ctx_len);
   return cudaGetLastError();
 }
 

@@ -275,10 +275,12 @@ bool make_tmap_2d(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows, uin
 
 namespace {
 
-// The slot pools as [U*C*bs][d] with 16-row boxes of 128 bytes: 64 bf16 or 128 E4M3 columns (the
-// TMA attention kernel's tiles).
+// The slot pools for the TMA attention kernel's tiles: E4M3 pools as [U*C*bs][128] with 16-row
+// boxes (a row is 128 bytes); bf16 pools as lines of 128 bytes, [U*C*bs*d/64][64], with 32-line
+// boxes, so that one tensor load brings all 16 rows of a tile.
 bool make_pool_map(CUtensorMap* m, void* base, size_t rows, int d, int elem_bytes) {
-  return kvs::make_tmap_2d(m, base, (uint64_t)d, (uint64_t)rows, 128 / elem_bytes, 16, elem_bytes);
+  if (elem_bytes == 1) return kvs::make_tmap_2d(m, base, (uint64_t)d, (uint64_t)rows, 128, 16, 1);
+  return kvs::make_tmap_2d(m, base, 64, (uint64_t)rows * (d / 64), 64, 16 * (d / 64), 2);
 }
 
 }  // namespace
