@@ -832,6 +832,9 @@ def run_point(args, dist, w, hist, link, e2e: bool, cpu_baseline: bool):
 
     rooflines = {k: kernel_roofline(k) for k in ("attn", "score", "fetch")}
     step_ms = {k: ms / max(1, n) * per_step_launches[k] for k, (ms, n) in kernel_times.items()}
+    if kernel_times["topk"][1] == 0 and kernel_times["update"][1] > 0:   # fused top-K + update kernel
+        step_ms["topk+update"] = step_ms.pop("update")
+        step_ms.pop("topk")
     dominant = args.timed_kernel if args.timed_kernel != "auto" else max(rooflines, key=lambda k: step_ms[k])
     roofline = dict(rooflines[dominant])
     roofline["dominant_by"] = "most CUDA-event time per step among attn, score, fetch (kernels one at a time)"

@@ -272,7 +272,10 @@ kvs_status kvs_poll_error(kvs_ctx* ctx, kvs_status* device_status);
  * `capacity` launches of that kernel (by any call, eager or captured in a CUDA graph) are each
  * bracketed by a pair of CUDA events recorded on the launch stream; several kernels can be armed
  * at once.  kvs_kernel_timer_read (synchronous) returns that kernel's summed elapsed milliseconds
- * and number of timed launches.  kernel: one of kvs_kernel_id; capacity 0 disarms it. */
+ * and number of timed launches.  kernel: one of kvs_kernel_id; capacity 0 disarms it.  Inside
+ * kvs_decode_step, when a unit's block scores fit one CTA's shared memory (at most 16384 blocks),
+ * top-K and the cache update run as one kernel, timed as KVS_K_UPDATE (KVS_K_TOPK then counts
+ * only kvs_topk_select calls and the two-kernel path). */
 typedef enum {
   KVS_K_SCORE = 1, KVS_K_TOPK = 2, KVS_K_UPDATE = 3, KVS_K_FETCH = 4, KVS_K_ATTN = 5,
   KVS_K_PREFETCH = 6, KVS_K_APPEND = 7, KVS_K_INDEX = 8

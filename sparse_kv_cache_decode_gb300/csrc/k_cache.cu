@@ -8,6 +8,7 @@
 #include "kvs_block.cuh"
 #include "kvs_common.cuh"
 #include "kvs_ptx.cuh"
+#include "kvs_select.cuh"
 
 #include <algorithm>
 
@@ -115,24 +116,66 @@ __device__ __forceinline__ unsigned long long fetch_rows(const Dims& d, int len,
   return (unsigned long long)min(d.bs, len - b * d.bs);
 }
 
-__global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Layer L, const int* __restrict__ sel,
-                                                                     const int* __restrict__ nsel,
-                                                                     const int* __restrict__ ctx_len,
-                                                                     int* __restrict__ slot_of_sel,
-                                                                     const float* __restrict__ imp, kvs_stats* stats) {
-  kvs_pdl_entry();
-  extern __shared__ __align__(16) unsigned char smraw[];
-  __shared__ int hist[256];
-  __shared__ int ws[33];
-  __shared__ int pick[2];
-  __shared__ unsigned s_now;
-  __shared__ int s_bad;
-  __shared__ unsigned long long s_cnt[4];  // hits, prefetch hits, evictions, bytes
+struct UpdateShared {
+  int hist[256];
+  int ws[33];
+  int pick[2];
+  int bad;
+  unsigned long long cnt[4];  // hits, prefetch hits, evictions, bytes
+};
+
+// The update stages the unit's block -> slot map in shared memory when it is this small.
+__host__ __device__ inline bool update_stages_b2s(const Dims& d) { return d.nb_max <= 16384; }
+// Caches of up to this many slots take their victims by counting ranks in one pass.
+constexpr int kRankVictimsMaxC = 1024;
+
+// Shared memory of the update: the CacheSmem arrays, then the staged selection and pending
+// slots [Kb] each, the victims' (key, slot) words [C], and the staged block -> slot map.
+__host__ __device__ inline size_t update_extra_offset(const Dims& d) { return (cache_smem_bytes(d) + 15) / 16 * 16; }
+__host__ __device__ inline size_t update_smem_bytes(const Dims& d) {
+  return update_extra_offset(d) + (size_t)d.Kb * 8 + (size_t)d.C * 8 + (update_stages_b2s(d) ? (size_t)d.nb_max * 4 : 0);
+}
+
+// The cache update of unit u (every thread of the CTA calls it).  Every input that does not depend
+// on another is read in one round of loads (the selection, the slot map and stamps, the pending
+// slots, the block -> slot map when it is staged); sel and nsel may have been written earlier in
+// the same kernel by this CTA (the fused top-K + update), so they are read through plain loads.
+__device__ void update_unit(const Dims& d, const Layer& L, int u, const int* sel, const int* nsel,
+                            const int* __restrict__ ctx_len, int* __restrict__ slot_of_sel,
+                            const float* __restrict__ imp, kvs_stats* stats, unsigned char* smraw, UpdateShared& sh) {
+  int* hist = sh.hist;
+  int* ws = sh.ws;
+  int* pick = sh.pick;
+  int& s_bad = sh.bad;
+  unsigned long long* s_cnt = sh.cnt;
   CacheSmem sm = carve(smraw, d);
-  const int u = blockIdx.x, r = u / d.Hkv;
+  int* su_s = reinterpret_cast<int*>(smraw + update_extra_offset(d));   // [Kb] the selection
+  int* ps_s = su_s + d.Kb;                                             // [Kb] the pending slots
+  unsigned long long* ck = reinterpret_cast<unsigned long long*>(ps_s + d.Kb);   // [C] victim (key, slot)
+  int* b2s_s = update_stages_b2s(d) ? reinterpret_cast<int*>(ck + d.C) : nullptr;   // [nb_max]
+  const int r = u / d.Hkv;
   const int tid = threadIdx.x, NT = blockDim.x;
+  int* b2s = L.block2slot + (size_t)u * d.nb_max;
+  int* s2b = L.slot2block + (size_t)u * d.C;
+  unsigned* st = L.stamp + (size_t)u * d.C;
   const int len = ctx_len[r];
   const int n = nsel[u];
+  const int pn = d.lookahead ? L.pend_n[u] : -1;
+  const unsigned now = 2u * (L.clock[u] + 1u);   // written back only once the update is accepted
+  if (tid == 0) s_bad = 0;
+  if (tid < 4) s_cnt[tid] = 0;
+  for (int s = tid; s < d.C; s += NT) {
+    sm.flags[s] = 0;
+    sm.s2b[s] = s2b[s];
+    sm.st[s] = st[s];
+  }
+  for (int i = tid; i < d.Kb; i += NT) {
+    su_s[i] = sel[(size_t)u * d.Kb + i];
+    ps_s[i] = d.lookahead ? L.pend_slot[(size_t)u * d.Kb + i] : -1;
+  }
+  if (b2s_s)
+    for (int b = tid; b < d.nb_max; b += NT) b2s_s[b] = b2s[b];
+  __syncthreads();
   const int nb = n_blocks_of(len, d.bs);
   if (len < 0 || len > d.max_ctx || n < 0 || n > d.Kb) {
     if (tid == 0) {
@@ -142,23 +185,7 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
     }
     return;
   }
-  const int* su = sel + (size_t)u * d.Kb;
-  int* b2s = L.block2slot + (size_t)u * d.nb_max;
-  int* s2b = L.slot2block + (size_t)u * d.C;
-  unsigned* st = L.stamp + (size_t)u * d.C;
-  if (tid == 0) {
-    s_now = 2u * (L.clock[u] + 1u);   // written back only once the update is accepted
-    s_bad = 0;
-  }
-  if (tid < 4) s_cnt[tid] = 0;
-  // the unit's slot map and stamps, read from global memory once (every later step uses these)
-  for (int s = tid; s < d.C; s += NT) {
-    sm.flags[s] = 0;
-    sm.s2b[s] = s2b[s];
-    sm.st[s] = st[s];
-  }
-  __syncthreads();
-  const unsigned now = s_now;
+  auto slot_of = [&](int b) { return b2s_s ? b2s_s[b] : b2s[b]; };
 
   // hits and misses, misses compacted in selection (ascending block) order
   const int per = (n + NT - 1) / NT;
@@ -166,10 +193,10 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
   int my_miss = 0;
   unsigned long long my_pfh = 0;
   for (int i = i0; i < i1; ++i) {
-    int b = su[i];
+    int b = su_s[i];
     // a selection is strictly ascending (top-K output order); anything else is refused
-    if (b < 0 || b >= nb || (i > 0 && su[i - 1] >= b)) { s_bad = 1; continue; }
-    int s = b2s[b];
+    if (b < 0 || b >= nb || (i > 0 && su_s[i - 1] >= b)) { s_bad = 1; continue; }
+    int s = slot_of(b);
     if (s >= d.C) { s_bad = 1; continue; }
     if (s >= 0) {
       sm.flags[s] = 1;
@@ -191,28 +218,29 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
   int m;
   int mpos = block_excl_sum(my_miss, ws, &m);
   for (int i = i0; i < i1; ++i) {
-    int b = su[i];
-    if (b2s[b] < 0) { sm.list_blk[mpos] = b; sm.list_pos[mpos] = i; ++mpos; }
+    int b = su_s[i];
+    if (slot_of(b) < 0) { sm.list_blk[mpos] = b; sm.list_pos[mpos] = i; ++mpos; }
   }
-  const bool pinned = d.lookahead && L.pend_n[u] >= 0;
+  const bool pinned = d.lookahead && pn >= 0;
   if (pinned) {
-    const int np = L.pend_n[u];
-    for (int i = tid; i < np && i < d.Kb; i += NT) {
-      int s = L.pend_slot[(size_t)u * d.Kb + i];
+    for (int i = tid; i < pn && i < d.Kb; i += NT) {
+      int s = ps_s[i];
       if (s >= 0 && s < d.C) sm.flags[s] |= 2;
     }
   }
   if (my_pfh) atomicAdd(&s_cnt[1], my_pfh);
   __syncthreads();
 
-  int my_el = 0, my_el_nopin = 0;
+  // eligible slots with and without the pins, in one prefix sum (both counts are below 2^16)
+  int my_el = 0, my_el_nopin = 0;   // C <= 8192
   for (int s = tid; s < d.C; s += NT) {
     my_el += sm.flags[s] == 0;
     my_el_nopin += (sm.flags[s] & 1) == 0;
   }
-  int n_el, n_el_nopin;
-  block_excl_sum(my_el, ws, &n_el);
-  block_excl_sum(my_el_nopin, ws, &n_el_nopin);
+  int both;
+  block_excl_sum(my_el | (my_el_nopin << 16), ws, &both);
+  int n_el = both & 0xffff;
+  const int n_el_nopin = both >> 16;
   bool fallback = false;
   if (n_el < m && pinned) { fallback = true; n_el = n_el_nopin; }
   if (n_el < m) {
@@ -229,14 +257,28 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
   // victim keys, smallest first: empty slots 0; LRU: the stamp (>= 2); importance: 1 + the
   // orderable key of the held block's score (NaN lowest), so the least important go first
   const float* imp_u = imp ? imp + (size_t)u * d.nb_max : nullptr;
-  select_victims(
-      d.C, m, [&](int s) { return (sm.flags[s] & emask) == 0; },
-      [&](int s) {
-        const int b = sm.s2b[s];
-        if (b < 0) return 0u;
-        return imp_u ? score_key(imp_u[b]) + 1u : sm.st[s];
-      },
-      hist, ws, pick, sm);
+  auto elig = [&](int s) { return (sm.flags[s] & emask) == 0; };
+  auto vkey = [&](int s) {
+    const int b = sm.s2b[s];
+    if (b < 0) return 0u;
+    return imp_u ? score_key(imp_u[b]) + 1u : sm.st[s];
+  };
+  if (d.C <= kRankVictimsMaxC) {
+    // the m smallest (key, slot) among the eligible slots by rank counting: one word per slot,
+    // all-ones for ineligible ones (never below an eligible word)
+    for (int s = tid; s < d.C; s += NT) ck[s] = elig(s) ? ((unsigned long long)vkey(s) << 32) | (unsigned)s : ~0ull;
+    __syncthreads();
+    for (int s = tid; s < d.C; s += NT) {
+      const unsigned long long mine = ck[s];
+      if (mine == ~0ull) continue;
+      int rank = 0;
+      for (int t = 0; t < d.C; ++t) rank += ck[t] < mine;
+      if (rank < m) sm.vict[rank] = s;
+    }
+    __syncthreads();
+  } else {
+    select_victims(d.C, m, elig, vkey, hist, ws, pick, sm);
+  }
 
   unsigned long long my_ev = 0, my_bytes = 0;
   for (int j = tid; j < m; j += NT) {
@@ -258,7 +300,7 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
     st[s] = now;
     slot_of_sel[(size_t)u * d.Kb + i] = s;
     if (d.lookahead) {   // staged; the fetch that follows commits it to pend_*
-      L.next_sel[(size_t)u * d.Kb + i] = su[i];
+      L.next_sel[(size_t)u * d.Kb + i] = su_s[i];
       L.next_slot[(size_t)u * d.Kb + i] = s;
     }
   }
@@ -278,6 +320,34 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Lay
       if (fallback) atomicAdd(&sl->pin_fallbacks, 1ull);
     }
   }
+}
+
+__global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(Dims d, Layer L, const int* __restrict__ sel,
+                                                                     const int* __restrict__ nsel,
+                                                                     const int* __restrict__ ctx_len,
+                                                                     int* __restrict__ slot_of_sel,
+                                                                     const float* __restrict__ imp, kvs_stats* stats) {
+  kvs_pdl_entry();
+  extern __shared__ __align__(16) unsigned char smraw[];
+  __shared__ UpdateShared sh;
+  update_unit(d, L, blockIdx.x, sel, nsel, ctx_len, slot_of_sel, imp, stats, smraw, sh);
+}
+
+// Top-K selection and cache update of one unit in one CTA (contexts of at most kTopkSmemKeys
+// blocks): the selection goes to sel / nsel as from the top-K kernel, and the update reads it
+// back after a barrier, with no kernel boundary between the two.
+__global__ void __launch_bounds__(kCacheThreads) select_update_kernel(Dims d, Layer L, const float* __restrict__ scores,
+                                                                      const int* __restrict__ ctx_len, int* sel,
+                                                                      int* nsel, int* __restrict__ slot_of_sel,
+                                                                      kvs_stats* stats) {
+  kvs_pdl_entry();
+  extern __shared__ __align__(16) unsigned char smraw[];
+  __shared__ TopkShared tsh;
+  __shared__ UpdateShared ush;
+  const int u = blockIdx.x;
+  topk_unit_smem(d, scores, ctx_len[u / d.Hkv], u, sel, nsel, L.err, reinterpret_cast<uint32_t*>(smraw), tsh);
+  __syncthreads();   // the selection (global) and the key buffer (shared, reused below) are done
+  update_unit(d, L, u, sel, nsel, ctx_len, slot_of_sel, d.evict_importance ? scores : nullptr, stats, smraw, ush);
 }
 
 __global__ void __launch_bounds__(kCacheThreads) prefetch_kernel(Dims d, Layer L, const int* __restrict__ hint,
@@ -585,13 +655,27 @@ __global__ void __launch_bounds__(kFetchThreads, SINGLE ? 5 : 1) fetch_kernel(Di
 
 cudaError_t launch_cache_update(const Dims& d, const Layer& L, const int* sel, const int* nsel, const int* ctx_len,
                                 int* slot_of_sel, const float* scores, kvs_stats* stats, cudaStream_t s) {
-  size_t smem = cache_smem_bytes(d);
+  size_t smem = update_smem_bytes(d);
   if (smem > 48 * 1024) {
     cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(cache_update_kernel), (int)smem);
     if (e != cudaSuccess) return e;
   }
   launch_pdl(cache_update_kernel, dim3(d.U), dim3(kCacheThreads), smem, s, d, L, sel, nsel, ctx_len, slot_of_sel, scores,
              stats);
+  return cudaGetLastError();
+}
+
+int select_update_fusable(const Dims& d) { return d.nb_max <= kTopkSmemKeys; }
+
+cudaError_t launch_select_update(const Dims& d, const Layer& L, const float* scores, const int* ctx_len, int* sel,
+                                 int* nsel, int* slot_of_sel, kvs_stats* stats, cudaStream_t s) {
+  const size_t smem = std::max(update_smem_bytes(d), (size_t)d.nb_max * sizeof(uint32_t));
+  if (smem > 48 * 1024) {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(select_update_kernel), (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  launch_pdl(select_update_kernel, dim3(d.U), dim3(kCacheThreads), smem, s, d, L, scores, ctx_len, sel, nsel,
+             slot_of_sel, stats);
   return cudaGetLastError();
 }
 

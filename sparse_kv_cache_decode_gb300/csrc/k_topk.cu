@@ -16,108 +16,25 @@
 // than k), so the two phases select exactly the single-pass result.
 #include "kvs_block.cuh"
 #include "kvs_common.cuh"
+#include "kvs_select.cuh"
 
 namespace kvs {
 
 namespace {
 
 constexpr int kTopkThreads = 512;
-constexpr int kTopkSmemKeys = 16384;  // scores cached in shared memory up to this many blocks
 constexpr int kTopkMaxChunks = 64;
 constexpr size_t kTopkMergeSmemMax = 160 * 1024;  // kept candidates (key + block) of one unit
-
-// Histogram of one 8-bit digit over the keys in shared memory that match `prefix` under
-// `mask`.  Each thread adds runs of equal digits once (the keys of one unit share their high
-// bytes, so most of a thread's keys land in the same bin on the first passes).
-__device__ __forceinline__ void digit_histogram(const uint32_t* keys, int n, uint32_t prefix, uint32_t mask,
-                                                int shift, int* hist) {
-  int cur = -1, cnt = 0;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const uint32_t key = keys[i];
-    if ((key & mask) != prefix) continue;
-    const int bin = (int)((key >> shift) & 255u);
-    if (bin == cur) {
-      ++cnt;
-    } else {
-      if (cnt) atomicAdd(&hist[cur], cnt);
-      cur = bin;
-      cnt = 1;
-    }
-  }
-  if (cnt) atomicAdd(&hist[cur], cnt);
-}
-
-// Top k of keys[0, n) in shared memory by (key desc, position asc); emit(rank, i) is called for
-// each selected position i, ranks 0..k-1 in ascending position order.  Every thread of the CTA
-// (at most 512) must call it.  Requires 0 < k < n.
-//
-// The threshold key T and the number of keys equal to T still needed come from four 8-bit radix
-// passes.  The compaction gives each warp a contiguous segment of positions and walks it 32
-// keys at a time (lane i reads position base + i: no bank conflicts); ballots give each lane
-// its rank among the equal keys and among the taken keys.
-template <class Emit>
-__device__ void select_ordered(const uint32_t* keys, int n, int k, int* hist, int* ws, int* pick, Emit emit) {
-  const int tid = threadIdx.x, NT = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = NT >> 5;
-  uint32_t prefix = 0, mask = 0;
-  int remaining = k;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += NT) hist[i] = 0;
-    __syncthreads();
-    digit_histogram(keys, n, prefix, mask, shift, hist);
-    __syncthreads();
-    if (tid < 32) radix_pick_digit(hist, remaining, true, pick);
-    __syncthreads();
-    prefix |= (uint32_t)pick[0] << shift;
-    mask |= 255u << shift;
-    remaining -= pick[1];
-    __syncthreads();
-  }
-  const uint32_t T = prefix;
-  const int need_eq = remaining;
-  const int seg = ((n + nw - 1) / nw + 31) & ~31;
-  const int w0 = min(n, warp * seg), w1 = min(n, w0 + seg);
-  int c_eq = 0, c_gt = 0;
-  for (int base = w0; base < w1; base += 32) {
-    const int i = base + lane;
-    const uint32_t key = i < w1 ? keys[i] : 0u;
-    c_eq += __popc(__ballot_sync(0xffffffffu, i < w1 && key == T));
-    c_gt += __popc(__ballot_sync(0xffffffffu, i < w1 && key > T));
-  }
-  if (lane == 0) {
-    ws[warp] = c_eq;
-    ws[16 + warp] = c_gt;
-  }
-  __syncthreads();
-  int run_eq = 0, run_take = 0;
-  for (int w = 0; w < warp; ++w) {
-    const int e = ws[w];
-    run_take += ws[16 + w] + max(0, min(e, need_eq - run_eq));
-    run_eq += e;
-  }
-  const unsigned below = (1u << lane) - 1u;
-  for (int base = w0; base < w1; base += 32) {
-    const int i = base + lane;
-    const uint32_t key = i < w1 ? keys[i] : 0u;
-    const bool eq = i < w1 && key == T;
-    const unsigned eqm = __ballot_sync(0xffffffffu, eq);
-    const bool take = (i < w1 && key > T) || (eq && run_eq + __popc(eqm & below) < need_eq);
-    const unsigned tm = __ballot_sync(0xffffffffu, take);
-    if (take) emit(run_take + __popc(tm & below), i);
-    run_eq += __popc(eqm);
-    run_take += __popc(tm);
-  }
-  __syncthreads();
-}
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(Dims d, const float* __restrict__ scores,
                                                             const int* __restrict__ ctx_len, int* __restrict__ sel,
                                                             int* __restrict__ nsel, unsigned* err) {
   kvs_pdl_entry();
   extern __shared__ uint32_t skeys[];
-  __shared__ int hist[256];
-  __shared__ int ws[33];
-  __shared__ int pick[2];
+  __shared__ TopkShared sh;
+  int* hist = sh.hist;
+  int* ws = sh.ws;
+  int* pick = sh.pick;
   const int u = blockIdx.x;
   const int r = u / d.Hkv;
   const int tid = threadIdx.x, NT = blockDim.x;
@@ -127,30 +44,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(Dims d, const float*
     return;
   }
   const int nb = n_blocks_of(len, d.bs);
+  if (nb <= kTopkSmemKeys) {
+    topk_unit_smem(d, scores, len, u, sel, nsel, err, skeys, sh);
+    return;
+  }
   int* out = sel + (size_t)u * d.Kb;
-  if (nb <= d.Kb) {
-    for (int i = tid; i < nb; i += NT) out[i] = i;
-    if (tid == 0) nsel[u] = nb;
-    return;
-  }
   const float* s = scores + (size_t)u * d.nb_max;
+  // more blocks than shared memory holds: the keys are read from the scores in global memory
   const int lo_forced = d.n_sink, hi_forced = nb - d.n_recent;  // forced: b < lo || b >= hi
-  const bool cached = nb <= kTopkSmemKeys;
-  const int k_free = d.Kb - d.n_sink - d.n_recent;  // >= 0 checked at create
-  if (cached) {
-    // candidates [lo_forced, hi_forced) are contiguous: select among their cached keys, and
-    // frame the result with the forced blocks (sinks first, recent blocks last)
-    const int nc = hi_forced - lo_forced;
-    for (int i = tid; i < nc; i += NT) skeys[i] = score_key(s[lo_forced + i]);
-    for (int i = tid; i < d.n_sink; i += NT) out[i] = i;
-    for (int i = tid; i < d.n_recent; i += NT) out[d.n_sink + k_free + i] = hi_forced + i;
-    __syncthreads();
-    if (k_free > 0)
-      select_ordered(skeys, nc, k_free, hist, ws, pick, [&](int r, int i) { out[d.n_sink + r] = lo_forced + i; });
-    if (tid == 0) nsel[u] = d.Kb;
-    return;
-  }
-  auto key_of = [&](int b) -> uint32_t { return cached ? skeys[b] : score_key(s[b]); };
+  auto key_of = [&](int b) -> uint32_t { return score_key(s[b]); };
   auto is_cand = [&](int b) { return b >= lo_forced && b < hi_forced; };
 
   const int k = d.Kb - d.n_sink - d.n_recent;  // >= 0 checked at create

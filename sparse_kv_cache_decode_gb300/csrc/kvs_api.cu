@@ -695,6 +695,26 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
                  [&] { return launch_cache_update(d, L, so, no, d_ctx_len, L.slot_of_sel,
                                                   d.evict_importance ? L.scores : nullptr, d_stats, ss); });
   };
+  // top-K then update on the same selection: one fused kernel when the unit's scores fit a CTA's
+  // shared memory, else the two kernels
+  auto select = [&](int* so, int* no) {
+    if (!select_update_fusable(d)) {
+      cudaError_t r = topk(so, no);
+      return r == cudaSuccess ? update(so, no) : r;
+    }
+    cudaError_t r = cudaSuccess;
+    if (c->pf_pending[layer]) {       // a prefetch into this layer ran on another stream
+      r = cudaStreamWaitEvent(ss, c->pf_done[layer], 0);
+      c->pf_pending[layer] = 0;
+    }
+    if (r == cudaSuccess)
+      r = timed(c, KVS_K_UPDATE, ss, 1, [&] {
+        return launch_select_update(d, L, L.scores, d_ctx_len, so, no, L.slot_of_sel, d_stats, ss);
+      });
+    if (r == cudaSuccess) r = cudaEventRecord(c->sel_ready[layer], ss);   // hint for a prefetch into layer + 1
+    if (r == cudaSuccess) c->sel_pending[layer] = 1;
+    return r;
+  };
   auto fetch = [&](cudaStream_t fs) {
     return timed(c, KVS_K_FETCH, fs, 1, [&] { return launch_fetch(d, L, d_ctx_len, fs); });
   };
@@ -705,8 +725,7 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
   if (kn) e = timed(c, KVS_K_APPEND, s, 1, [&] { return launch_append(d, L, kn, vn, idx, d_ctx_len, s); });
   if (!d.lookahead) {
     if (e == cudaSuccess) e = score(sq, nq);
-    if (e == cudaSuccess) e = topk(sel, nsel);
-    if (e == cudaSuccess) e = update(sel, nsel);
+    if (e == cudaSuccess) e = select(sel, nsel);
     if (e == cudaSuccess) e = fetch(s);
     if (e == cudaSuccess) e = attn(sel, L.slot_of_sel, nsel);
     return cuda_status(e);
@@ -715,8 +734,7 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
   // it resident, on the stream that runs the selection chain, before the attention reads it
   auto bootstrap = [&](cudaStream_t fs) {
     cudaError_t r = score(q, 1);
-    if (r == cudaSuccess) r = topk(L.sel, L.nsel);
-    if (r == cudaSuccess) r = update(L.sel, L.nsel);
+    if (r == cudaSuccess) r = select(L.sel, L.nsel);
     if (r == cudaSuccess) r = fetch(fs);
     if (r == cudaSuccess) c->booted[layer] = 1;
     return r;
@@ -726,8 +744,7 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
     if (e == cudaSuccess && !c->booted[layer]) e = bootstrap(s);
     if (e == cudaSuccess) e = attn(L.pend_sel, L.pend_slot, L.pend_n);
     if (e == cudaSuccess) e = score(sq, nq);
-    if (e == cudaSuccess) e = topk(sel, nsel);
-    if (e == cudaSuccess) e = update(sel, nsel);
+    if (e == cudaSuccess) e = select(sel, nsel);
     if (e == cudaSuccess) e = fetch(s);
     return cuda_status(e);
   }
@@ -746,8 +763,7 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->upd_done[layer], 0);
   }
   if (e == cudaSuccess) e = score(sq, nq);
-  if (e == cudaSuccess) e = topk(sel, nsel);
-  if (e == cudaSuccess) e = update(sel, nsel);
+  if (e == cudaSuccess) e = select(sel, nsel);
   if (e == cudaSuccess) e = cudaEventRecord(c->upd_done[layer], ss);
   if (e == cudaSuccess) e = attn(L.pend_sel, L.pend_slot, L.pend_n);
   if (e == cudaSuccess) e = cudaEventRecord(c->attn_done[layer], s);

@@ -165,6 +165,10 @@ cudaError_t launch_topk(const Dims& d, const float* scores, const int* ctx_len, 
                         unsigned* err, cudaStream_t s, const TopkScratch* scratch);
 cudaError_t launch_cache_update(const Dims& d, const Layer& L, const int* sel, const int* nsel, const int* ctx_len,
                                 int* slot_of_sel, const float* scores, kvs_stats* stats, cudaStream_t s);
+// Top-K and cache update of each unit in one kernel (contexts of at most 16384 blocks).
+int select_update_fusable(const Dims& d);
+cudaError_t launch_select_update(const Dims& d, const Layer& L, const float* scores, const int* ctx_len, int* sel,
+                                 int* nsel, int* slot_of_sel, kvs_stats* stats, cudaStream_t s);
 // Restore a layer's cache state from a snapshot (per-unit refetch list, then the maps).
 struct SnapshotPlan {
   size_t b2s, s2b, stamp, clock, pend_sel, pend_slot, pend_n, total;

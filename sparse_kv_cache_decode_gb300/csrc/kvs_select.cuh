@@ -1,0 +1,170 @@
+// Block selection in shared memory (one CTA per unit): the radix top-k over orderable 32-bit
+// keys shared by the top-K kernels and the fused top-K + cache update kernel.
+#pragma once
+#include "kvs_block.cuh"
+#include "kvs_common.cuh"
+
+namespace kvs {
+
+constexpr int kTopkSmemKeys = 16384;   // block scores a CTA caches in shared memory (one unit)
+
+// Histogram of one 8-bit digit over the keys in shared memory that match `prefix` under
+// `mask`.  The lanes of a warp that hold the same digit add their count once (the keys of one
+// unit share their high bytes, so on the first passes most keys land in one or two bins).
+__device__ __forceinline__ void digit_histogram(const uint32_t* keys, int n, uint32_t prefix, uint32_t mask,
+                                                int shift, int* hist) {
+  const int lane = threadIdx.x & 31;
+  for (int base = threadIdx.x - lane; base < n; base += blockDim.x) {   // warp-uniform trip count
+    const int i = base + lane;
+    int bin = -1;
+    if (i < n) {
+      const uint32_t key = keys[i];
+      if ((key & mask) == prefix) bin = (int)((key >> shift) & 255u);
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+    if (bin >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+  }
+}
+
+// Top k of keys[0, n) in shared memory by (key desc, position asc); emit(rank, i) is called for
+// each selected position i, ranks 0..k-1 in ascending position order.  Every thread of the CTA
+// (at most 512) must call it.  Requires 0 < k < n.  ws holds at least 33 ints.
+//
+// The threshold key T and the number of keys equal to T still needed come from 8-bit radix passes
+// (at most four), cut short once at most 32 keys still match the prefix.  The compaction gives
+// each warp a contiguous segment of positions and walks it 32 keys at a time (lane i reads
+// position base + i: no bank conflicts); ballots give each lane its rank among the equal keys and
+// among the taken keys.
+template <class Emit>
+__device__ void select_ordered(const uint32_t* keys, int n, int k, int* hist, int* ws, int* pick, Emit emit) {
+  const int tid = threadIdx.x, NT = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = NT >> 5;
+  uint32_t prefix = 0, mask = 0;
+  int remaining = k;
+  if (tid == 0) ws[32] = 0;   // gather counter of the short finish (below)
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 256; i += NT) hist[i] = 0;
+    __syncthreads();
+    digit_histogram(keys, n, prefix, mask, shift, hist);
+    __syncthreads();
+    if (tid < 32) radix_pick_digit(hist, remaining, true, pick);
+    __syncthreads();
+    prefix |= (uint32_t)pick[0] << shift;
+    mask |= 255u << shift;
+    remaining -= pick[1];
+    const int in_bin = hist[pick[0]];   // keys that match the longer prefix
+    __syncthreads();
+    if (pass < 3 && in_bin <= 32) {
+      // Short finish: the threshold is the remaining-th largest of the <= 32 keys that match the
+      // prefix.  They are gathered (in any order) into the free histogram, and one warp finds it
+      // by counting, for each key, the keys above it and equal to it.
+      for (int i = tid; i < n; i += NT) {
+        const uint32_t key = keys[i];
+        if ((key & mask) == prefix) hist[atomicAdd(&ws[32], 1)] = (int)key;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const int cnt = ws[32];
+        const uint32_t mine = lane < cnt ? (uint32_t)hist[lane] : 0u;
+        int gt = 0, eq = 0;
+        for (int j = 0; j < cnt; ++j) {
+          const uint32_t kj = (uint32_t)__shfl_sync(0xffffffffu, (int)mine, j);
+          gt += kj > mine;
+          eq += kj == mine;
+        }
+        const bool is_t = lane < cnt && gt < remaining && remaining <= gt + eq;
+        const int src = __ffs(__ballot_sync(0xffffffffu, is_t)) - 1;   // some lane holds the threshold
+        const int t_gt = __shfl_sync(0xffffffffu, gt, src);
+        const uint32_t t_key = (uint32_t)__shfl_sync(0xffffffffu, (int)mine, src);
+        if (lane == 0) {
+          pick[0] = (int)t_key;
+          pick[1] = remaining - t_gt;
+        }
+      }
+      __syncthreads();
+      prefix = (uint32_t)pick[0];
+      remaining = pick[1];
+      __syncthreads();   // pick and hist are free again
+      break;
+    }
+  }
+  const uint32_t T = prefix;
+  const int need_eq = remaining;
+  const int seg = ((n + nw - 1) / nw + 31) & ~31;
+  const int w0 = min(n, warp * seg), w1 = min(n, w0 + seg);
+  int c_eq = 0, c_gt = 0;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < w1 ? keys[i] : 0u;
+    c_eq += __popc(__ballot_sync(0xffffffffu, i < w1 && key == T));
+    c_gt += __popc(__ballot_sync(0xffffffffu, i < w1 && key > T));
+  }
+  if (lane == 0) {
+    ws[warp] = c_eq;
+    ws[16 + warp] = c_gt;
+  }
+  __syncthreads();
+  int run_eq = 0, run_take = 0;
+  for (int w = 0; w < warp; ++w) {
+    const int e = ws[w];
+    run_take += ws[16 + w] + max(0, min(e, need_eq - run_eq));
+    run_eq += e;
+  }
+  const unsigned below = (1u << lane) - 1u;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < w1 ? keys[i] : 0u;
+    const bool eq = i < w1 && key == T;
+    const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+    const bool take = (i < w1 && key > T) || (eq && run_eq + __popc(eqm & below) < need_eq);
+    const unsigned tm = __ballot_sync(0xffffffffu, take);
+    if (take) emit(run_take + __popc(tm & below), i);
+    run_eq += __popc(eqm);
+    run_take += __popc(tm);
+  }
+  __syncthreads();
+}
+
+
+struct TopkShared {
+  int hist[256];
+  int ws[33];
+  int pick[2];
+};
+
+// Selection of unit u from its block scores when the unit's candidates fit the `skeys` shared
+// buffer (at most cap keys): forced sink and recent blocks plus the top (K_b - forced) other
+// blocks by (score desc, block asc), in ascending block order, into sel[u][..] and nsel[u].  A
+// context length out of range is reported as KVS_ERR_BAD_INDEX (nothing written).  Every thread
+// of the CTA must call it.
+__device__ inline void topk_unit_smem(const Dims& d, const float* __restrict__ scores, int len, int u,
+                                      int* __restrict__ sel, int* __restrict__ nsel, unsigned* err, uint32_t* skeys,
+                                      TopkShared& sh) {
+  const int tid = threadIdx.x, NT = blockDim.x;
+  if (len < 0 || len > d.max_ctx) {
+    if (tid == 0) set_error(err, KVS_ERR_BAD_INDEX);
+    return;
+  }
+  const int nb = n_blocks_of(len, d.bs);
+  int* out = sel + (size_t)u * d.Kb;
+  if (nb <= d.Kb) {
+    for (int i = tid; i < nb; i += NT) out[i] = i;
+    if (tid == 0) nsel[u] = nb;
+    return;
+  }
+  const float* s = scores + (size_t)u * d.nb_max;
+  const int lo_forced = d.n_sink, hi_forced = nb - d.n_recent;  // forced: b < lo || b >= hi
+  const int k_free = d.Kb - d.n_sink - d.n_recent;              // >= 0 checked at create
+  // candidates [lo_forced, hi_forced) are contiguous: select among their cached keys, and frame
+  // the result with the forced blocks (sinks first, recent blocks last)
+  const int nc = hi_forced - lo_forced;
+  for (int i = tid; i < nc; i += NT) skeys[i] = score_key(s[lo_forced + i]);
+  for (int i = tid; i < d.n_sink; i += NT) out[i] = i;
+  for (int i = tid; i < d.n_recent; i += NT) out[d.n_sink + k_free + i] = hi_forced + i;
+  __syncthreads();
+  if (k_free > 0)
+    select_ordered(skeys, nc, k_free, sh.hist, sh.ws, sh.pick, [&](int r, int i) { out[d.n_sink + r] = lo_forced + i; });
+  if (tid == 0) nsel[u] = d.Kb;
+}
+
+}  // namespace kvs

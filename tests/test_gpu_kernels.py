@@ -146,6 +146,47 @@ def test_topk_select_bit_exact(lens, budget, sink, recent, bs):
     assert g.ctx.poll_error() == 0
 
 
+def _threshold_dup_scores(seed, n, k, mode):
+    """Scores whose k-th largest value (the top-K threshold) recurs a few times: fine values
+    ('fine': the threshold's 8-bit digit bin holds a few keys after the second radix pass) or
+    values spread over many exponents and both signs ('spread': already after the first)."""
+    u = W.uniform_f32(seed, 9, n, 0.0, 1.0).astype(np.float64)
+    if mode == "fine":
+        s = (0.5 + 2.5 * u).astype(np.float32)
+    else:
+        e = W.uniform_f32(seed, 10, n, -60.0, 60.0).astype(np.float64)
+        sign = np.where(W.uniform_f32(seed, 11, n, 0.0, 1.0) < 0.3, -1.0, 1.0)
+        s = (sign * np.exp2(e) * (1.0 + u)).astype(np.float32)
+    t = np.sort(s)[::-1][k - 1]
+    pos = W.randint(seed, 12, 5, n)
+    s[pos] = t                                   # duplicates of the threshold value
+    return s
+
+
+@pytest.mark.parametrize("mode", ["fine", "spread"])
+def test_topk_select_threshold_ties_bit_exact(mode):
+    lens, budget, sink, recent = [32768, 20000, 7001], 128, 1, 2
+    w = W.TINY.with_(name="topk_ties", n_req=len(lens), ctx0=max(lens), budget_blocks=budget, n_sink=sink,
+                     n_recent=recent, cap_blocks=budget, n_heavy=0, n_layer=1)
+    g = GpuCase(w, lens)
+    nbm = g.nb_max
+    k = budget - sink - recent
+    host = np.stack([np.stack([_threshold_dup_scores(31 + r * 5 + h, nbm, k, mode) for h in range(w.n_kv_head)])
+                     for r in range(w.n_req)])
+    scores = torch.from_numpy(host).cuda()
+    sel = torch.full((w.n_req, w.n_kv_head, budget), -7, dtype=torch.int32, device="cuda")
+    nsel = torch.zeros((w.n_req, w.n_kv_head), dtype=torch.int32, device="cuda")
+    g.ctx.topk_select(scores, g.ctx_len, sel, nsel)
+    gs, gn = sel.cpu().numpy(), nsel.cpu().numpy()
+    for r, L in enumerate(lens):
+        for h in range(w.n_kv_head):
+            nb = _nb(L, w.block_size)
+            ref = select_blocks(host[r, h], nb, budget, sink, recent)
+            assert gn[r, h] == len(ref)
+            np.testing.assert_array_equal(gs[r, h, :len(ref)], ref, err_msg=f"unit {(r, h)}")
+    assert g.ctx.poll_error() == 0
+
+
 def _correlated_selections(seed, nb, budget, steps, keep=0.7):
     rng = np.random.default_rng(seed)
     cur = np.sort(rng.choice(nb, min(budget, nb), replace=False))
