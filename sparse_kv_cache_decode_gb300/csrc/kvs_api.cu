@@ -156,7 +156,7 @@ Plan plan_of(const Dims& d) {
   if (attention_tma_supported(d)) parts = std::max<size_t>(parts, (size_t)attention_tma_partials(d));
   p.part = align_up(U * parts * d.G * d.dv * 4);
   p.ml = align_up(U * parts * d.G * 2 * 4);
-  p.done = align_up(U * 4);
+  p.done = align_up(U * 8);   // attention and scoring completion counters, U each
   const size_t P = (size_t)topk_chunks(d);
   p.tk_key = 2 * align_up(U * P * d.Kb * 4);   // one copy per layer parity
   p.tk_idx = 2 * align_up(U * P * d.Kb * 4);
@@ -356,6 +356,7 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
     L.attn_part = part;
     L.attn_ml = ml;
     L.unit_done = done;
+    L.score_done = done + d.U;
     L.host_k = L.host_v = nullptr;
     L.err = c->err;
     // slot pools start zeroed: rows past a context end that a tile still reads are then zeros
@@ -755,6 +756,30 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
   // selection, which the attention must no longer be reading.  Layers of one parity share the
   // block-score and top-K scratch, so their chains run on the same one of the two selection streams.
   ss = c->sel_stream[layer & 1];
+  if (layer_kernel_supported(d, nq, L.tmK && L.tmV)) {
+    // one kernel on `s` runs this layer's attention over S_t beside the selection of S_{t+1} (a
+    // fixed split of one wave of CTAs); the fetch then waits for it on the copy stream
+    if (e == cudaSuccess && !c->booted[layer]) {
+      // the bootstrap's selection chain runs on the selection stream after the work queued on `s`
+      // (the inputs), and `s` waits for it
+      e = cudaEventRecord(c->layer_start[layer], s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(ss, c->layer_start[layer], 0);
+      if (e == cudaSuccess) e = bootstrap(ss);
+      if (e == cudaSuccess) e = cudaEventRecord(c->upd_done[layer], ss);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->upd_done[layer], 0);
+    }
+    if (e == cudaSuccess)
+      e = timed(c, KVS_K_ATTN, s, 1,
+                [&] { return launch_layer(d, L, q, idx, sq, nq, d_ctx_len, d_out, sel, nsel, d_stats, s); });
+    if (e == cudaSuccess) e = cudaEventRecord(c->sel_ready[layer], s);   // hint for a prefetch into layer + 1
+    if (e == cudaSuccess) c->sel_pending[layer] = 1;
+    if (e == cudaSuccess) e = cudaEventRecord(c->attn_done[layer], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, c->attn_done[layer], 0);
+    if (e == cudaSuccess) e = fetch(cs);
+    if (e == cudaSuccess) e = cudaEventRecord(c->fetch_done[layer], cs);
+    if (e == cudaSuccess) c->fetch_pending[layer] = 1;
+    return cuda_status(e);
+  }
   if (e == cudaSuccess) e = cudaEventRecord(c->layer_start[layer], s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(ss, c->layer_start[layer], 0);
   if (e == cudaSuccess && !c->booted[layer]) {

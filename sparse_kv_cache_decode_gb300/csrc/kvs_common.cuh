@@ -57,6 +57,7 @@ struct Layer {
   float* attn_part;      // [U][n_split_max][Hq/Hkv][dv] partial outputs
   float* attn_ml;        // [U][n_split_max][Hq/Hkv][2] partial (max, sum)
   unsigned* unit_done;   // [U] CTAs finished per unit in the current attention launch (0 between launches)
+  unsigned* score_done;  // [U] scoring CTAs finished per unit in the current layer-kernel launch (0 between launches)
   const __nv_bfloat16* host_k;  // device-mapped host history of this layer [B][Hkv][max_ctx][dk]
   const __nv_bfloat16* host_v;  // [B][Hkv][max_ctx][dv] or nullptr
   unsigned* err;         // sticky status word (shared by all layers)
@@ -167,6 +168,13 @@ cudaError_t launch_cache_update(const Dims& d, const Layer& L, const int* sel, c
                                 int* slot_of_sel, const float* scores, kvs_stats* stats, cudaStream_t s);
 // Top-K and cache update of each unit in one kernel (contexts of at most 16384 blocks).
 int select_update_fusable(const Dims& d);
+// Overlapped lookahead layer in one kernel: attention over the pending selection, scoring with the
+// drafts, top-K and cache update (GQA groups of up to 8, the TMA attention path, the mma.sync
+// scoring path with up to 32 scoring rows, at most one unit per SM).
+int layer_kernel_supported(const Dims& d, int nq, bool have_tmaps);
+cudaError_t launch_layer(const Dims& d, const Layer& L, const __nv_bfloat16* q, const __nv_bfloat16* index,
+                         const __nv_bfloat16* sq, int nq, const int* ctx_len, float* out, int* sel, int* nsel,
+                         kvs_stats* stats, cudaStream_t s);
 cudaError_t launch_select_update(const Dims& d, const Layer& L, const float* scores, const int* ctx_len, int* sel,
                                  int* nsel, int* slot_of_sel, kvs_stats* stats, cudaStream_t s);
 // Restore a layer's cache state from a snapshot (per-unit refetch list, then the maps).

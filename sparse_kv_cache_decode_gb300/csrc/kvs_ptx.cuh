@@ -14,6 +14,8 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem), "r"(src_bytes)
                : "memory");
 }
+// Wait until every cp.async this thread issued has landed in shared memory.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
@@ -203,6 +205,32 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+}  // namespace kvs
+
+namespace kvs {
+
+// Copies n 32-bit words global -> shared, spread over the CTA's threads, read through L2 (the words
+// may have been written by other CTAs of the running kernel): asynchronous 16-byte copies when both
+// ends are 16-byte aligned and n is a multiple of 4 (the caller waits with cp_async_wait_all and
+// synchronises the CTA before reading), else loads eight at a time per thread.
+__device__ __forceinline__ void stage_words(void* smem_dst, const void* gsrc, int n) {
+  const int tid = threadIdx.x, NT = blockDim.x;
+  unsigned* dst = static_cast<unsigned*>(smem_dst);
+  const unsigned* src = static_cast<const unsigned*>(gsrc);
+  if (((reinterpret_cast<uintptr_t>(gsrc) | (uintptr_t)smem_u32(smem_dst)) & 15u) == 0 && (n & 3) == 0) {
+    for (int i = tid; i < n / 4; i += NT) cp_async16(dst + 4 * i, src + 4 * i, 16);
+    return;
+  }
+  for (int i0 = tid; i0 < n; i0 += 8 * NT) {
+    unsigned v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = i0 + k * NT < n ? __ldcg(src + i0 + k * NT) : 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (i0 + k * NT < n) dst[i0 + k * NT] = v[k];
+  }
 }
 
 }  // namespace kvs

@@ -3,6 +3,7 @@
 #pragma once
 #include "kvs_block.cuh"
 #include "kvs_common.cuh"
+#include "kvs_ptx.cuh"
 
 namespace kvs {
 
@@ -133,38 +134,70 @@ struct TopkShared {
 };
 
 // Selection of unit u from its block scores when the unit's candidates fit the `skeys` shared
-// buffer (at most cap keys): forced sink and recent blocks plus the top (K_b - forced) other
-// blocks by (score desc, block asc), in ascending block order, into sel[u][..] and nsel[u].  A
-// context length out of range is reported as KVS_ERR_BAD_INDEX (nothing written).  Every thread
-// of the CTA must call it.
-__device__ inline void topk_unit_smem(const Dims& d, const float* __restrict__ scores, int len, int u,
-                                      int* __restrict__ sel, int* __restrict__ nsel, unsigned* err, uint32_t* skeys,
-                                      TopkShared& sh) {
+// buffer: forced sink and recent blocks plus the top (K_b - forced) other blocks by (score desc,
+// block asc), in ascending block order, into sel[u][..] and nsel[u].  In two phases, so that the
+// score reads can travel with other reads of the caller:
+//   topk_stage issues the reads of the unit's score row (blocks [0, nb - n_recent)) into skeys,
+//   through L2 (the scores may have been written by other CTAs of the running kernel);
+//   after cp_async_wait_all and a CTA barrier, topk_staged turns them into orderable keys in
+//   place and selects; it returns the selection's count (also copied to out_s when not null), or
+//   -1 for a context length out of range (KVS_ERR_BAD_INDEX, nothing written).
+// Every thread of the CTA calls both.
+__device__ inline void topk_stage(const Dims& d, const float* scores, int len, int u, uint32_t* skeys) {
+  if (len < 0 || len > d.max_ctx) return;
+  const int nb = n_blocks_of(len, d.bs);
+  if (nb <= d.Kb) return;
+  const int n_stage = min(d.nb_max, (nb - d.n_recent + 3) & ~3);
+  stage_words(skeys, scores + (size_t)u * d.nb_max, n_stage);
+}
+
+__device__ inline int topk_staged(const Dims& d, int len, int u, int* __restrict__ sel, int* __restrict__ nsel,
+                                  unsigned* err, uint32_t* skeys, int* out_s, TopkShared& sh) {
   const int tid = threadIdx.x, NT = blockDim.x;
   if (len < 0 || len > d.max_ctx) {
     if (tid == 0) set_error(err, KVS_ERR_BAD_INDEX);
-    return;
+    return -1;
   }
   const int nb = n_blocks_of(len, d.bs);
   int* out = sel + (size_t)u * d.Kb;
   if (nb <= d.Kb) {
-    for (int i = tid; i < nb; i += NT) out[i] = i;
+    for (int i = tid; i < nb; i += NT) {
+      out[i] = i;
+      if (out_s) out_s[i] = i;
+    }
     if (tid == 0) nsel[u] = nb;
-    return;
+    return nb;
   }
-  const float* s = scores + (size_t)u * d.nb_max;
   const int lo_forced = d.n_sink, hi_forced = nb - d.n_recent;  // forced: b < lo || b >= hi
   const int k_free = d.Kb - d.n_sink - d.n_recent;              // >= 0 checked at create
-  // candidates [lo_forced, hi_forced) are contiguous: select among their cached keys, and frame
-  // the result with the forced blocks (sinks first, recent blocks last)
-  const int nc = hi_forced - lo_forced;
-  for (int i = tid; i < nc; i += NT) skeys[i] = score_key(s[lo_forced + i]);
-  for (int i = tid; i < d.n_sink; i += NT) out[i] = i;
-  for (int i = tid; i < d.n_recent; i += NT) out[d.n_sink + k_free + i] = hi_forced + i;
+  // candidates [lo_forced, hi_forced) are contiguous: their keys, in place (each thread converts
+  // the words it reads); the result is framed with the forced blocks (sinks first, recent last)
+  for (int b = lo_forced + tid; b < hi_forced; b += NT) skeys[b] = score_key(__uint_as_float(skeys[b]));
+  for (int i = tid; i < d.n_sink; i += NT) {
+    out[i] = i;
+    if (out_s) out_s[i] = i;
+  }
+  for (int i = tid; i < d.n_recent; i += NT) {
+    out[d.n_sink + k_free + i] = hi_forced + i;
+    if (out_s) out_s[d.n_sink + k_free + i] = hi_forced + i;
+  }
   __syncthreads();
   if (k_free > 0)
-    select_ordered(skeys, nc, k_free, sh.hist, sh.ws, sh.pick, [&](int r, int i) { out[d.n_sink + r] = lo_forced + i; });
+    select_ordered(skeys + lo_forced, hi_forced - lo_forced, k_free, sh.hist, sh.ws, sh.pick, [&](int r, int i) {
+      out[d.n_sink + r] = lo_forced + i;
+      if (out_s) out_s[d.n_sink + r] = lo_forced + i;
+    });
   if (tid == 0) nsel[u] = d.Kb;
+  return d.Kb;
+}
+
+// Both phases back to back (the score reads alone in their round).
+__device__ inline void topk_unit_smem(const Dims& d, const float* scores, int len, int u, int* __restrict__ sel,
+                                      int* __restrict__ nsel, unsigned* err, uint32_t* skeys, TopkShared& sh) {
+  topk_stage(d, scores, len, u, skeys);
+  cp_async_wait_all();
+  __syncthreads();
+  topk_staged(d, len, u, sel, nsel, err, skeys, nullptr, sh);
 }
 
 }  // namespace kvs
