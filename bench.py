@@ -314,7 +314,8 @@ def dependency_bound_ms(w, per_layer, link_per_layer, hbm_peak, link_peak):
 
 # ----------------------------------------------------------------------------- ncu traffic
 
-KERNEL_SOURCES = {"attn": ["k_attn_tma.cu", "k_attn.cu"], "score": ["k_score.cu", "k_score_tc.cu"],
+KERNEL_SOURCES = {"attn": ["k_attn_tma.cu", "kvs_attn_tma.cuh", "k_attn.cu"],
+                  "score": ["k_score.cu", "kvs_score.cuh", "k_score_tc.cu"],
                   "fetch": ["k_cache.cu"]}
 
 

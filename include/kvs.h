@@ -218,11 +218,14 @@ kvs_status kvs_sparse_decode_attn(kvs_ctx* ctx, int layer, const void* d_q, cons
  *   lookahead mode: [append] -> attention over the previous selection, and score(drafts) ->
  *                   select -> update with that selection pinned -> fetch on copy_stream.
  * The first lookahead step of a layer has no previous selection and runs the sync part first.
- * Lookahead with a separate copy_stream overlaps the two halves [SPEC 1, OASIS module 2]: the
- * selection chain (score, select, update) runs on one of two streams the context owns (one per
- * layer parity), starting once the work enqueued on `stream` before this call (the layer below's
- * attention) has finished, beside this layer's attention on `stream` and the chain of the layer
- * below; the fetch on copy_stream waits for the chain and the attention.
+ * Lookahead with a separate copy_stream overlaps the two halves [SPEC 1, OASIS module 2].  For
+ * GQA groups of up to 8 heads on the TMA attention path, with up to 32 scoring rows, one kernel on
+ * `stream` runs both on a fixed split of the SMs: attention CTAs, scoring CTAs, and per unit the
+ * last scoring CTA to finish runs the select + update; the fetch on copy_stream follows it.
+ * Otherwise the selection chain (score, select, update) runs on one of two streams the context
+ * owns (one per layer parity), starting once the work enqueued on `stream` before this call (the
+ * layer below's attention) has finished, beside this layer's attention on `stream` and the chain
+ * of the layer below; the fetch on copy_stream waits for the chain and the attention.
  * k_new / v_new NULL: no append (else as kvs_append, after kvs_advance_ctx).  d_score_q NULL
  * scores with d_q (nq = 1).  copy_stream NULL or == stream: the fetch runs on stream.  With a
  * separate copy_stream the caller calls kvs_join before reusing the layer or ending a capture.

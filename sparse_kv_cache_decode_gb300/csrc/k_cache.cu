@@ -43,7 +43,8 @@ __global__ void __launch_bounds__(kCacheThreads) select_update_kernel(Dims d, La
   topk_stage(d, scores, in.len, u, keys);
   cp_async_wait_all();
   __syncthreads();
-  in.n = topk_staged(d, in.len, u, sel, nsel, L.err, keys, update_sel_buffer(d, smraw), tsh);
+  in.n = topk_staged(d, in.len, u, sel, nsel, L.err, keys, update_sel_buffer(d, smraw), tsh,
+                     reinterpret_cast<uint32_t*>(smraw + select_scratch_offset(d)));
   __syncthreads();
   update_run(d, L, u, in, slot_of_sel, d.evict_importance ? scores : nullptr, stats, smraw, ush);
 }
@@ -366,13 +367,13 @@ cudaError_t launch_cache_update(const Dims& d, const Layer& L, const int* sel, c
 int select_update_fusable(const Dims& d) { return d.nb_max <= kTopkSmemKeys; }
 
 cudaError_t launch_select_update(const Dims& d, const Layer& L, const float* scores, const int* ctx_len, int* sel,
-                                 int* nsel, int* slot_of_sel, kvs_stats* stats, cudaStream_t s) {
+                                 int* nsel, int* slot_of_sel, kvs_stats* stats, cudaStream_t s, int threads) {
   const size_t smem = select_update_smem_bytes(d);
   if (smem > 48 * 1024) {
     cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(select_update_kernel), (int)smem);
     if (e != cudaSuccess) return e;
   }
-  launch_pdl(select_update_kernel, dim3(d.U), dim3(kCacheThreads), smem, s, d, L, scores, ctx_len, sel, nsel,
+  launch_pdl(select_update_kernel, dim3(d.U), dim3(threads), smem, s, d, L, scores, ctx_len, sel, nsel,
              slot_of_sel, stats);
   return cudaGetLastError();
 }

@@ -67,7 +67,8 @@ __global__ void __maxnreg__(160)
   topk_stage(d, L.scores, in.len, u, keys);
   cp_async_wait_all();
   __syncthreads();
-  in.n = topk_staged(d, in.len, u, sel, nsel, L.err, keys, update_sel_buffer(d, smem_raw), tsh);
+  in.n = topk_staged(d, in.len, u, sel, nsel, L.err, keys, update_sel_buffer(d, smem_raw), tsh,
+                     reinterpret_cast<uint32_t*>(smem_raw + select_scratch_offset(d)));
   __syncthreads();
   update_run(d, L, u, in, L.slot_of_sel, d.evict_importance ? L.scores : nullptr, stats, smem_raw, ush);
 }

@@ -175,8 +175,9 @@ int layer_kernel_supported(const Dims& d, int nq, bool have_tmaps);
 cudaError_t launch_layer(const Dims& d, const Layer& L, const __nv_bfloat16* q, const __nv_bfloat16* index,
                          const __nv_bfloat16* sq, int nq, const int* ctx_len, float* out, int* sel, int* nsel,
                          kvs_stats* stats, cudaStream_t s);
+// threads: the CTA size (a multiple of 32, at most 512).
 cudaError_t launch_select_update(const Dims& d, const Layer& L, const float* scores, const int* ctx_len, int* sel,
-                                 int* nsel, int* slot_of_sel, kvs_stats* stats, cudaStream_t s);
+                                 int* nsel, int* slot_of_sel, kvs_stats* stats, cudaStream_t s, int threads = 512);
 // Restore a layer's cache state from a snapshot (per-unit refetch list, then the maps).
 struct SnapshotPlan {
   size_t b2s, s2b, stamp, clock, pend_sel, pend_slot, pend_n, total;

@@ -133,6 +133,85 @@ struct TopkShared {
   int pick[2];
 };
 
+constexpr int kTopkSample = 256;       // sampled keys of the threshold guess
+constexpr int kTopkFastMax = 1024;     // keys at or above the guess kept for the exact selection
+constexpr int kTopkFastScratch = kTopkSample + 2 * kTopkFastMax;   // 32-bit words of shared scratch
+
+// select_ordered, fronted by a threshold guess when the keys are many: T0 = a sampled key of rank
+// about 1.25 k n / 256 among 256 evenly spaced keys; if between k and kTopkFastMax keys are >= T0,
+// they (with their positions, in position order) are the only candidates: every selected key and
+// every key equal to the k-th largest is >= T0, so the exact selection among them is the same.
+// Otherwise the full selection runs.  scratch: kTopkFastScratch words of shared memory, or null
+// (always the full selection).  Same contract as select_ordered.
+template <class Emit>
+__device__ void select_topk(const uint32_t* keys, int n, int k, uint32_t* scratch, TopkShared& sh, Emit emit) {
+  const int tid = threadIdx.x, NT = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = NT >> 5;
+  if (scratch == nullptr || n < 4 * k || n <= 2 * kTopkSample) {
+    select_ordered(keys, n, k, sh.hist, sh.ws, sh.pick, emit);
+    return;
+  }
+  uint32_t* sample = scratch;
+  uint32_t* lkey = scratch + kTopkSample;
+  int* lpos = reinterpret_cast<int*>(lkey + kTopkFastMax);
+  for (int i = tid; i < kTopkSample; i += NT) sample[i] = keys[(long long)i * n / kTopkSample];
+  const int ks = min(kTopkSample, (int)(1.25f * (float)k * kTopkSample / (float)n) + 8);
+  if (tid == 0) sh.ws[32] = 0;
+  __syncthreads();
+  // the ks-th largest sampled key (ties by sample index)
+  for (int i = tid; i < kTopkSample; i += NT) {
+    const uint32_t v = sample[i];
+    int r = 0;
+    for (int j = 0; j < kTopkSample; ++j) {
+      const uint32_t sj = sample[j];
+      r += sj > v || (sj == v && j < i);
+    }
+    if (r == ks - 1) sh.pick[0] = (int)v;
+  }
+  __syncthreads();
+  const uint32_t T0 = (uint32_t)sh.pick[0];
+  // keys >= T0, counted a warp at a time
+  const int seg = ((n + nw - 1) / nw + 31) & ~31;
+  const int w0 = min(n, warp * seg), w1 = min(n, w0 + seg);
+  int cw = 0;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    cw += __popc(__ballot_sync(0xffffffffu, i < w1 && keys[i] >= T0));
+  }
+  if (lane == 0) {
+    sh.ws[warp] = cw;
+    atomicAdd(&sh.ws[32], cw);
+  }
+  __syncthreads();
+  const int cnt = sh.ws[32];
+  if (cnt < k || cnt > kTopkFastMax) {
+    __syncthreads();
+    select_ordered(keys, n, k, sh.hist, sh.ws, sh.pick, emit);
+    return;
+  }
+  // ordered compaction of the keys >= T0 (warp segments in order, ballots within a segment)
+  int off = 0;
+  for (int w = 0; w < warp; ++w) off += sh.ws[w];
+  const unsigned below = (1u << lane) - 1u;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t key = i < w1 ? keys[i] : 0u;
+    const bool p = i < w1 && key >= T0;
+    const unsigned m = __ballot_sync(0xffffffffu, p);
+    if (p) {
+      lkey[off + __popc(m & below)] = key;
+      lpos[off + __popc(m & below)] = i;
+    }
+    off += __popc(m);
+  }
+  __syncthreads();
+  if (cnt == k) {
+    for (int i = tid; i < cnt; i += NT) emit(i, lpos[i]);
+    __syncthreads();
+    return;
+  }
+  select_ordered(lkey, cnt, k, sh.hist, sh.ws, sh.pick, [&](int r, int i) { emit(r, lpos[i]); });
+}
+
 // Selection of unit u from its block scores when the unit's candidates fit the `skeys` shared
 // buffer: forced sink and recent blocks plus the top (K_b - forced) other blocks by (score desc,
 // block asc), in ascending block order, into sel[u][..] and nsel[u].  In two phases, so that the
@@ -141,7 +220,8 @@ struct TopkShared {
 //   through L2 (the scores may have been written by other CTAs of the running kernel);
 //   after cp_async_wait_all and a CTA barrier, topk_staged turns them into orderable keys in
 //   place and selects; it returns the selection's count (also copied to out_s when not null), or
-//   -1 for a context length out of range (KVS_ERR_BAD_INDEX, nothing written).
+//   -1 for a context length out of range (KVS_ERR_BAD_INDEX, nothing written); fast_scratch
+//   (kTopkFastScratch words of shared memory, or null) enables select_topk's threshold guess.
 // Every thread of the CTA calls both.
 __device__ inline void topk_stage(const Dims& d, const float* scores, int len, int u, uint32_t* skeys) {
   if (len < 0 || len > d.max_ctx) return;
@@ -152,7 +232,8 @@ __device__ inline void topk_stage(const Dims& d, const float* scores, int len, i
 }
 
 __device__ inline int topk_staged(const Dims& d, int len, int u, int* __restrict__ sel, int* __restrict__ nsel,
-                                  unsigned* err, uint32_t* skeys, int* out_s, TopkShared& sh) {
+                                  unsigned* err, uint32_t* skeys, int* out_s, TopkShared& sh,
+                                  uint32_t* fast_scratch = nullptr) {
   const int tid = threadIdx.x, NT = blockDim.x;
   if (len < 0 || len > d.max_ctx) {
     if (tid == 0) set_error(err, KVS_ERR_BAD_INDEX);
@@ -183,7 +264,7 @@ __device__ inline int topk_staged(const Dims& d, int len, int u, int* __restrict
   }
   __syncthreads();
   if (k_free > 0)
-    select_ordered(skeys + lo_forced, hi_forced - lo_forced, k_free, sh.hist, sh.ws, sh.pick, [&](int r, int i) {
+    select_topk(skeys + lo_forced, hi_forced - lo_forced, k_free, fast_scratch, sh, [&](int r, int i) {
       out[d.n_sink + r] = lo_forced + i;
       if (out_s) out_s[d.n_sink + r] = lo_forced + i;
     });

@@ -8,6 +8,7 @@
 #include "kvs_block.cuh"
 #include "kvs_common.cuh"
 #include "kvs_ptx.cuh"
+#include "kvs_select.cuh"
 
 namespace kvs {
 
@@ -116,6 +117,7 @@ struct UpdateShared {
   int ws[33];
   int pick[2];
   int bad;
+  int n_ck;                   // eligible slots gathered for the victim ranking
   unsigned long long cnt[4];  // hits, prefetch hits, evictions, bytes
 };
 
@@ -283,16 +285,28 @@ __device__ inline void update_run(const Dims& d, const Layer& L, int u, const Up
     return imp_u ? score_key(__ldcg(imp_u + b)) + 1u : sm.st[s];
   };
   if (d.C <= kRankVictimsMaxC) {
-    // the m smallest (key, slot) among the eligible slots by rank counting: one word per slot,
-    // all-ones for ineligible ones (never below an eligible word)
-    for (int s = tid; s < d.C; s += NT) ck[s] = elig(s) ? ((unsigned long long)vkey(s) << 32) | (unsigned)s : ~0ull;
+    // the m smallest (key, slot) among the eligible slots by rank counting: the eligible slots'
+    // (key, slot) words are gathered first (in any order: a rank depends only on the values), then
+    // each is ranked against the others
+    if (tid == 0) sh.n_ck = 0;
     __syncthreads();
-    for (int s = tid; s < d.C; s += NT) {
-      const unsigned long long mine = ck[s];
-      if (mine == ~0ull) continue;
+    const int lane = tid & 31;
+    for (int s0 = tid - lane; s0 < d.C; s0 += NT) {   // warp-uniform trip count
+      const int s = s0 + lane;
+      const bool e = s < d.C && elig(s);
+      const unsigned em = __ballot_sync(0xffffffffu, e);
+      int base = 0;
+      if (lane == 0 && em) base = atomicAdd(&sh.n_ck, __popc(em));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (e) ck[base + __popc(em & ((1u << lane) - 1u))] = ((unsigned long long)vkey(s) << 32) | (unsigned)s;
+    }
+    __syncthreads();
+    const int ne = sh.n_ck;
+    for (int i = tid; i < ne; i += NT) {
+      const unsigned long long mine = ck[i];
       int rank = 0;
-      for (int t = 0; t < d.C; ++t) rank += ck[t] < mine;
-      if (rank < m) sm.vict[rank] = s;
+      for (int t = 0; t < ne; ++t) rank += ck[t] < mine;
+      if (rank < m) sm.vict[rank] = (int)(mine & 0xffffffffu);
     }
     __syncthreads();
   } else {
@@ -342,10 +356,14 @@ __device__ inline void update_run(const Dims& d, const Layer& L, int u, const Up
 }
 
 // Top-K + update of one unit in one CTA: the update's shared memory, then the unit's score row
-// (nb_max words, turned into keys in place) from a 16-byte aligned offset.
+// (nb_max words, turned into keys in place) from a 16-byte aligned offset, then the top-K's
+// threshold-guess scratch.
 __host__ __device__ inline size_t select_keys_offset(const Dims& d) { return (update_smem_bytes(d) + 15) / 16 * 16; }
+__host__ __device__ inline size_t select_scratch_offset(const Dims& d) {
+  return (select_keys_offset(d) + (size_t)d.nb_max * 4 + 15) / 16 * 16;
+}
 __host__ __device__ inline size_t select_update_smem_bytes(const Dims& d) {
-  return select_keys_offset(d) + (size_t)d.nb_max * 4;
+  return select_scratch_offset(d) + (size_t)kTopkFastScratch * 4;
 }
 
 // The cache update of unit u with the selection read from sel / nsel (every thread of the CTA
