@@ -26,13 +26,15 @@ int attention_tma_supported(const Dims& d) {
   return !d.v_shares_k && d.dk == D && d.dv == D && d.G <= 16 && d.bs % 16 == 0;
 }
 
-// Partial-result slots per unit the TMA path needs (one per CTA segment of a unit).
-int attention_tma_partials(const Dims& d) { return make_plan(d, sm_count()).max_segs; }
+// Partial-result slots per unit the TMA path needs (one per CTA segment of a unit, for each of the
+// two phases of a split launch).
+int attention_tma_partials(const Dims& d) { return 2 * make_plan(d, sm_count()).max_segs; }
 
 cudaError_t launch_attention_tma(const Dims& d, const Layer& L, const CUtensorMap* tmK, const CUtensorMap* tmV,
                                  const __nv_bfloat16* q, const int* sel, const int* slot_of_sel, const int* nsel,
-                                 const int* ctx_len, float* out, cudaStream_t s) {
+                                 const int* ctx_len, float* out, cudaStream_t s, int phase) {
   Plan plan = make_plan(d, sm_count());
+  plan.phase = phase;
   auto go = [&](auto kern, int smem) {
     cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;

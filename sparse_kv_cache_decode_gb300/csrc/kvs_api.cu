@@ -120,7 +120,7 @@ bool fill_dims(const kvs_config* c, Dims* d) {
 // Byte sizes of the per-layer and shared workspace regions.
 struct Plan {
   size_t kpool, vpool, b2s, s2b, stamp, clock, pend_sel, pend_slot, pend_n, sel, nsel, sos, fblk, fslot, nfetch;
-  size_t next_sel, next_slot, next_n, next_commit;
+  size_t next_sel, next_slot, next_n, next_commit, mflag;
   size_t per_layer;
   size_t err, scores, part, ml, done, tk_key, tk_idx, tk_cnt;
   size_t total;
@@ -148,8 +148,9 @@ Plan plan_of(const Dims& d) {
   p.next_slot = align_up(U * d.Kb * 4);
   p.next_n = align_up(U * 4);
   p.next_commit = align_up(U * 4);
+  p.mflag = align_up(U * d.Kb);
   p.per_layer = p.kpool + p.vpool + p.b2s + p.s2b + p.stamp + p.clock + p.pend_sel + p.pend_slot + p.pend_n + p.sel +
-                p.nsel + p.sos + p.fblk + p.fslot + p.nfetch + p.next_sel + p.next_slot + p.next_n + p.next_commit;
+                p.nsel + p.sos + p.fblk + p.fslot + p.nfetch + p.next_sel + p.next_slot + p.next_n + p.next_commit + p.mflag;
   p.err = align_up(16);
   p.scores = 2 * align_up(U * d.nb_max * 4);   // one copy per layer parity
   size_t parts = kAttnSplitMax;
@@ -352,6 +353,7 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
     L.next_slot = reinterpret_cast<int*>(b); b += p.next_slot;
     L.next_n = reinterpret_cast<int*>(b); b += p.next_n;
     L.next_commit = reinterpret_cast<int*>(b); b += p.next_commit;
+    L.miss_flag = reinterpret_cast<uint8_t*>(b); b += p.mflag;
     L.scores = scores + (size_t)(l & 1) * (p.scores / 2 / sizeof(float));   // this layer's parity copy
     L.attn_part = part;
     L.attn_ml = ml;
@@ -727,8 +729,24 @@ kvs_status kvs_decode_step(kvs_ctx* c, int layer, const void* d_q, const void* d
   if (!d.lookahead) {
     if (e == cudaSuccess) e = score(sq, nq);
     if (e == cudaSuccess) e = select(sel, nsel);
-    if (e == cudaSuccess) e = fetch(s);
-    if (e == cudaSuccess) e = attn(sel, L.slot_of_sel, nsel);
+    if (cs == s || !attention_tma_supported(d) || !L.tmK || !L.tmV) {
+      if (e == cudaSuccess) e = fetch(s);
+      if (e == cudaSuccess) e = attn(sel, L.slot_of_sel, nsel);
+      return cuda_status(e);
+    }
+    // with a copy stream: the misses are fetched there while the attention runs over the hits
+    // (their slots are resident), then the attention over the fetched blocks merges both parts
+    if (e == cudaSuccess) e = cudaEventRecord(c->upd_done[layer], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, c->upd_done[layer], 0);
+    if (e == cudaSuccess) e = fetch(cs);
+    if (e == cudaSuccess) e = cudaEventRecord(c->fetch_done[layer], cs);
+    for (int phase = 1; phase <= 2 && e == cudaSuccess; ++phase) {
+      if (phase == 2) e = cudaStreamWaitEvent(s, c->fetch_done[layer], 0);
+      if (e == cudaSuccess)
+        e = timed(c, KVS_K_ATTN, s, 1, [&] {
+          return launch_attention_tma(d, L, L.tmK, L.tmV, q, sel, L.slot_of_sel, nsel, d_ctx_len, d_out, s, phase);
+        });
+    }
     return cuda_status(e);
   }
   // no selection yet (the layer's first lookahead step): pick S_t from the current query and make

@@ -91,8 +91,11 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   return d;
 }
 
+// phase: 0 every selected position, partials merged; 1 only the positions that hit in the last
+// update (miss_flag 0), partials kept; 2 only the positions that missed, then the unit's partials
+// of both phases merged.  Phases 1 and 2 use the same split (their partials side by side).
 struct Plan {
-  int n_cta, per_cta, max_segs;
+  int n_cta, per_cta, max_segs, phase;
 };
 
 // The split of the layer's (unit, block) positions over `ctas` CTAs (fewer when the caps bind).
@@ -110,6 +113,7 @@ __host__ __device__ inline Plan make_plan_ctas(const Dims& d, int ctas) {
   if ((long long)p.per_cta > (long long)(kMaxUnits - 2) * d.Kb) p.per_cta = (kMaxUnits - 2) * d.Kb;
   p.n_cta = (int)((positions + p.per_cta - 1) / p.per_cta);
   p.max_segs = (d.Kb + p.per_cta - 1) / p.per_cta + 1;
+  p.phase = 0;
   return p;
 }
 
@@ -167,8 +171,11 @@ __device__ __forceinline__ void attn_tma_cta(const CUtensorMap& tmK, const CUten
     u_len[j] = ctx_len[(u_first + j) / d.Hkv];
     u_n[j] = nsel[u_first + j];
   }
+  constexpr int kOtherPhase = -0x40000000;   // a position of the other phase: skipped, no error
   for (int i = tid; i < (int)(p1 - p0); i += blockDim.x) {
-    m_blk[i] = sel[p0 + i];
+    int b = sel[p0 + i];
+    if (plan.phase != 0 && ((plan.phase == 1) == (L.miss_flag[p0 + i] != 0))) b = kOtherPhase;
+    m_blk[i] = b;
     m_slot[i] = slot_of_sel[p0 + i];
   }
   __syncthreads();
@@ -181,7 +188,7 @@ __device__ __forceinline__ void attn_tma_cta(const CUtensorMap& tmK, const CUten
     const bool unit_ok = len >= 0 && len <= d.max_ctx && n >= 0 && n <= d.Kb;
     if (!unit_ok && ii == 0) set_error(L.err, KVS_ERR_BAD_INDEX);
     int blk = -1;
-    if (unit_ok && ii < n) {
+    if (unit_ok && ii < n && m_blk[i] != kOtherPhase) {
       blk = m_blk[i];
       const int slot = m_slot[i];
       if (blk < 0 || blk >= n_blocks_of(len, d.bs) || slot < 0 || slot >= d.C) {
@@ -245,7 +252,8 @@ __device__ __forceinline__ void attn_tma_cta(const CUtensorMap& tmK, const CUten
   // warp order: O = sum_w 2^(m_w - M) O_w, l = sum_w 2^(m_w - M) l_w, M = max_w m_w
   auto combine = [&](int u, int slot) {
     const int c0 = (int)(((long long)u * d.Kb) / plan.per_cta);
-    const size_t pidx = (size_t)u * plan.max_segs + (size_t)(c - c0);
+    const size_t pidx = (size_t)u * plan.max_segs * (plan.phase ? 2 : 1) + (plan.phase == 2 ? plan.max_segs : 0) +
+                        (size_t)(c - c0);
     const float* sw = cmb + slot * kConsumers * G * D;
     const float* sml = cmb_ml + slot * kConsumers * H8 * 2;
     for (int e = tid; e < G * (D / 4); e += kConsumers * 32) {
@@ -457,6 +465,10 @@ __device__ __forceinline__ void attn_tma_cta(const CUtensorMap& tmK, const CUten
   // 4 columns per lane.  The counter goes back to 0 for the next launch.
   named_bar_sync(1, kConsumers * 32);
   for (int u = u_first + n_imm; u <= u_last; ++u) combine(u, u - u_first - n_imm);
+  if (plan.phase == 1) {   // the partials wait for the second phase's merge
+    if (!ok) set_error(L.err, KVS_ERR_TIMEOUT);
+    return;
+  }
   __threadfence();
   named_bar_sync(1, kConsumers * 32);
   for (int j = tid; j <= u_last - u_first; j += kConsumers * 32) {
@@ -474,21 +486,23 @@ __device__ __forceinline__ void attn_tma_cta(const CUtensorMap& tmK, const CUten
     const int c0 = (int)(((long long)u * d.Kb) / plan.per_cta);
     const int c1 = min(plan.n_cta - 1, (int)(((long long)(u + 1) * d.Kb - 1) / plan.per_cta));
     const int np = c1 - c0 + 1;
-    const size_t base = (size_t)u * plan.max_segs;
+    const size_t base = (size_t)u * plan.max_segs * (plan.phase ? 2 : 1);
+    const int np_all = plan.phase == 2 ? 2 * np : np;   // with the first phase's partials
+    auto pix = [&](int p) { return base + (size_t)(p < np ? p : plan.max_segs + (p - np)); };
     const int r_out = u / d.Hkv, h_out = u % d.Hkv;
     for (int g = warp; g < G; g += kConsumers) {
       // chunks of kMergeChunk partials, each read in one round of loads (the (max, sum) pairs and the rows
       // together), merged online: the running state is rescaled when a chunk raises the max
       float M = -INFINITY, lpart = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int q0 = 0; q0 < np; q0 += kMergeChunk) {
-        const int nj = min(kMergeChunk, np - q0);
+      for (int q0 = 0; q0 < np_all; q0 += kMergeChunk) {
+        const int nj = min(kMergeChunk, np_all - q0);
         float2 ml = make_float2(-INFINITY, 0.f);
-        if (lane < nj) ml = __ldcg(reinterpret_cast<const float2*>(L.attn_ml + ((base + q0 + lane) * G + g) * 2));
+        if (lane < nj) ml = __ldcg(reinterpret_cast<const float2*>(L.attn_ml + (pix(q0 + lane) * G + g) * 2));
         float4 x[kMergeChunk];
 #pragma unroll
         for (int kq = 0; kq < kMergeChunk; ++kq)
-          x[kq] = kq < nj ? __ldcg(reinterpret_cast<const float4*>(L.attn_part + ((base + q0 + kq) * G + g) * D) + lane)
+          x[kq] = kq < nj ? __ldcg(reinterpret_cast<const float4*>(L.attn_part + (pix(q0 + kq) * G + g) * D) + lane)
                           : make_float4(0.f, 0.f, 0.f, 0.f);
         float mc = ml.x;
 #pragma unroll

@@ -57,6 +57,7 @@ struct Layer {
   float* attn_part;      // [U][n_split_max][Hq/Hkv][dv] partial outputs
   float* attn_ml;        // [U][n_split_max][Hq/Hkv][2] partial (max, sum)
   unsigned* unit_done;   // [U] CTAs finished per unit in the current attention launch (0 between launches)
+  uint8_t* miss_flag;    // [U][Kb] selected position i was a miss in the last update (fetched, not resident)
   unsigned* score_done;  // [U] scoring CTAs finished per unit in the current layer-kernel launch (0 between launches)
   const __nv_bfloat16* host_k;  // device-mapped host history of this layer [B][Hkv][max_ctx][dk]
   const __nv_bfloat16* host_v;  // [B][Hkv][max_ctx][dv] or nullptr
@@ -198,9 +199,11 @@ cudaError_t launch_score_tc(const Dims& d, const __nv_bfloat16* index, const __n
                             const int* ctx_len, float* scores, unsigned* err, cudaStream_t s);
 int attention_tma_supported(const Dims& d);
 int attention_tma_partials(const Dims& d);
+// phase: 0 all selected positions; 1 the positions that hit in the layer's last update, partials
+// kept; 2 those that missed, then every partial merged (1 and 2 in that order on one stream).
 cudaError_t launch_attention_tma(const Dims& d, const Layer& L, const CUtensorMap* tmK, const CUtensorMap* tmV,
                                  const __nv_bfloat16* q, const int* sel, const int* slot_of_sel, const int* nsel,
-                                 const int* ctx_len, float* out, cudaStream_t s);
+                                 const int* ctx_len, float* out, cudaStream_t s, int phase = 0);
 int attention_split(const Dims& d, int* n_split, int* blocks_per_split);
 int score_supported(const Dims& d);
 

@@ -129,8 +129,11 @@ constexpr int kRankVictimsMaxC = 1024;
 // Shared memory of the update: the CacheSmem arrays, then the staged selection and pending
 // slots [Kb] each, the victims' (key, slot) words [C], and the staged block -> slot map.
 __host__ __device__ inline size_t update_extra_offset(const Dims& d) { return (cache_smem_bytes(d) + 15) / 16 * 16; }
-__host__ __device__ inline size_t update_smem_bytes(const Dims& d) {
+__host__ __device__ inline size_t update_missf_offset(const Dims& d) {
   return update_extra_offset(d) + (size_t)d.Kb * 8 + (size_t)d.C * 8 + (update_stages_b2s(d) ? (size_t)d.nb_max * 4 : 0);
+}
+__host__ __device__ inline size_t update_smem_bytes(const Dims& d) {
+  return update_missf_offset(d) + ((size_t)d.Kb + 15) / 16 * 16;   // + the per-position miss flags
 }
 
 // Inputs of the update that do not depend on the selection (per-thread copies of the scalars).
@@ -191,6 +194,7 @@ __device__ inline void update_run(const Dims& d, const Layer& L, int u, const Up
   int* ps_s = su_s + d.Kb;                                             // [Kb] the pending slots
   unsigned long long* ck = reinterpret_cast<unsigned long long*>(ps_s + d.Kb);   // [C] victim (key, slot)
   int* b2s_s = update_stages_b2s(d) ? reinterpret_cast<int*>(ck + d.C) : nullptr;   // [nb_max]
+  uint8_t* mf_s = smraw + update_missf_offset(d);                      // [Kb] position i missed
   const int tid = threadIdx.x, NT = blockDim.x;
   int* b2s = L.block2slot + (size_t)u * d.nb_max;
   int* s2b = L.slot2block + (size_t)u * d.C;
@@ -221,10 +225,12 @@ __device__ inline void update_run(const Dims& d, const Layer& L, int u, const Up
     if (s >= d.C) { s_bad = 1; continue; }
     if (s >= 0) {
       sm.flags[s] = 1;
+      mf_s[i] = 0;
       sm.sos[i] = s;
       my_pfh += sm.st[s] == now - 1u;
     } else {
       ++my_miss;
+      mf_s[i] = 1;
     }
   }
   __syncthreads();
@@ -332,6 +338,7 @@ __device__ inline void update_run(const Dims& d, const Layer& L, int u, const Up
     int s = sm.sos[i];
     st[s] = now;
     slot_of_sel[(size_t)u * d.Kb + i] = s;
+    L.miss_flag[(size_t)u * d.Kb + i] = mf_s[i];
     if (d.lookahead) {   // staged; the fetch that follows commits it to pend_*
       L.next_sel[(size_t)u * d.Kb + i] = su_s[i];
       L.next_slot[(size_t)u * d.Kb + i] = s;

@@ -1,7 +1,8 @@
 """GPU parity at the workloads' full sizes, in the launch configuration bench.py times.
 
 Each test binds the whole host history and runs the fused step for a few steps (lookahead with
-the fetch on a side stream for the 8B case, append for the 128K case, prefetch for the MLA case).
+the fetch on a side stream for the 8B case, append with the fetch on a side stream beside the
+attention over the hits for the 128K case, prefetch for the MLA case).
 The oracle recomputes one sampled request in full (every layer and kv head) step by step; for
 every unit the size-independent properties are checked: selection count, order, range and forced
 blocks, and the bytes of resident slots against the host history."""
@@ -73,7 +74,7 @@ def test_llama8b_32k_lookahead_full():
 
 
 def test_llama8b_128k_append_full():
-    _run(W.LONG_128K.with_(steps=8), steps=3)
+    _run(W.LONG_128K.with_(steps=8), steps=3, copy_stream=True)
 
 
 def test_mla_128k_token_topk_full():
@@ -82,3 +83,13 @@ def test_mla_128k_token_topk_full():
 
 def test_sweep_bs16_budget2048_full():
     _run(W.sweep_workload(16, 2048, 0.9), steps=2)
+
+
+def test_sweep_bs64_budget2048_full():
+    # block 64: four 16-row sub-tiles per block in the attention kernel
+    _run(W.sweep_workload(64, 2048, 0.9, n_layer=4), steps=2)
+
+
+def test_sweep_bs16_budget4096_full():
+    # K_b 256, cache 320 slots: the largest budget of the sweep
+    _run(W.sweep_workload(16, 4096, 0.9, n_layer=4), steps=2)

@@ -42,6 +42,17 @@ INT_CASES = [
                          v_scale=2.0), [4096, 1000], False),
     (W.TINY_LOOKAHEAD.with_(name="tiny_la_fp8_int_cs", n_req=2, int_scale=2.0, int_clip=4.0, kv_dtype="fp8"),
      [4096, 2050], True),
+    # sync steps with a copy stream: the attention over the hits runs while the misses are fetched,
+    # then the attention over the fetched blocks merges both parts
+    (W.TINY.with_(name="tiny_int_cs", n_req=2, int_scale=2.0), [4096, 3001], True),
+    (W.TINY_APPEND.with_(name="tiny_app_int_cs", n_req=2, int_scale=2.0), [4096, 1000], True),
+    (W.TINY.with_(name="tiny_bs64_int_cs", n_req=2, block_size=64, ctx0=4000, budget_blocks=8, cap_blocks=10,
+                  int_scale=2.0), [4000, 3900], True),
+    (W.TINY.with_(name="tiny_imp_int_cs", n_req=2, int_scale=2.0, evict_policy="importance"), [4096, 3001], True),
+    (W.TINY_APPEND.with_(name="tiny_app_bound_int_cs", n_req=2, int_scale=2.0, score_mode="bound"), [4096, 1000],
+     True),
+    (W.TINY_APPEND.with_(name="tiny_app_fp8_int_cs", n_req=2, int_scale=2.0, int_clip=4.0, kv_dtype="fp8",
+                         k_scale=0.5, v_scale=2.0), [4096, 1000], True),
 ]
 
 
