@@ -314,7 +314,9 @@ def dependency_bound_ms(w, per_layer, link_per_layer, hbm_peak, link_peak):
 
 # ----------------------------------------------------------------------------- ncu traffic
 
-KERNEL_SOURCES = {"attn": ["k_attn_tma.cu", "kvs_attn_tma.cuh", "k_attn.cu"],
+# the sources that define each timed kernel ("attn": the TMA-fed GQA attention kernel that the
+# committed traffic figures were taken from)
+KERNEL_SOURCES = {"attn": ["k_attn_tma.cu", "kvs_attn_tma.cuh"],
                   "score": ["k_score.cu", "kvs_score.cuh", "k_score_tc.cu"],
                   "fetch": ["k_cache.cu"]}
 

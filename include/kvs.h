@@ -207,8 +207,9 @@ kvs_status kvs_cache_restore(kvs_ctx* ctx, int layer, const void* d_snapshot, co
  * out[r][g] = sum_t softmax_t(scale * q[r][g] . k_t) v_t over the tokens t < ctx_len[r] of the
  * blocks sel[r][h] (h = g / G), read from their slots; fp32 accumulation, fp32 output.
  * Shapes: d_k = d_v = 128 with G <= 16 (TMA-fed kernel when block_size is a multiple of 16), or
- * MLA (v_shares_k, d_k 576, d_v <= 512, a multiple of 128) with G <= 16 or G = 128 (heads in
- * groups of 32 when d_v = 512); others KVS_ERR_NOT_SUPPORTED. */
+ * MLA (v_shares_k, d_k 576, d_v <= 512, a multiple of 128) with G <= 16, G = 128, or (d_v = 512)
+ * G = 32, 64 or 96.  bf16 MLA with G = 128 and d_v = 512 runs on the tensor cores (tcgen05: S, O
+ * and P in tensor memory); the other MLA shapes on mma.sync tiles.  Others KVS_ERR_NOT_SUPPORTED. */
 kvs_status kvs_sparse_decode_attn(kvs_ctx* ctx, int layer, const void* d_q, const int* d_sel,
                                   const int* d_slot_of_sel, const int* d_nsel, const int* d_ctx_len,
                                   float* d_out, kvs_stream_t stream);

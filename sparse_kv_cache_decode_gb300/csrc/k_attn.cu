@@ -593,6 +593,12 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(Dims d, Layer L, floa
 }
 
 }  // namespace
+
+cudaError_t launch_attn_combine(const Dims& d, const Layer& L, float* out, int n_split, cudaStream_t s) {
+  launch_pdl(attn_combine_kernel, dim3(dim3(d.U, d.G)), dim3(128), 0, s, d, L, out, n_split);
+  return cudaGetLastError();
+}
+
 int attention_split(const Dims& d, int* n_split_out, int* bps_out);
 namespace {
 
@@ -669,7 +675,7 @@ int attention_split(const Dims& d, int* n_split_out, int* bps_out) {
 int attention_supported(const Dims& d) {
   if (d.fp8) return attention_tma_supported(d);   // E4M3 tiles: the TMA kernel only
   if (d.dv % kDVC) return 0;
-  if (d.v_shares_k) return d.dk == 576 && d.dv <= 512 && (d.G <= 16 || d.G == 128);
+  if (d.v_shares_k) return d.dk == 576 && d.dv <= 512 && (d.G <= 16 || (mla_path(d) && d.G <= 128) || d.G == 128);
   return d.dk == 128 && d.dv == 128 && d.G <= 16;
 }
 
@@ -682,6 +688,7 @@ cudaError_t launch_attention(const Dims& d, const Layer& L, const __nv_bfloat16*
   if (d.fp8) return cudaErrorInvalidValue;
   if (d.v_shares_k) {
     if (d.G <= 16) return launch_attn_t<576, 1, true>(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, s);
+    if (attention_mla_tc_supported(d)) return launch_attention_mla_tc(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, s);
     if (mla_path(d)) return launch_attn_mla(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, s);
     return launch_attn_t<576, 8, true>(d, L, q, sel, slot_of_sel, nsel, ctx_len, out, s);
   }

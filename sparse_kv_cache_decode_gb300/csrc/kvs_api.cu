@@ -234,9 +234,9 @@ cudaError_t timed(kvs_ctx* c, int kernel, cudaStream_t s, int n_kernels, F&& lau
 }
 
 int attn_kernels(const Dims& d) {
-  // attention kernel (the TMA path merges its partials in-kernel), plus the split combine of the
-  // cp.async paths when the selection is split across CTAs
-  if (attention_tma_supported(d)) return 1;
+  // attention kernel (the TMA and tensor-memory MLA paths merge their partials in-kernel), plus the
+  // split combine of the cp.async paths when the selection is split across CTAs
+  if (attention_tma_supported(d) || attention_mla_tc_supported(d)) return 1;
   int n_split = 1, bps = 0;
   if (!attention_split(d, &n_split, &bps)) return 1;
   return n_split > 1 ? 2 : 1;

@@ -65,7 +65,9 @@ def test_cache_update_refuses_bad_selection(bad):
 
 
 @pytest.mark.parametrize("w", [W.TINY.with_(name="err_attn_tma", n_req=2),
-                               W.TINY_MLA.with_(name="err_attn_mla", n_req=2)], ids=["tma", "cp_async"])
+                               W.TINY_MLA.with_(name="err_attn_mla", n_req=2),
+                               W.MLA_128K.with_(name="err_attn_mla_tc", n_req=2, n_layer=1, ctx0=2048, budget_blocks=256,
+                                                cap_blocks=384, n_heavy=20)], ids=["tma", "cp_async", "tcgen05"])
 @pytest.mark.parametrize("bad", ["slot_past_end", "slot_negative", "block_past_end", "count"])
 def test_attention_refuses_bad_indices(w, bad):
     g = GpuCase(w, [w.ctx0, w.ctx0 - 77])

@@ -18,6 +18,10 @@ torch = pytest.importorskip("torch")
 
 MLA_G128 = W.MLA_128K.with_(name="mla_g128_small", n_req=2, n_layer=1, ctx0=2048, steps=4, budget_blocks=256,
                             cap_blocks=384, n_heavy=20)
+# 64 heads per latent row: the mma.sync MLA kernel; 128 heads: the tcgen05 kernel, here with 8 units
+# so that each CTA runs 8 tiles of 32 tokens (the stage ring wraps; ragged last tile)
+MLA_G64 = MLA_G128.with_(name="mla_g64_small", n_q_head=64)
+MLA_G128_B8 = MLA_G128.with_(name="mla_g128_b8", n_req=8, ctx0=4096, budget_blocks=2048, cap_blocks=2304, n_heavy=40)
 TINY3 = W.TINY.with_(name="tiny3", n_req=3)
 TINY_G8 = W.TINY.with_(name="tiny_g8", n_req=2, n_q_head=16, n_kv_head=2)
 TINY_BS64 = W.TINY.with_(name="tiny_bs64", n_req=2, block_size=64, ctx0=3000, budget_blocks=8, cap_blocks=12)
@@ -311,7 +315,9 @@ def test_layer_prefetch_sequences_bit_exact():
 
 
 @pytest.mark.parametrize("w,lens", [(TINY3, [4096, 1000, 17]), (TINY_G8, [4096, 3001]), (TINY_BS64, [3000, 2999]),
-                                    (W.TINY_MLA, [4096]), (MLA_G128, [2048, 1999]),
+                                    (W.TINY_MLA, [4096]), (MLA_G128, [2048, 1999]), (MLA_G64, [2048, 1999]),
+                                    (MLA_G128.with_(name="mla_g128_ragged", budget_blocks=700, cap_blocks=800), [2048, 777]),
+                                    (MLA_G128_B8, [4096, 4000, 3001, 2048, 2047, 1500, 4096, 3333]),
                                     (W.TINY.with_(name="tiny_bigbudget", n_req=2, budget_blocks=300, cap_blocks=300),
                                      [4096, 4000]),
                                     (TINY3_FP8, [4096, 1000, 17]), (TINY_G8.with_(kv_dtype="fp8", v_scale=2.0), [4096, 3001])])
