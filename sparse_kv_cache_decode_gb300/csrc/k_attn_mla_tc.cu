@@ -9,11 +9,10 @@
 // The 512 value dims do not fit tensor memory beside S, so the two halves of O are two CTAs, each
 // computing S the same way (same inputs, same instruction sequence, so bit-identical).
 //
-// Products of one accumulator run one after another, and a 128 x 32 x 16 product is short, so one
-// chain of 36 products (576 dims) would leave the tensor pipe idle between them: S is summed in 4
-// independent chains (chain c takes the 16-dim steps 4i + c) that the softmax adds.  Q's first 128
-// dims are an A operand in tensor memory, the other 448 in shared memory beside a 3-stage ring of
-// token tiles.  Roles (256 threads):
+// S is double-buffered in tensor memory, so the products of tile j+1 run while the softmax reads
+// tile j, and summed in 2 accumulator chains (even and odd 16-dim steps) that the softmax adds.
+// Q's first 128 dims are an A operand in tensor memory, the other 448 in shared memory beside a
+// 3-stage ring of token tiles.  Roles (256 threads):
 //   warps 0-2  warp w gathers tiles w, w + 3, ... into stage w (the tile's token rows are slot
 //              pool rows, scattered) with 16-byte cp.async as K-major 128-byte-swizzled chunks of
 //              64 dims, so up to three tiles are in flight;
@@ -24,8 +23,10 @@
 //              a tile's max exceeds the reference max by more than 2^8, so every P stays <= 256),
 //              write P, and finally write O.
 // The value tile is read by the PV product as an MN-major operand of the same swizzled storage.
-// With several splits, the last CTA of a (unit, half) to finish merges the splits' partial states
-// (a per-unit completion counter).  Every wait is bounded by the context's timeout
+// With several splits, the splits of a (unit, half) form a thread-block cluster: each CTA sends
+// its O rows and (max, sum) straight from tensor memory to the CTA that owns those heads (its
+// shared memory, through the cluster's distributed shared memory), and each CTA merges its share
+// of the heads and writes them out.  Every wait is bounded by the context's timeout
 // (KVS_ERR_TIMEOUT); tensor memory is always freed.
 #include <algorithm>
 
@@ -40,7 +41,7 @@ constexpr int DK = 576, DV = 512, H = 128;
 constexpr int NTOK = 32;                            // tokens per tile
 constexpr int KC = DK / 64;                         // 64-dim chunks of a row (128 bytes each)
 constexpr int KC_TM = 2;                            // chunks of Q held in tensor memory (dims 0-127)
-constexpr int NCHAIN = 4;                           // independent accumulator chains of S
+constexpr int NCHAIN = 2;                           // accumulator chains of S (even / odd 16-dim steps)
 constexpr int DVZ = DV / 2;                         // value dims per CTA
 constexpr int CHUNK = NTOK * 128;                   // one 64-dim chunk of a tile (4 KiB)
 constexpr int TILE = KC * CHUNK;                    // 36 KiB
@@ -50,6 +51,7 @@ constexpr int STAGES = 3;                           // one per producer warp
 constexpr int MMA_WARP = STAGES;
 constexpr int SOFT0 = STAGES + 1;                   // first softmax warp (its warp index % 4 = TMEM lane quarter)
 constexpr int MAX_TOK = 512;                        // tokens per CTA (their pool rows staged in shared memory)
+constexpr int MAX_SPLIT = 8;                        // CTAs per cluster (portable limit)
 constexpr int SOFT = 128;
 constexpr int THREADS = SOFT0 * 32 + SOFT;
 constexpr int NWARPS = THREADS / 32;
@@ -57,9 +59,11 @@ constexpr int OFF_TILES = QS_BYTES;
 constexpr int OFF_ROWS = OFF_TILES + STAGES * TILE;
 constexpr int OFF_BAR = OFF_ROWS + MAX_TOK * 4;
 constexpr int SMEM = OFF_BAR + 256 + 1024;          // + slack for 1024-byte alignment
-// tensor memory columns: O, S (4 chains), P (2 buffers of hi 16 + lo 16), Q dims 0-127 (bf16 pairs)
+// tensor memory columns: O, S (2 buffers x 2 chains), P (2 buffers of hi 16 + lo 16), Q dims 0-127
+// (bf16 pairs)
 constexpr uint32_t T_O = 0, T_S = 256, T_P = 384, T_Q = 448, TMEM_COLS = 512;
-static_assert(T_S + NCHAIN * NTOK == T_P && T_P + 64 == T_Q && T_Q + KC_TM * 32 == TMEM_COLS, "tensor memory plan");
+constexpr uint32_t S_BUF = NCHAIN * NTOK;           // columns of one S buffer
+static_assert(T_S + 2 * S_BUF == T_P && T_P + 64 == T_Q && T_Q + KC_TM * 32 == TMEM_COLS, "tensor memory plan");
 static_assert(SMEM <= 227 * 1024, "shared memory plan");
 static_assert(SOFT0 % 4 == 0, "softmax warps must cover the four TMEM lane quarters in order");
 constexpr float kMaxGrowth = 8.f;                   // log2 of the largest P before O is rescaled
@@ -80,15 +84,14 @@ __global__ void __launch_bounds__(mtc::THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* full = bars;           // [3] producer warp (32 arrivals)
   uint64_t* empty = bars + 3;      // [3] tcgen05.commit after the tile's PV
-  uint64_t* s_full = bars + 6;     // commit after QK
-  uint64_t* s_free = bars + 7;     // softmax warps (4 arrivals) have read S
-  uint64_t* p_full = bars + 8;     // [2] softmax warps have written P (and rescaled O)
-  uint64_t* pv_done = bars + 10;   // [2] commit after PV
-  uint64_t* drained = bars + 12;
-  uint64_t* q_ready = bars + 13;   // softmax warps (4 arrivals) have placed Q
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* s_full = bars + 6;     // [2] commit after QK
+  uint64_t* s_free = bars + 8;     // [2] softmax warps (4 arrivals) have read S
+  uint64_t* p_full = bars + 10;    // [2] softmax warps have written P (and rescaled O)
+  uint64_t* pv_done = bars + 12;   // [2] commit after PV
+  uint64_t* drained = bars + 14;
+  uint64_t* q_ready = bars + 15;   // softmax warps (4 arrivals) have placed Q
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* last_flag = const_cast<int*>(abort_flag + 1);
 
   const int split = blockIdx.x, u = blockIdx.y, z = blockIdx.z;
   const int r = u / d.Hkv, h = u % d.Hkv;
@@ -111,9 +114,9 @@ __global__ void __launch_bounds__(mtc::THREADS, 1)
       mbar_init(&full[s], 32);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(s_free, SOFT / 32);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], SOFT / 32);
       mbar_init(&p_full[b], SOFT / 32);
       mbar_init(&pv_done[b], 1);
     }
@@ -143,6 +146,8 @@ __global__ void __launch_bounds__(mtc::THREADS, 1)
     set_error(L.err, KVS_ERR_TIMEOUT);
     *abort_flag = 1;
   };
+  float sm_m = -INFINITY, sm_l = 0.f;        // this thread's head state, handed to the merge
+  bool sm_ok = false;
 
   if (warp < STAGES) {
     // ------------------------------------------------------------------ producers: warp w, stage w
@@ -185,22 +190,25 @@ __global__ void __launch_bounds__(mtc::THREADS, 1)
         if (j < T) {
           const int s = j % STAGES;
           if (!mbar_wait(&full[s], (j / STAGES) & 1, timeout_ns)) { fail(); break; }
-          if (j >= 1 && !mbar_wait(s_free, (j - 1) & 1, timeout_ns)) { fail(); break; }
+          const int sb = j & 1;
+          if (j >= 2 && !mbar_wait(&s_free[sb], ((j >> 1) - 1) & 1, timeout_ns)) { fail(); break; }
           tc_fence_after();
           const uint64_t dk0 = smem_desc_sw128(smem_u32(tiles + s * TILE));
+          const uint32_t sacc = tmem + T_S + sb * S_BUF;
 #pragma unroll
           for (int kc = 0; kc < KC; ++kc) {
 #pragma unroll
-            for (int c = 0; c < NCHAIN; ++c) {
-              const uint64_t bdesc = dk0 + (uint64_t)((kc * CHUNK + c * 32) >> 4);
-              const uint32_t acc = tmem + T_S + c * NTOK;
+            for (int k16 = 0; k16 < 4; ++k16) {
+              const uint64_t bdesc = dk0 + (uint64_t)((kc * CHUNK + k16 * 32) >> 4);
+              const uint32_t acc = sacc + (k16 & 1) * NTOK;
+              const uint32_t first = kc == 0 && k16 < NCHAIN;
               if (kc < KC_TM)
-                tc_mma_f16_ts(acc, tmem + T_Q + kc * 32 + c * 8, bdesc, idesc_qk, kc != 0);
+                tc_mma_f16_ts(acc, tmem + T_Q + kc * 32 + k16 * 8, bdesc, idesc_qk, !first);
               else
-                tc_mma_f16(acc, dq0 + (uint64_t)(((kc - KC_TM) * QCHUNK + c * 32) >> 4), bdesc, idesc_qk, kc != 0);
+                tc_mma_f16(acc, dq0 + (uint64_t)(((kc - KC_TM) * QCHUNK + k16 * 32) >> 4), bdesc, idesc_qk, !first);
             }
           }
-          tc_commit(s_full);
+          tc_commit(&s_full[sb]);
         }
         if (j >= 1) {
           const int jj = j - 1, b = jj & 1, s = jj % STAGES;
@@ -276,26 +284,25 @@ __global__ void __launch_bounds__(mtc::THREADS, 1)
     };
     for (int j = 0; j < T && ok; ++j) {
       const int b = j & 1;
-      if (!wait_all_lanes(s_full, j & 1)) { ok = false; break; }
+      // token i of the tile is valid when bit i is set (lane i looks its token up)
+      const int tl = j * NTOK + lane;
+      const unsigned vmask = __ballot_sync(0xffffffffu, tl < ntok && rows[tl] >= 0);
+      if (!wait_all_lanes(&s_full[b], (j >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
       float sv[32];
-      tmem_ld32(trow + T_S, sv);
+      {
+        float s2[2 * NTOK];
+        tmem_ld64(trow + T_S + b * S_BUF, s2);
 #pragma unroll
-      for (int c = 1; c < NCHAIN; ++c) {
-        float sc[32];
-        tmem_ld32(trow + T_S + c * NTOK, sc);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[i] += sc[i];
+        for (int i = 0; i < NTOK; ++i) sv[i] = s2[i] + s2[NTOK + i];
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
+      if (lane == 0) mbar_arrive(&s_free[b]);
       float tmax = -INFINITY;
 #pragma unroll
       for (int i = 0; i < NTOK; ++i) {
-        const int t = j * NTOK + i;
-        const bool valid = t < ntok && rows[t] >= 0;
-        sv[i] = valid ? sv[i] * sl2 : -INFINITY;
+        sv[i] = (vmask >> i) & 1u ? sv[i] * sl2 : -INFINITY;
         tmax = fmaxf(tmax, sv[i]);
       }
       const bool grow = tmax > m + kMaxGrowth || (m == -INFINITY && tmax != -INFINITY);
@@ -339,21 +346,12 @@ __global__ void __launch_bounds__(mtc::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[b]);
     }
-    // the last PV, then O out: normalised (one split) or the split's partial state
+    // the last PV
     if (ok && T > 0 && !wait_all_lanes(&pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1)) ok = false;
-    if (ok) {
-      tc_fence_after();
-      const int g = head;                                    // q head within the unit's group
-      float* dst;
-      float sc = 1.f;
-      if (n_split == 1) {
-        dst = out + ((size_t)r * d.Hq + (size_t)h * d.G + g) * d.dv + z * DVZ;
-        sc = l > 0.f ? 1.f / l : 0.f;
-      } else {
-        dst = L.attn_part + (((size_t)u * n_split + split) * d.G + g) * d.dv + z * DVZ;
-        // both halves write the same (bit-identical) state, so each half's merge reads its own
-        *reinterpret_cast<float2*>(L.attn_ml + (((size_t)u * n_split + split) * d.G + g) * 2) = make_float2(m, l);
-      }
+    tc_fence_after();
+    if (n_split == 1 && ok) {
+      const float sc = l > 0.f ? 1.f / l : 0.f;
+      float* dst = out + ((size_t)r * d.Hq + (size_t)h * d.G + head) * d.dv + z * DVZ;
 #pragma unroll 1
       for (int c0 = 0; c0 < DVZ; c0 += 32) {
         float ov[32];
@@ -368,94 +366,88 @@ __global__ void __launch_bounds__(mtc::THREADS, 1)
           *reinterpret_cast<float4*>(dst + c0 + i) = make_float4(ov[i] * sc, ov[i + 1] * sc, ov[i + 2] * sc, ov[i + 3] * sc);
       }
     }
-    __threadfence();                        // the partial state is visible before the CTA is counted
+    if (!ok) {                                // reported; the partial state sent below is empty
+      m = -INFINITY;
+      l = 0.f;
+    }
+    sm_m = m;
+    sm_l = l;
+    sm_ok = ok && T > 0;
+  }
+  if (n_split > 1) {
+    // ---------------------------------------------------------------- merge over the cluster
+    // head g belongs to cluster rank g * n / 128; each rank's heads arrive in its shared memory
+    // (the Q and ring area, free once every CTA of the cluster has left its main loop) as
+    // [source rank][head - first head][256] floats and [source rank][head - first head] (max, sum)
+    const uint32_t me = cluster_ctarank();
+    const int rows_max = (H + n_split - 1) / n_split;
+    float* oslots = reinterpret_cast<float*>(smem);
+    float2* mlslots = reinterpret_cast<float2*>(smem + (size_t)n_split * rows_max * DVZ * 4);
+    float* wts = reinterpret_cast<float*>(mlslots + n_split * rows_max);
+    __syncwarp();
+    cluster_sync();
+    if (warp >= SOFT0) {
+      const int head = (warp & 3) * 32 + lane;
+      const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+      const int owner = head * n_split / H;
+      const int first = (owner * H + n_split - 1) / n_split;
+      const int row = (int)me * rows_max + (head - first);
+      const uint32_t ro = mapa_shared(smem_u32(oslots + (size_t)row * DVZ), (uint32_t)owner);
+#pragma unroll 1
+      for (int c0 = 0; c0 < DVZ; c0 += 32) {
+        float ov[32];
+        if (sm_ok) {
+          tmem_ld32(trow + T_O + c0, ov);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) st_cluster_f4(ro + (c0 + i) * 4, ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
+      }
+      st_cluster_f2(mapa_shared(smem_u32(mlslots + row), (uint32_t)owner), sm_m, sm_l);
+    }
+    cluster_sync();
+    const int first = ((int)me * H + n_split - 1) / n_split;
+    const int cnt = (((int)me + 1) * H + n_split - 1) / n_split - first;
+    // weights 2^(m_k - M) / sum_k 2^(m_k - M) l_k of each source rank k, per head of this rank
+    if (tid < cnt) {
+      float M = -INFINITY;
+      for (int k = 0; k < n_split; ++k) M = fmaxf(M, mlslots[k * rows_max + tid].x);
+      float lsum = 0.f;
+      for (int k = 0; k < n_split; ++k) {
+        const float2 v = mlslots[k * rows_max + tid];
+        if (v.x != -INFINITY) lsum += exp2f(v.x - M) * v.y;
+      }
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      for (int k = 0; k < n_split; ++k) {
+        const float mk = mlslots[k * rows_max + tid].x;
+        wts[k * rows_max + tid] = mk == -INFINITY ? 0.f : exp2f(mk - M) * inv;
+      }
+    }
+    __syncthreads();
+    constexpr int F4 = DVZ / 4;
+    const float4* os4 = reinterpret_cast<const float4*>(oslots);
+    float4* outv = reinterpret_cast<float4*>(out + ((size_t)r * d.Hq + (size_t)h * d.G + first) * d.dv + z * DVZ);
+    for (int i = tid; i < cnt * F4; i += THREADS) {
+      const int g = i / F4, c4 = i - g * F4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < n_split; ++k) {
+        const float w = wts[k * rows_max + g];
+        const float4 x = os4[(size_t)(k * rows_max + g) * F4 + c4];
+        acc.x += w * x.x;
+        acc.y += w * x.y;
+        acc.z += w * x.z;
+        acc.w += w * x.w;
+      }
+      outv[(size_t)g * (d.dv / 4) + c4] = acc;
+    }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
-  }
-  if (n_split == 1) return;
-  // ---------------------------------------------------------------- merge of the splits (last CTA)
-  // counter: low 16 bits count the finished CTAs of half 0, high 16 bits those of half 1
-  if (tid == 0) {
-    __threadfence();
-    const unsigned one = z == 0 ? 1u : 65536u;
-    const unsigned prev = atomicAdd(&L.unit_done[u], one);
-    const unsigned mine = z == 0 ? (prev & 0xffffu) : (prev >> 16);
-    *last_flag = mine == (unsigned)(n_split - 1);
-    if (*last_flag) {
-      atomicSub(&L.unit_done[u], one * (unsigned)n_split);   // 0 again for the next launch
-      __threadfence();
-    }
-  }
-  __syncthreads();
-  if (!*last_flag) return;
-  // the splits' (max, sum) -> per-split weights 2^(m_s - M) / sum_s 2^(m_s - M) l_s in shared
-  // memory (the tile ring is free now), then every output float4 of the half as a weighted sum of
-  // the splits' partial rows, sixteen loads in flight per thread
-  float2* mls = reinterpret_cast<float2*>(tiles);                     // [n_split][128]
-  float* wts = reinterpret_cast<float*>(tiles + (size_t)kAttnSplitMax * H * sizeof(float2));
-  const float2* pml = reinterpret_cast<const float2*>(L.attn_ml) + (size_t)u * n_split * d.G;
-  for (int i = tid; i < n_split * H; i += THREADS) mls[i] = __ldcg(pml + i);
-  __syncthreads();
-  if (tid < H) {
-    float M = -INFINITY;
-    for (int s = 0; s < n_split; ++s) M = fmaxf(M, mls[s * H + tid].x);
-    float lsum = 0.f;
-    for (int s = 0; s < n_split; ++s) {
-      const float2 v = mls[s * H + tid];
-      if (v.x != -INFINITY) lsum += exp2f(v.x - M) * v.y;
-    }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    for (int s = 0; s < n_split; ++s) {
-      const float ms = mls[s * H + tid].x;
-      wts[s * H + tid] = ms == -INFINITY ? 0.f : exp2f(ms - M) * inv;
-    }
-  }
-  __syncthreads();
-  constexpr int F4 = DVZ / 4;                                         // float4 per head row half
-  constexpr int ITEMS = H * F4;
-  const float4* part = reinterpret_cast<const float4*>(L.attn_part + (size_t)u * n_split * d.G * d.dv + z * DVZ);
-  float4* outv = reinterpret_cast<float4*>(out + ((size_t)r * d.Hq + (size_t)h * d.G) * d.dv + z * DVZ);
-  const size_t split_f4 = (size_t)d.G * d.dv / 4, row_f4 = d.dv / 4;
-  for (int base = tid; base < ITEMS; base += 4 * THREADS) {
-    int gi[4], ci[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = min(base + k * THREADS, ITEMS - 1);
-      gi[k] = i / F4;
-      ci[k] = i - gi[k] * F4;
-    }
-    float4 acc[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < n_split; s0 += 4) {
-      float4 x[4][4];
-#pragma unroll
-      for (int ss = 0; ss < 4; ++ss) {
-        const int s = min(s0 + ss, n_split - 1);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) x[ss][k] = __ldcg(part + s * split_f4 + gi[k] * row_f4 + ci[k]);
-      }
-#pragma unroll
-      for (int ss = 0; ss < 4; ++ss) {
-        if (s0 + ss < n_split) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float w = wts[(s0 + ss) * H + gi[k]];
-            acc[k].x += w * x[ss][k].x;
-            acc[k].y += w * x[ss][k].y;
-            acc[k].z += w * x[ss][k].z;
-            acc[k].w += w * x[ss][k].w;
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (base + k * THREADS < ITEMS) outv[gi[k] * row_f4 + ci[k]] = acc[k];
   }
 }
 
@@ -470,11 +462,11 @@ int attention_mla_tc_split(const Dims& d, int* n_split_out, int* bps_out) {
   // tiles of tokens per CTA
   const int fill = device_sm_count() / (2 * d.U);
   const int tiles = (d.Kb * d.bs + mtc::NTOK - 1) / mtc::NTOK;
-  int n = std::max(n_min, std::min(fill, tiles / 2));
+  int n = std::max(n_min, std::min(std::min(fill, tiles / 2), mtc::MAX_SPLIT));
   n = std::max(n, 1);
   int bps = (d.Kb + n - 1) / n;
   n = (d.Kb + bps - 1) / bps;
-  if (n > kAttnSplitMax) return 0;
+  if (n > mtc::MAX_SPLIT) return 0;
   *n_split_out = n;
   *bps_out = bps;
   return 1;
@@ -492,8 +484,12 @@ cudaError_t launch_attention_mla_tc(const Dims& d, const Layer& L, const __nv_bf
   if (!attention_mla_tc_split(d, &n_split, &bps)) return cudaErrorInvalidValue;
   cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(attn_mla_tc_kernel), mtc::SMEM);
   if (e != cudaSuccess) return e;
-  launch_pdl(attn_mla_tc_kernel, dim3(n_split, d.U, 2), dim3(mtc::THREADS), mtc::SMEM, s, d, L, q, sel, slot_of_sel,
-             nsel, ctx_len, out, n_split, bps);
+  if (n_split == 1)
+    launch_pdl(attn_mla_tc_kernel, dim3(1, d.U, 2), dim3(mtc::THREADS), mtc::SMEM, s, d, L, q, sel, slot_of_sel, nsel,
+               ctx_len, out, n_split, bps);
+  else
+    launch_pdl_cluster(attn_mla_tc_kernel, dim3(n_split, d.U, 2), dim3(mtc::THREADS), mtc::SMEM, s, (unsigned)n_split, d,
+                       L, q, sel, slot_of_sel, nsel, ctx_len, out, n_split, bps);
   return cudaGetLastError();
 }
 
