@@ -256,10 +256,22 @@ def link_peaks(K, host_tensors):
                 best, shape = gbs, f"{ctas}x{threads}"
         out[name] = best
         out[name + "_grid"] = shape
+    # bursts of the size a layer's fetch moves: time = fixed latency + bytes / streaming rate
+    bursts = []
+    for nit in (278, 490, 2000, 65536):
+        offs = rnd[:nit] if nit <= rnd.numel() else rnd
+        ms = _time_ms(lambda: K.probe_host_read(hist, region, offs, item, 152, 128, sink))
+        bursts.append((offs.numel() * item, ms * 1e3))
+    x = np.array([b for b, _ in bursts], dtype=np.float64)
+    y = np.array([t for _, t in bursts], dtype=np.float64)
+    slope, icpt = np.polyfit(x, y, 1)
+    out["bursts"] = [{"mb": round(b / 1e6, 2), "us": round(t, 1), "gbs": round(b / (t * 1e-6) / 1e9, 1)} for b, t in bursts]
+    out["burst_fixed_us"] = round(float(icpt), 1)
+    out["burst_stream_gbs"] = round(float(1e-3 / slope), 1)
     torch.cuda.synchronize()
     if int(sink[1].item()) != 0:
         raise RuntimeError("link probe skipped items")
-    vals = {k: v for k, v in out.items() if not k.endswith("_grid")}
+    vals = {k: v for k, v in out.items() if k in ("ce_pinned", "ce_history", "sm_seq", "sm_rand")}
     best_key = max(vals, key=vals.get)
     res = {k: (round(v, 1) if isinstance(v, float) else v) for k, v in out.items()}
     res["peak_gbs"] = round(vals[best_key], 1)

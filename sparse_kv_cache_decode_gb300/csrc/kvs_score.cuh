@@ -52,19 +52,6 @@ __device__ inline void score_cta(const Dims& d, const __nv_bfloat16* __restrict_
   if (tile0 >= tile1) return;
   const int R = nq * d.G;
 
-  // scoring rows -> smem (zero rows beyond R)
-  unsigned char* qs = smem;
-  for (int i = threadIdx.x; i < NP * 8 * CH; i += blockDim.x) {
-    int row = i / CH, ch = i % CH;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < R) {
-      int j = row / d.G, g = row % d.G;
-      v = score_row_chunk(q + (((size_t)r * nq + j) * d.Hq + h * d.G + g) * d.dk, ch, d);
-    }
-    *reinterpret_cast<uint4*>(qs + row * RS + ch * 16) = v;
-  }
-  __syncthreads();
-
   constexpr int ST = score_stages<DK>();
   unsigned char* buf = smem + NP * 8 * RS + (size_t)warp * ST * 16 * RS;
   const __nv_bfloat16* ik = index + (size_t)u * d.nb_max * DK;
@@ -81,7 +68,8 @@ __device__ inline void score_cta(const Dims& d, const __nv_bfloat16* __restrict_
   };
 
   // ring of ST stages: tiles my, my + nwarps, ... ; ST - 1 loads stay in flight ahead of the one
-  // being computed (an empty group is committed past the end so the wait count stays fixed)
+  // being computed (an empty group is committed past the end so the wait count stays fixed).  The
+  // first loads are issued before the scoring rows are staged, so that their latency overlaps it.
   const int first = tile0 + warp;
 #pragma unroll
   for (int i = 0; i < ST - 1; ++i) {
@@ -89,6 +77,18 @@ __device__ inline void score_cta(const Dims& d, const __nv_bfloat16* __restrict_
     if (t < tile1) load_tile(t, i);
     else cp_async_commit();
   }
+  // scoring rows -> smem (zero rows beyond R); the ring buffers lie after them
+  unsigned char* qs = smem;
+  for (int i = threadIdx.x; i < NP * 8 * CH; i += blockDim.x) {
+    int row = i / CH, ch = i % CH;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (row < R) {
+      int j = row / d.G, g = row % d.G;
+      v = score_row_chunk(q + (((size_t)r * nq + j) * d.Hq + h * d.G + g) * d.dk, ch, d);
+    }
+    *reinterpret_cast<uint4*>(qs + row * RS + ch * 16) = v;
+  }
+  __syncthreads();
   int stage = 0;
   for (int my = first; my < tile1; my += nwarps, stage = (stage + 1) % ST) {
     const int ahead = my + (ST - 1) * nwarps;
