@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kFetchThreads, SINGLE ? 5 : 1) fetch_kernel(Di
 cudaError_t launch_cache_update(const Dims& d, const Layer& L, const int* sel, const int* nsel, const int* ctx_len,
                                 int* slot_of_sel, const float* scores, kvs_stats* stats, cudaStream_t s) {
   size_t smem = update_smem_bytes(d);
-  if (smem > 48 * 1024) {
+  {   // always, not only above 48 KB: with the kernel's static shared memory the total may pass it
     cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(cache_update_kernel), (int)smem);
     if (e != cudaSuccess) return e;
   }
@@ -369,7 +369,7 @@ int select_update_fusable(const Dims& d) { return d.nb_max <= kTopkSmemKeys; }
 cudaError_t launch_select_update(const Dims& d, const Layer& L, const float* scores, const int* ctx_len, int* sel,
                                  int* nsel, int* slot_of_sel, kvs_stats* stats, cudaStream_t s, int threads) {
   const size_t smem = select_update_smem_bytes(d);
-  if (smem > 48 * 1024) {
+  {   // always, not only above 48 KB: with the kernel's static shared memory the total may pass it
     cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(select_update_kernel), (int)smem);
     if (e != cudaSuccess) return e;
   }
@@ -381,7 +381,7 @@ cudaError_t launch_select_update(const Dims& d, const Layer& L, const float* sco
 cudaError_t launch_prefetch(const Dims& d, const Layer& L, const int* hint, const int* hint_n, const int* ctx_len,
                             kvs_stats* stats, cudaStream_t s) {
   size_t smem = cache_smem_bytes(d);
-  if (smem > 48 * 1024) {
+  {   // always, not only above 48 KB: with the kernel's static shared memory the total may pass it
     cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(prefetch_kernel), (int)smem);
     if (e != cudaSuccess) return e;
   }

@@ -53,6 +53,12 @@ INT_CASES = [
      True),
     (W.TINY_APPEND.with_(name="tiny_app_fp8_int_cs", n_req=2, int_scale=2.0, int_clip=4.0, kv_dtype="fp8",
                          k_scale=0.5, v_scale=2.0), [4096, 1000], True),
+    # the sweep's block size 16 / 2048-token budget unit shape (4096 blocks, K_b 128, C 160): the
+    # fused top-K + update kernel's dynamic shared memory is just under 48 KB there, and with its
+    # static shared memory above it
+    (W.sweep_workload(16, 2048, 0.98, n_layer=1, name="sweep16_2048_int").with_(n_req=2, n_q_head=8, n_kv_head=2,
+                                                                              steps=6, int_scale=2.0),
+     [65536, 60001], True),
 ]
 
 
