@@ -259,7 +259,9 @@ kvs_status kvs_advance_ctx(kvs_ctx* ctx, int* d_ctx_len, kvs_stream_t stream);
 kvs_status kvs_append(kvs_ctx* ctx, int layer, const void* d_k_new, const void* d_v_new, void* d_index,
                       const int* d_ctx_len, kvs_stream_t stream);
 
-/* Copy one layer's cache state to host buffers (synchronous): block2slot [B*H_kv][n_b(max_ctx)],
+/* Copy one layer's cache state to host buffers (synchronous: it waits for all work on the
+ * device, because the context's kernels may be on any of the caller's streams; a diagnostic, not
+ * for the inside of a pipelined step loop): block2slot [B*H_kv][n_b(max_ctx)],
  * slot2block [B*H_kv][C], stamp [B*H_kv][C], clock [B*H_kv]; any pointer may be NULL. */
 kvs_status kvs_cache_export(kvs_ctx* ctx, int layer, int* h_block2slot, int* h_slot2block, unsigned* h_stamp,
                             unsigned* h_clock);
@@ -268,8 +270,9 @@ kvs_status kvs_cache_export(kvs_ctx* ctx, int layer, int* h_block2slot, int* h_s
  * (V NULL when v_shares_k), for inspection. */
 kvs_status kvs_slot_pools(kvs_ctx* ctx, int layer, void** d_k_pool, void** d_v_pool);
 
-/* Read and clear the sticky device status word (synchronous).  *device_status = KVS_OK when no
- * device-side error happened since the last poll. */
+/* Read and clear the sticky device status word (synchronous: it waits for all work on the device,
+ * as the context's kernels may be on any of the caller's streams; poll between steps).
+ * *device_status = KVS_OK when no device-side error happened since the last poll. */
 kvs_status kvs_poll_error(kvs_ctx* ctx, kvs_status* device_status);
 
 /* Kernel timers (diagnostics).  After kvs_kernel_timer_arm(ctx, kernel, capacity), the next
