@@ -593,12 +593,6 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(Dims d, Layer L, floa
 }
 
 }  // namespace
-
-cudaError_t launch_attn_combine(const Dims& d, const Layer& L, float* out, int n_split, cudaStream_t s) {
-  launch_pdl(attn_combine_kernel, dim3(dim3(d.U, d.G)), dim3(128), 0, s, d, L, out, n_split);
-  return cudaGetLastError();
-}
-
 int attention_split(const Dims& d, int* n_split_out, int* bps_out);
 namespace {
 

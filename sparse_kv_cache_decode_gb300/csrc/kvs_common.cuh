@@ -233,8 +233,6 @@ int attention_mla_tc_supported(const Dims& d);
 cudaError_t launch_attention_mla_tc(const Dims& d, const Layer& L, const __nv_bfloat16* q, const int* sel,
                                     const int* slot_of_sel, const int* nsel, const int* ctx_len, float* out,
                                     cudaStream_t s);
-// out[unit][head] = the splits' partial states in attn_part / attn_ml merged and normalised.
-cudaError_t launch_attn_combine(const Dims& d, const Layer& L, float* out, int n_split, cudaStream_t s);
 int score_supported(const Dims& d);
 
 // Raise `kernel`'s dynamic shared-memory limit to at least `bytes` on the current device.  The
