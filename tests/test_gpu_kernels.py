@@ -317,6 +317,12 @@ def test_layer_prefetch_sequences_bit_exact():
 @pytest.mark.parametrize("w,lens", [(TINY3, [4096, 1000, 17]), (TINY_G8, [4096, 3001]), (TINY_BS64, [3000, 2999]),
                                     (W.TINY_MLA, [4096]), (MLA_G128, [2048, 1999]), (MLA_G64, [2048, 1999]),
                                     (MLA_G128.with_(name="mla_g128_ragged", budget_blocks=700, cap_blocks=800), [2048, 777]),
+                                    # one split (output written directly, no cluster) and three splits
+                                    # (a cluster of 3: heads 43 / 43 / 42 per merging CTA)
+                                    (MLA_G128.with_(name="mla_g128_one_split", budget_blocks=64, cap_blocks=128),
+                                     [2048, 1500]),
+                                    (MLA_G128.with_(name="mla_g128_three_splits", budget_blocks=200, cap_blocks=256),
+                                     [2048, 999]),
                                     (MLA_G128_B8, [4096, 4000, 3001, 2048, 2047, 1500, 4096, 3333]),
                                     (W.TINY.with_(name="tiny_bigbudget", n_req=2, budget_blocks=300, cap_blocks=300),
                                      [4096, 4000]),
