@@ -21,7 +21,7 @@
 //   warps 4-7  load Q (while the first tiles arrive), then one thread per head: read its S row,
 //              update its running max with lazy rescaling (O is rescaled in tensor memory only when
 //              a tile's max exceeds the reference max by more than 2^8, so every P stays <= 256),
-//              write P, and finally write O.
+//              write P, and finally write O (one split) or send it to the cluster merge.
 // The value tile is read by the PV product as an MN-major operand of the same swizzled storage.
 // With several splits, the splits of a (unit, half) form a thread-block cluster: each CTA sends
 // its O rows and (max, sum) straight from tensor memory to the CTA that owns those heads (its
@@ -54,7 +54,6 @@ constexpr int MAX_TOK = 512;                        // tokens per CTA (their poo
 constexpr int MAX_SPLIT = 8;                        // CTAs per cluster (portable limit)
 constexpr int SOFT = 128;
 constexpr int THREADS = SOFT0 * 32 + SOFT;
-constexpr int NWARPS = THREADS / 32;
 constexpr int OFF_TILES = QS_BYTES;
 constexpr int OFF_ROWS = OFF_TILES + STAGES * TILE;
 constexpr int OFF_BAR = OFF_ROWS + MAX_TOK * 4;
