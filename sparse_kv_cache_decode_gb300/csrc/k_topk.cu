@@ -131,10 +131,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(Dims d, const 
                                                                   uint32_t* __restrict__ ckey, int* __restrict__ cidx,
                                                                   int* __restrict__ ccnt) {
   kvs_pdl_entry();
-  extern __shared__ uint32_t skeys[];
-  __shared__ int hist[256];
-  __shared__ int ws[33];
-  __shared__ int pick[2];
+  extern __shared__ uint32_t skeys[];                   // [kChunk] keys, then the threshold-guess scratch
+  __shared__ TopkShared sh;
   const int c = blockIdx.x, u = blockIdx.y;
   const int tid = threadIdx.x;
   const int len = ctx_len[u / d.Hkv];
@@ -156,7 +154,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(Dims d, const 
   }
   for (int i = tid; i < n; i += blockDim.x) skeys[i] = score_key(s[i]);
   __syncthreads();
-  select_ordered(skeys, n, k, hist, ws, pick, [&](int r, int i) {
+  select_topk(skeys, n, k, skeys + kChunk, sh, [&](int r, int i) {
     okey[r] = skeys[i];
     oidx[r] = b0 + i;
   });
@@ -171,10 +169,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(Dims d, const 
                                                                   const int* __restrict__ ccnt, int* __restrict__ sel,
                                                                   int* __restrict__ nsel, unsigned* err) {
   kvs_pdl_entry();
-  extern __shared__ uint32_t smem[];
-  __shared__ int hist[256];
-  __shared__ int ws[33];
-  __shared__ int pick[2];
+  extern __shared__ uint32_t smem[];                    // [P * Kb] keys, [P * Kb] blocks, guess scratch
+  __shared__ TopkShared sh;
   __shared__ int off[kTopkMaxChunks + 1];
   const int u = blockIdx.x;
   const int tid = threadIdx.x, NT = blockDim.x;
@@ -224,7 +220,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_merge_kernel(Dims d, const 
     if (n == k) {
       for (int i = tid; i < n; i += NT) out[d.n_sink + i] = idx[i];
     } else {
-      select_ordered(keys, n, k, hist, ws, pick, [&](int r, int i) { out[d.n_sink + r] = idx[i]; });
+      select_topk(keys, n, k, smem + (size_t)2 * P * d.Kb, sh, [&](int r, int i) { out[d.n_sink + r] = idx[i]; });
     }
   }
   if (tid == 0) nsel[u] = d.Kb;
@@ -244,18 +240,20 @@ cudaError_t launch_topk(const Dims& d, const float* scores, const int* ctx_len, 
                         cudaStream_t s, const TopkScratch* scratch) {
   const int P = scratch ? topk_chunks(d) : 0;
   if (P > 0) {
+    // each kernel's keys plus the scratch of the threshold guess (kTopkFastScratch words)
+    const size_t chunk_smem = (kChunk + kTopkFastScratch) * sizeof(uint32_t);
+    const size_t merge_smem = (size_t)P * d.Kb * 8 + kTopkFastScratch * sizeof(uint32_t);
     {
-      cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(topk_chunk_kernel),
-                                           (int)(kChunk * sizeof(uint32_t)));
-      if (e == cudaSuccess) e = set_max_dynamic_smem(reinterpret_cast<const void*>(topk_merge_kernel), (int)kTopkMergeSmemMax);
+      cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(topk_chunk_kernel), (int)chunk_smem);
+      if (e == cudaSuccess) e = set_max_dynamic_smem(reinterpret_cast<const void*>(topk_merge_kernel), (int)merge_smem);
       if (e != cudaSuccess) return e;
     }
-    launch_pdl(topk_chunk_kernel, dim3(dim3(P, d.U)), dim3(kTopkThreads), kChunk * sizeof(uint32_t), s, d, scores, ctx_len, P, scratch->key,
-                                                                                  scratch->idx, scratch->cnt);
+    launch_pdl(topk_chunk_kernel, dim3(dim3(P, d.U)), dim3(kTopkThreads), chunk_smem, s, d, scores, ctx_len, P,
+               scratch->key, scratch->idx, scratch->cnt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    launch_pdl(topk_merge_kernel, dim3(d.U), dim3(kTopkThreads), (size_t)P * d.Kb * 8, s, d, ctx_len, P, scratch->key, scratch->idx,
-                                                                     scratch->cnt, sel, nsel, err);
+    launch_pdl(topk_merge_kernel, dim3(d.U), dim3(kTopkThreads), merge_smem, s, d, ctx_len, P, scratch->key,
+               scratch->idx, scratch->cnt, sel, nsel, err);
     return cudaGetLastError();
   }
   size_t smem = (size_t)kTopkSmemKeys * sizeof(uint32_t);

@@ -134,7 +134,7 @@ struct TopkShared {
 };
 
 constexpr int kTopkSample = 256;       // sampled keys of the threshold guess
-constexpr int kTopkFastMax = 1024;     // keys at or above the guess kept for the exact selection
+constexpr int kTopkFastMax = 4096;     // keys at or above the guess kept for the exact selection
 constexpr int kTopkFastScratch = kTopkSample + 2 * kTopkFastMax;   // 32-bit words of shared scratch
 
 // select_ordered, fronted by a threshold guess when the keys are many: T0 = a sampled key of rank
