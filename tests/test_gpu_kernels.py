@@ -167,6 +167,36 @@ def _threshold_dup_scores(seed, n, k, mode):
     return s
 
 
+def test_topk_two_phase_guess_falls_back_bit_exact():
+    """Two-phase top-K whose unit-wide threshold guess is too high: the scores at the guess's
+    evenly spaced sample positions are large and every other score is small, so fewer than k kept
+    keys reach the guess and the merge selects again from the scores in global memory."""
+    lens, budget = [131072, 131072 - 77], 2048
+    w = W.TINY.with_(name="topk_fallback", n_req=len(lens), ctx0=max(lens), budget_blocks=budget, n_sink=0,
+                     n_recent=0, cap_blocks=budget, n_heavy=0, n_layer=1, block_size=1)
+    g = GpuCase(w, lens)
+    nbm = g.nb_max
+    host = np.zeros((w.n_req, w.n_kv_head, nbm), np.float32)
+    for r, L in enumerate(lens):
+        for h in range(w.n_kv_head):
+            s = W.uniform_f32(41 + r * 7 + h, 13, nbm, -1.0, 0.0)
+            # the guess samples position i * L / 4096 of the unit's L candidates
+            samp = (np.arange(4096, dtype=np.int64) * L) // 4096
+            s[samp] = 10.0 + W.uniform_f32(42 + r * 7 + h, 14, 4096, 0.0, 1.0)
+            host[r, h] = s
+    scores = torch.from_numpy(host).cuda()
+    sel = torch.full((w.n_req, w.n_kv_head, budget), -7, dtype=torch.int32, device="cuda")
+    nsel = torch.zeros((w.n_req, w.n_kv_head), dtype=torch.int32, device="cuda")
+    g.ctx.topk_select(scores, g.ctx_len, sel, nsel)
+    gs, gn = sel.cpu().numpy(), nsel.cpu().numpy()
+    for r, L in enumerate(lens):
+        for h in range(w.n_kv_head):
+            ref = select_blocks(host[r, h], _nb(L, 1), budget, 0, 0)
+            assert gn[r, h] == len(ref)
+            np.testing.assert_array_equal(gs[r, h, :len(ref)], ref, err_msg=f"unit {(r, h)}")
+    assert g.ctx.poll_error() == 0
+
+
 @pytest.mark.parametrize("mode", ["fine", "spread"])
 def test_topk_select_threshold_ties_bit_exact(mode):
     lens, budget, sink, recent = [32768, 20000, 7001], 128, 1, 2
