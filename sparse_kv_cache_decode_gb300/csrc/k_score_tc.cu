@@ -29,7 +29,10 @@ constexpr int kChunkBytes = kTileM * kChunk * 2;  // 16 KiB
 constexpr int kThreads = 192;
 constexpr int kEpiWarps = 4;
 constexpr int kMaxSmem = 227 * 1024;
-constexpr int kSmemLeft = 8 * 1024;               // left free on the SM for a concurrent fetch CTA
+// No shared memory is kept free for a concurrent fetch CTA: with 128 scoring rows of 576 dims the
+// staged rows leave room for 4 or 5 ring stages, and the fifth is worth more (per 16-layer MLA
+// step, 3 / 4 / 5 stages: 7.89 / 7.21 / 7.13 ms of scoring, 0.72 / 0.79 / 0.80 of HBM).
+constexpr int kSmemLeft = 0;
 
 struct TcPlan {
   int n_rows, n_pad, kc, stages, q_bytes, tiles_per_unit, ctas_per_unit, per_cta, n_cta, tmem_cols, smem;
