@@ -37,6 +37,13 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# The step runs on several streams (compute, copy, selection) and as a CUDA graph whose branches
+# run concurrently; all of them map onto the context's hardware work queues, 8 by default.  More
+# queues keep the copy-stream fetch from sharing one with the compute stream (where it would wait
+# behind the layer kernels).  Read when CUDA initialises, so it is set before torch touches it;
+# children inherit it.
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
+
 import numpy as np  # noqa: E402
 
 import workload as W  # noqa: E402
