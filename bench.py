@@ -227,6 +227,15 @@ def _time_ms(fn, reps=3):
     return best
 
 
+def burst_fit(bursts):
+    """Least-squares line through (bytes, microseconds) points of host-link bursts: time = fixed
+    cost + bytes / streaming rate.  Returns (fixed cost in us, streaming rate in GB/s)."""
+    x = np.array([b for b, _ in bursts], dtype=np.float64)
+    y = np.array([t for _, t in bursts], dtype=np.float64)
+    slope, icpt = np.polyfit(x, y, 1)
+    return float(icpt), float(1e-3 / slope)
+
+
 def link_peaks(K, host_tensors):
     """The host link measured three ways; the largest is the link peak of the step roofline.
       ce_pinned   copy engine, 1 GiB of cudaHostAlloc memory -> device
@@ -269,12 +278,10 @@ def link_peaks(K, host_tensors):
         offs = rnd[:nit] if nit <= rnd.numel() else rnd
         ms = _time_ms(lambda: K.probe_host_read(hist, region, offs, item, 152, 128, sink))
         bursts.append((offs.numel() * item, ms * 1e3))
-    x = np.array([b for b, _ in bursts], dtype=np.float64)
-    y = np.array([t for _, t in bursts], dtype=np.float64)
-    slope, icpt = np.polyfit(x, y, 1)
+    fixed_us, stream_gbs = burst_fit(bursts)
     out["bursts"] = [{"mb": round(b / 1e6, 2), "us": round(t, 1), "gbs": round(b / (t * 1e-6) / 1e9, 1)} for b, t in bursts]
-    out["burst_fixed_us"] = round(float(icpt), 1)
-    out["burst_stream_gbs"] = round(float(1e-3 / slope), 1)
+    out["burst_fixed_us"] = round(fixed_us, 1)
+    out["burst_stream_gbs"] = round(stream_gbs, 1)
     torch.cuda.synchronize()
     if int(sink[1].item()) != 0:
         raise RuntimeError("link probe skipped items")
