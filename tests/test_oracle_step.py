@@ -32,6 +32,25 @@ def test_budget_covering_context_is_dense_attention():
             assert recs[(0, 0, h)].sel.tolist() == list(range(63))
 
 
+def test_mla_budget_covering_context_is_dense_attention_over_the_latent():
+    """MLA reading: every q head attends over the full latent row as K and its first d_v entries
+    as V (one latent head shared by all 16 q heads); with the budget above the context the step is
+    dense attention, so a wrong value slice, head mapping or scale fails here."""
+    w = W.TINY_MLA.with_(name="mla_dense", ctx0=200, steps=3)            # bs 1: 200 blocks <= K_b 256
+    k, _ = W.kv_numpy(w)
+    dec = OracleDecoder(w, k, None, [w.ctx0])
+    qs = W.QueryStream(w)
+    assert w.softmax_scale == float(np.float32(1.0 / 24.0))             # 1 / sqrt(576), held in fp32
+    for t in range(2):
+        q = qs.queries(t)
+        out, recs = dec.step(q)
+        lat = k[0, 0, 0, : w.ctx0]
+        ref = _sdpa(q[0, 0], lat, lat[:, : w.d_v], w.softmax_scale)
+        assert out.shape[-1] == 512
+        np.testing.assert_allclose(out[0, 0], ref, atol=1e-6, rtol=0)
+        assert recs[(0, 0, 0)].sel.tolist() == list(range(w.ctx0))
+
+
 def test_ragged_tail_and_capacity_do_not_change_outputs():
     w = SMALL.with_(ctx0=1000)
     k, v = W.kv_numpy(w)
