@@ -1,5 +1,8 @@
 """Pins for oracle.step: dense equivalence (torch SDPA), append, prefetch and lookahead properties."""
+import math
+
 import numpy as np
+import pytest
 import torch
 
 import workload as W
@@ -49,6 +52,45 @@ def test_mla_budget_covering_context_is_dense_attention_over_the_latent():
         assert out.shape[-1] == 512
         np.testing.assert_allclose(out[0, 0], ref, atol=1e-6, rtol=0)
         assert recs[(0, 0, 0)].sel.tolist() == list(range(w.ctx0))
+
+
+def _brute_selection(rows, ik, nb, budget, n_sink, n_recent, scale):
+    """Sink + recent + the best of the rest, each block scored as the largest scaled dot product
+    over the given query rows (exact sums), ties to the lower block; ascending block ids."""
+    rows64 = [bf16_to_f32(r).astype(np.float64) for r in rows]
+    keys64 = [bf16_to_f32(k).astype(np.float64) for k in ik]
+    score = [np.float32(scale * max(math.fsum(a * b for a, b in zip(r, keys64[blk])) for r in rows64))
+             for blk in range(nb)]
+    if nb <= budget:
+        return list(range(nb))
+    forced = set(range(min(n_sink, nb))) | set(range(max(0, nb - n_recent), nb))
+    rest = sorted((blk for blk in range(nb) if blk not in forced), key=lambda blk: (-score[blk], blk))
+    return sorted(forced | set(rest[: budget - len(forced)]))
+
+
+@pytest.mark.parametrize("lookahead", [False, True])
+def test_selection_scores_each_kv_head_with_its_own_group_and_every_draft(lookahead):
+    """Scoring rows of kv head h are q heads [h G, (h + 1) G) (contiguous groups), and in lookahead
+    mode those heads of every draft; checked against a brute-force selection on a ragged 300-token
+    context (19 blocks, budget 8 = 1 sink + 2 recent + 5 scored)."""
+    base = W.TINY_LOOKAHEAD if lookahead else W.TINY
+    w = base.with_(name="sel_rows", ctx0=300, steps=3, budget_blocks=8, cap_blocks=12)
+    k, v = W.kv_numpy(w)
+    dec = OracleDecoder(w, k, v, [w.ctx0])
+    qs = W.QueryStream(w)
+    g, nb = w.group, 19
+    for t in range(2):
+        q = qs.queries(t)
+        d = qs.drafts(t) if lookahead else None
+        _, recs = dec.step(q, d)
+        for h in range(w.n_kv_head):
+            ik = index_keys(k[0, 0, h], w.ctx0, w.block_size)
+            if lookahead:
+                rows = [d[0, 0, j, hq] for j in range(w.n_draft) for hq in range(h * g, (h + 1) * g)]
+            else:
+                rows = [q[0, 0, hq] for hq in range(h * g, (h + 1) * g)]
+            want = _brute_selection(rows, ik, nb, w.budget_blocks, w.n_sink, w.n_recent, w.softmax_scale)
+            assert recs[(0, 0, h)].sel.tolist() == want, (t, h)
 
 
 def test_ragged_tail_and_capacity_do_not_change_outputs():
