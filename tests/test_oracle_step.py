@@ -35,21 +35,23 @@ def test_budget_covering_context_is_dense_attention():
             assert recs[(0, 0, h)].sel.tolist() == list(range(63))
 
 
-def test_each_request_attends_over_its_own_length():
-    """Two requests of different lengths (1000 and 517 tokens: 63 and 33 blocks, budget 64): each
-    one's output is dense attention over its own tokens only."""
-    w = SMALL.with_(name="two_req", n_req=2, budget_blocks=64, cap_blocks=64)
+def test_each_request_and_layer_attends_over_its_own_tokens():
+    """Two layers and two requests of different lengths (1000 and 517 tokens: 63 and 33 blocks,
+    budget 64): each (layer, request) output is dense attention over that layer's and request's
+    own tokens only."""
+    w = SMALL.with_(name="two_req", n_req=2, n_layer=2, budget_blocks=64, cap_blocks=64)
     k, v = W.kv_numpy(w)
     lens = [1000, 517]
     dec = OracleDecoder(w, k, v, lens)
     q = W.QueryStream(w).queries(0)
     out, recs = dec.step(q)
-    for r, n in enumerate(lens):
-        for h in range(w.n_kv_head):
-            heads = slice(h * w.group, (h + 1) * w.group)
-            ref = _sdpa(q[0, r, heads], k[0, r, h, :n], v[0, r, h, :n], w.softmax_scale)
-            np.testing.assert_allclose(out[0, r, heads], ref, atol=1e-6, rtol=0)
-            assert recs[(0, r, h)].sel.tolist() == list(range((n + 15) // 16))
+    for l in range(2):
+        for r, n in enumerate(lens):
+            for h in range(w.n_kv_head):
+                heads = slice(h * w.group, (h + 1) * w.group)
+                ref = _sdpa(q[l, r, heads], k[l, r, h, :n], v[l, r, h, :n], w.softmax_scale)
+                np.testing.assert_allclose(out[l, r, heads], ref, atol=1e-6, rtol=0)
+                assert recs[(l, r, h)].sel.tolist() == list(range((n + 15) // 16))
 
 
 def test_mla_budget_covering_context_is_dense_attention_over_the_latent():
