@@ -146,6 +146,28 @@ def test_append_updates_last_block_key_and_length():
             assert nb - 1 in dec.records[(0, 0, h)].sel
 
 
+def test_query_attends_to_the_token_appended_with_it():
+    """Reading 14: the query of a step attends to [0, L) after that step's append, its own token
+    included; with the budget above the context the output is dense attention over all of them."""
+    w = SMALL.with_(name="append_dense", append=True, ctx0=1000, steps=4, budget_blocks=64, cap_blocks=64)
+    k, v = W.kv_numpy(w)
+    dec = OracleDecoder(w, k, v, [w.ctx0])
+    qs = W.QueryStream(w)
+    full_k, full_v = k.copy(), v.copy()
+    for t in range(3):
+        nk, nv = W.token(w, w.ctx0 + t)
+        full_k[:, :, :, w.ctx0 + t], full_v[:, :, :, w.ctx0 + t] = nk, nv
+        q = qs.queries(t)
+        out, _ = dec.step(q, new_k=nk, new_v=nv)
+        L = w.ctx0 + t + 1
+        for h in range(w.n_kv_head):
+            heads = slice(h * w.group, (h + 1) * w.group)
+            ref = _sdpa(q[0, 0, heads], full_k[0, 0, h, :L], full_v[0, 0, h, :L], w.softmax_scale)
+            np.testing.assert_allclose(out[0, 0, heads], ref, atol=1e-6, rtol=0)
+            without = _sdpa(q[0, 0, heads], full_k[0, 0, h, : L - 1], full_v[0, 0, h, : L - 1], w.softmax_scale)
+            assert np.abs(without - ref).max() > 1e-4        # the new token is not negligible here
+
+
 def test_prefetch_never_changes_outputs():
     w = SMALL.with_(n_layer=3, layer_prefetch=True, rho_layer=0.8, cap_blocks=14)
     k, v = W.kv_numpy(w)
