@@ -245,7 +245,13 @@ kvs_status kvs_join(kvs_ctx* ctx, kvs_stream_t stream);
  * is the least recently used slot that is empty or (stamp < 2*clock and holds no hint block);
  * it is mapped, fetched from host and stamped 2*clock + 1.  Call it before dst_layer's update
  * of the same step; it may run on another stream: it waits for the top-K of the layer below made
- * by kvs_decode_step, and kvs_decode_step(dst_layer) waits for it before its update. */
+ * by kvs_decode_step, and kvs_decode_step(dst_layer) waits for it before its update.
+ * It pays only where the layer below's selection foretells this layer's new blocks [HISP insight
+ * 3: enable it for selectors that share choices across layers, off otherwise].  Hint blocks this
+ * layer never selects are not resident, so they are fetched again at every step, into slots the
+ * previous step left unused, which are the ones that give hits when a selection drifts back: the
+ * device counters prefetched / prefetch_hits show which case a workload is in, and a smaller
+ * max_prefetch bounds the cost. */
 kvs_status kvs_layer_prefetch(kvs_ctx* ctx, int dst_layer, const int* d_hint_sel, const int* d_hint_nsel,
                               const int* d_ctx_len, kvs_stats* d_stats, kvs_stream_t stream);
 
