@@ -127,3 +127,17 @@ def test_burst_fit_recovers_fixed_cost_and_rate():
     fixed, rate = b.burst_fit(pts)
     assert fixed == pytest.approx(14.0, abs=1e-6)
     assert rate == pytest.approx(210.5, rel=1e-9)
+
+
+def test_profile_commands_run_committed_files_only():
+    """Each ncu summary under profiles/ gives the command that made it; the scripts it runs must
+    be files of this repository (not scratch copies)."""
+    pdir = os.path.join(ROOT, "profiles")
+    seen = 0
+    for f in sorted(os.listdir(pdir)):
+        text = open(os.path.join(pdir, f)).read()
+        assert "_work/" not in text, f
+        for script in re.findall(r"python3?\s+([\w./-]+\.py)", text):
+            assert os.path.isfile(os.path.join(ROOT, script)), (f, script)
+            seen += 1
+    assert seen >= 5
