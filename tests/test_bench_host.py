@@ -1,7 +1,8 @@
 """bench.py's host-side helpers that feed the reported figures: the committed ncu traffic lookup
 (a figure is used only for the kernel source it was taken from), the step-to-step selection
-overlap, the clock summary that decides whether a run is kept, and the fit of the host link's
-burst cost.  Every expected value below is worked out by hand."""
+overlap, the clock summary that decides whether a run is kept, the fit of the host link's burst
+cost, and that the profile summaries' commands run committed scripts.  Every expected value below
+is worked out by hand."""
 import hashlib
 import importlib.util
 import os
